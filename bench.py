@@ -1,0 +1,424 @@
+#!/usr/bin/env python3
+"""Benchmark: attention forward + backward TFLOPS on one GB300 (or N replicas).
+
+One step = the whole hot path over one batch of synthetic input: the forward
+(work list, fused attention kernel) and the backward (work list, preprocess
+D = rowsum(dO * O), fused dK/dV-stationary kernel with dQ accumulation, dQ
+conversion), for the workload named by --workload (default: B=2, H=16,
+S=8192, D=128, bf16, no mask).
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on
+the launching stream; between timed steps a 512 MiB buffer is written to flush
+L2 (outside the events).  Work counted is algorithmic: 4*D FLOPs per unmasked
+(query, key) pair per head forward, 10*D backward.
+
+Prints ONE JSON line (rank 0).  --impl reference times the float64 CPU oracle
+instead, on a bounded sample of the same workload, on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def peak_value(peaks, key):
+    """Find a peak by key in a possibly nested MEASURED_PEAKS.json."""
+    if key in peaks and isinstance(peaks[key], (int, float)):
+        return float(peaks[key])
+    for v in peaks.values():
+        if isinstance(v, dict):
+            r = peak_value(v, key)
+            if r is not None:
+                return r
+    return None
+
+
+def flops_of(wl, bm=None):
+    from bwd_flashattention_fwd_sm_gb300 import workloads as W
+    pairs = W.unmasked_pairs(wl, bm)
+    heads = wl.heads_q
+    fwd = 4.0 * wl.head_dim * pairs * heads
+    bwd = 10.0 * wl.head_dim * pairs * heads
+    return fwd, bwd, pairs
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id is not None:
+            cmd.insert(1, f"--id={self.gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_identity(torch):
+    try:
+        uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        return uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+    except Exception:
+        return os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or None
+
+
+def run_ours(args, wl, rank, world, dist):
+    import ctypes
+
+    import torch
+
+    from bwd_flashattention_fwd_sm_gb300 import BlockMask, SeqLens, attn_bwd, attn_fwd, get_status, make_params
+    from bwd_flashattention_fwd_sm_gb300 import _lib
+    from bwd_flashattention_fwd_sm_gb300 import workloads as W
+
+    lib = _lib.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = W.make_inputs(wl)
+    bm = inp.get("block_mask")
+    fwd_flops, bwd_flops, pairs = flops_of(wl, bm)
+    kw = {"scale": wl.scale}
+    if wl.mask == "causal":
+        kw["causal"] = True
+    if bm is not None:
+        kw["block_mask"] = BlockMask.from_csr(bm, device=dev)
+    if wl.varlen:
+        kw["seqlens"] = SeqLens(inp["cu_seqlens"], device=dev)
+        kw["seqlen"] = wl.seqlen
+    q, k, v, do = (inp[n].to(dev) for n in ("q", "k", "v", "do"))
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # Workspaces allocated once; every call reuses them.
+    o, lse = attn_fwd(q, k, v, **kw)
+    p = make_params(q, k, **kw)
+    ws_f = torch.empty(max(1, lib.attn_fwd_workspace_size(ctypes.byref(p))), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(max(1, lib.attn_bwd_workspace_size(ctypes.byref(p))), dtype=torch.uint8, device=dev)
+
+    def step():
+        o, lse = attn_fwd(q, k, v, workspace=ws_f, **kw)
+        dq, dk, dv = attn_bwd(q, k, v, o, do, lse, workspace=ws_b, **kw)
+        return o, lse, dq, dk, dv
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    step_ev = [(ev(), ev()) for _ in range(args.steps)]
+    fwd_ev = [(ev(), ev()) for _ in range(args.steps)]
+    bwd_ev = [(ev(), ev()) for _ in range(args.steps)]
+    clocks = ClockSampler(gpu_identity(torch)) if rank == 0 else None
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        lib.attn_set_timing_events(0, ctypes.c_void_p(fwd_ev[i][0].cuda_event), ctypes.c_void_p(fwd_ev[i][1].cuda_event))
+        lib.attn_set_timing_events(1, ctypes.c_void_p(bwd_ev[i][0].cuda_event), ctypes.c_void_p(bwd_ev[i][1].cuda_event))
+        step_ev[i][0].record(stream)
+        step()
+        step_ev[i][1].record(stream)
+    lib.attn_set_timing_events(0, None, None)
+    lib.attn_set_timing_events(1, None, None)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    status = get_status()
+    if status != 0:
+        raise RuntimeError(f"device status word set during the benchmark: {status}")
+
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    fwd_ms = [a.elapsed_time(b) for a, b in fwd_ev]
+    bwd_ms = [a.elapsed_time(b) for a, b in bwd_ev]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    step_flops = fwd_flops + bwd_flops
+    value = world * step_flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # End to end through the public API with host buffers: pinned inputs copied
+    # in, outputs copied back, every step.
+    host_in = {n: inp[n].pin_memory() for n in ("q", "k", "v", "do")}
+    host_out = None
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+
+    def e2e_step():
+        nonlocal host_out
+        dq_, dk_, dv_ = None, None, None
+        qd, kd, vd, dod = (host_in[n].to(dev, non_blocking=True) for n in ("q", "k", "v", "do"))
+        o_, lse_ = attn_fwd(qd, kd, vd, workspace=ws_f, **kw)
+        dq_, dk_, dv_ = attn_bwd(qd, kd, vd, o_, dod, lse_, workspace=ws_b, **kw)
+        outs = (o_, lse_, dq_, dk_, dv_)
+        if host_out is None:
+            host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        for h, d in zip(host_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(1, min(args.steps, 5))
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    e2e_value = world * step_flops * e2e_steps / e2e_s / 1e12
+
+    peaks, peak_src = load_peaks()
+    peak = peak_value(peaks, "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
+    bwd_avg = sum(bwd_ms) / len(bwd_ms)
+    fwd_avg = sum(fwd_ms) / len(fwd_ms)
+    achieved = bwd_flops / (bwd_avg * 1e-3) / 1e12
+    fwd_ach = fwd_flops / (fwd_avg * 1e-3) / 1e12
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        try:
+            with open(prof) as f:
+                t = json.load(f)
+            if t.get("workload") == wl.name and t.get("kernel_build") == kernel_build_id():
+                traffic = t.get("bwd_main_bytes")
+        except Exception:
+            traffic = None
+    launches_per_step = 2 + 4 + (1 if wl.mask == "block" else 0)
+
+    line = {
+        "metric": "attention fwd+bwd TFLOPS (bf16, D=128, S=8192) and % of GB300 BF16 tensor peak",
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic: Q,K,V,dO iid N(0,1) from a fixed seed, rounded to bf16",
+        "config": {
+            "workload": wl.name,
+            "batch": wl.batch, "heads_q": wl.heads_q, "heads_kv": wl.heads_kv, "seq_len": wl.seqlen,
+            "head_dim": wl.head_dim, "mask": wl.mask, "varlen": wl.varlen,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "512 MiB L2 flush written between timed steps (outside the step events)",
+            "fwd_flops": fwd_flops, "bwd_flops": bwd_flops,
+        },
+        "fwd_ms": round(fwd_avg, 4), "bwd_ms": round(bwd_avg, 4),
+        "fwd_tflops": round(fwd_ach, 2), "bwd_tflops": round(achieved, 2),
+        "fwd_frac_of_peak": round(fwd_ach / peak, 4), "bwd_frac_of_peak": round(achieved / peak, 4),
+        "roofline": {
+            "kernel": "backward main (dK/dV-stationary, dQ accumulation)",
+            "bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "peak_source": f"{peak_src} bf16 dense" + (" (MEASURED_PEAKS.json)" if peak_src == "measured" else
+                                                        " (no MEASURED_PEAKS.json: 1.9 PFLOP/s burst)"),
+        },
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    return line
+
+
+def kernel_build_id():
+    try:
+        from bwd_flashattention_fwd_sm_gb300 import build as B
+        return B._stamp([])[:16]
+    except Exception:
+        return None
+
+
+def cpu_baseline(wl, budget_s=20.0, rank=0):
+    """The float64 oracle on a bounded sample of the workload: whole heads at full length."""
+    import oracle
+    from bwd_flashattention_fwd_sm_gb300 import workloads as W
+
+    inp = W.make_inputs(wl)
+    cores = os.cpu_count() or 1
+    kw = {"scale": wl.scale}
+    if wl.mask == "causal":
+        kw["causal"] = True
+    if wl.mask == "block":
+        kw["block_mask"] = inp["block_mask"]
+    if wl.varlen:
+        cu = inp["cu_seqlens"]
+        sel = lambda t, h: t[:, h:h + 1]
+        kw["cu_seqlens"] = cu
+    else:
+        sel = lambda t, h: t[0:1, h:h + 1]
+    fwd_flops, bwd_flops, pairs = flops_of(wl, inp.get("block_mask"))
+    per_head = (fwd_flops + bwd_flops) / wl.heads_q / (1 if wl.varlen else wl.batch)
+    heads_done, flops_done = 0, 0.0
+    t0 = time.perf_counter()
+    while True:
+        h = heads_done % wl.heads_q
+        G = wl.heads_q // wl.heads_kv
+        q, do = (sel(inp[n], h).double().numpy() for n in ("q", "do"))
+        k, v = (sel(inp[n], h // G).double().numpy() for n in ("k", "v"))
+        oracle.attn_fwd(q, k, v, **kw)
+        oracle.attn_bwd(q, k, v, do, **kw)
+        heads_done += 1
+        flops_done += per_head
+        if time.perf_counter() - t0 >= budget_s * 0.5 or heads_done >= 4:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": flops_done / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{heads_done} head(s) of {wl.name} at full length (fwd+bwd, float64), {dt:.1f} s",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args, wl):
+    """Reference arm: the float64 oracle as it stands, on the host cores."""
+    fwd_flops, bwd_flops, _ = flops_of(wl)
+    per_step = []
+    base = None
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(wl, budget_s=6.0)
+        if i >= args.warmup:
+            per_step.append(r)
+        base = r
+    value = statistics.mean(r["value"] for r in per_step)
+    line = {
+        "metric": "attention fwd+bwd TFLOPS (bf16, D=128, S=8192) and % of GB300 BF16 tensor peak",
+        "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.mean(r["seconds"] for r in per_step) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: Q,K,V,dO iid N(0,1) from a fixed seed, rounded to bf16",
+        "config": {"workload": wl.name, "batch": wl.batch, "heads_q": wl.heads_q, "heads_kv": wl.heads_kv,
+                   "seq_len": wl.seqlen, "head_dim": wl.head_dim, "mask": wl.mask,
+                   "sample": "each step: whole heads at full length, bounded to a few seconds"},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": base["cores"], "kind": "oracle",
+                         "sample": base["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="h0_dense_s8192")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    from bwd_flashattention_fwd_sm_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, wl)), flush=True)
+        return 0
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    line = run_ours(args, wl, rank, world, dist)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

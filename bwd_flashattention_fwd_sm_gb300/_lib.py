@@ -1,0 +1,123 @@
+"""ctypes view of libgbattn.so: the structures and entry points of include/gbattn.h.
+
+Argument marshalling only.  Loading fails loudly if the library cannot be
+built or found; there is no other implementation to fall back to.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_WORKSPACE = 3
+ATTN_ERR_CUDA = 4
+ATTN_ERR_DEVICE_TIMEOUT = 5
+ATTN_ERR_DEVICE_BOUNDS = 6
+
+ATTN_F32 = 0
+ATTN_BF16 = 1
+
+ATTN_MASK_NONE = 0
+ATTN_MASK_CAUSAL = 1
+ATTN_MASK_BLOCK = 2
+
+SIZE_MAX = ctypes.c_size_t(-1).value
+
+I32P = ctypes.POINTER(ctypes.c_int32)
+
+
+class BlockMaskC(ctypes.Structure):
+    _fields_ = [
+        ("row_ptr", ctypes.c_void_p),
+        ("col_idx", ctypes.c_void_p),
+        ("row_ptr_host", ctypes.c_void_p),
+        ("col_idx_host", ctypes.c_void_p),
+        ("block_q", ctypes.c_int32),
+        ("block_k", ctypes.c_int32),
+        ("n_row_blocks", ctypes.c_int32),
+        ("n_col_blocks", ctypes.c_int32),
+        ("nnz", ctypes.c_int32),
+        ("causal_in_block", ctypes.c_int32),
+    ]
+
+
+class ParamsC(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32),
+        ("heads_q", ctypes.c_int32),
+        ("heads_kv", ctypes.c_int32),
+        ("seqlen", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("cu_seqlens", ctypes.c_void_p),
+        ("cu_seqlens_host", ctypes.c_void_p),
+        ("n_seqs", ctypes.c_int32),
+        ("q_stride_b", ctypes.c_int64),
+        ("q_stride_h", ctypes.c_int64),
+        ("q_stride_s", ctypes.c_int64),
+        ("kv_stride_b", ctypes.c_int64),
+        ("kv_stride_h", ctypes.c_int64),
+        ("kv_stride_s", ctypes.c_int64),
+        ("scale", ctypes.c_float),
+        ("dtype", ctypes.c_int32),
+        ("mask", ctypes.c_int32),
+        ("block_mask", ctypes.POINTER(BlockMaskC)),
+    ]
+
+
+# Every symbol include/gbattn.h declares, with its ctypes signature.
+_VP = ctypes.c_void_p
+_PP = ctypes.POINTER(ParamsC)
+SIGNATURES = {
+    "attn_fwd_workspace_size": (ctypes.c_size_t, [_PP]),
+    "attn_bwd_workspace_size": (ctypes.c_size_t, [_PP]),
+    "attn_fwd": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
+    "attn_bwd": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
+    "attn_get_status": (ctypes.c_int, [_VP]),
+    "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "attn_last_error": (ctypes.c_char_p, []),
+    "attn_set_timing_events": (ctypes.c_int, [ctypes.c_int, _VP, _VP]),
+    "attn_version": (ctypes.c_char_p, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libgbattn.so (building it first if needed) and set up signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build() if build_if_missing else _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libgbattn.so not found at {path}; build it with bwd_flashattention_fwd_sm_gb300.build")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str, detail: str = ""):
+        self.code = code
+        name = load().attn_status_string(code).decode()
+        super().__init__(f"{where}: {name}" + (f" ({detail})" if detail else ""))
+
+
+def check(code: int, where: str) -> None:
+    if code != ATTN_OK:
+        raise AttnError(code, where, load().attn_last_error().decode())

@@ -1,0 +1,15 @@
+// Tensor-core (tcgen05 / TMEM / TMA) attention kernels for sm_103a.
+#pragma once
+
+#include "common.cuh"
+
+namespace gbattn {
+
+// True when this build carries the tensor-core kernels.
+bool tc_available();
+
+// bf16, head_dim 128.  Work list of 128-row units already built in p.units.
+cudaError_t launch_tc_fwd(const KParams& p, int sms, cudaStream_t st);
+cudaError_t launch_tc_bwd(const KParams& p, int sms, cudaStream_t st);
+
+}  // namespace gbattn

@@ -59,14 +59,6 @@ namespace {
 
 const double kNegInf = -std::numeric_limits<double>::infinity();
 
-struct Seq {
-  int64_t q_row0;   // first row of this sequence in the q/o tensors (in units of rows of D)
-  int64_t kv_row0;  // same for k/v
-  int64_t lse0;     // first LSE element
-  int64_t q_rstride, kv_rstride, lse_rstride;  // distance between consecutive positions
-  int32_t len;
-};
-
 // Position i may attend to position j (both relative to the sequence start).
 bool keep(const oracle_params_t* p, int i, int j, int len) {
   if (j < 0 || j >= len) return false;
@@ -83,12 +75,6 @@ bool keep(const oracle_params_t* p, int i, int j, int len) {
   }
   return true;
 }
-
-// Location of (sequence n, head h) inside the flat arrays.
-// Returns the element offset of position 0 and the per-position stride.
-struct HeadView {
-  int64_t base, rstride;
-};
 
 int n_sequences(const oracle_params_t* p) { return p->cu_seqlens ? p->n_seqs : p->batch; }
 
@@ -115,6 +101,20 @@ double dot(const double* a, const double* b, int d) {
   double s = 0.0;
   for (int t = 0; t < d; ++t) s += a[t] * b[t];
   return s;
+}
+
+// Rows per work item (rows of one head are independent in the forward and in
+// the per-row pass of the backward; keys are independent in the per-key pass).
+const int kRowChunk = 64;
+
+int row_chunks(const oracle_params_t* p) {
+  int maxlen = p->seqlen;
+  if (p->cu_seqlens)
+    for (int n = 0; n < p->n_seqs; ++n) {
+      const int L = p->cu_seqlens[n + 1] - p->cu_seqlens[n];
+      if (L > maxlen) maxlen = L;
+    }
+  return maxlen > 0 ? (maxlen + kRowChunk - 1) / kRowChunk : 1;
 }
 
 template <class F>
@@ -156,16 +156,18 @@ double row_scores(const oracle_params_t* p, const double* q, const double* k, in
 extern "C" {
 
 // Forward: O and LSE by the plain definition (full softmax over each row).
+// Rows are independent, so work items are (sequence, query head, chunk of rows).
 int oracle_attn_fwd(const oracle_params_t* p, const double* q, const double* k, const double* v,
                     double* o, double* lse, int nthreads) {
   const int NS = n_sequences(p), Hq = p->heads_q, D = p->head_dim;
   if (Hq <= 0 || p->heads_kv <= 0 || Hq % p->heads_kv) return 1;
-  parallel_for(NS * Hq, nthreads, [&](int item) {
-    const int n = item / Hq, h = item % Hq;
+  const int chunks = row_chunks(p);
+  parallel_for(NS * Hq * chunks, nthreads, [&](int item) {
+    const int n = item / (Hq * chunks), h = (item / chunks) % Hq, c = item % chunks;
     const int L = seq_len(p, n);
     const int G = Hq / p->heads_kv, g = h / G;
     std::vector<double> s(L > 0 ? L : 1);
-    for (int i = 0; i < L; ++i) {
+    for (int i = c * kRowChunk; i < L && i < (c + 1) * kRowChunk; ++i) {
       double* oi = o + row_off(p, n, h, Hq, i);
       for (int t = 0; t < D; ++t) oi[t] = 0.0;
       const double m = row_scores(p, q, k, n, h, i, s);
@@ -241,51 +243,79 @@ int oracle_attn_fwd_blocked(const oracle_params_t* p, const double* q, const dou
   return 0;
 }
 
-// Backward: dQ, dK, dV by the softmax Jacobian, recomputing P row by row.
-// Work items are (sequence, KV head) so that dK/dV of a group are owned by one
-// thread and summed over the group's query heads without locks.
+// Backward: dQ, dK, dV by the softmax Jacobian, recomputing P from the scores.
+//   pass 1, per query row i (items: sequence, query head, chunk of rows):
+//     m_i, l_i (max and sum of the row's softmax), dP_ij = <dO_i, v_j>,
+//     delta_i = sum_j P_ij dP_ij and dQ_i = scale sum_j dS_ij k_j;
+//   pass 2, per key row j (items: sequence, KV head, chunk of keys):
+//     dK_j = scale sum_{h in group} sum_i dS_ij q_i,  dV_j = sum_{h in group} sum_i P_ij dO_i,
+//     with P_ij = exp(s_ij - m_i) / l_i and dS_ij = P_ij (dP_ij - delta_i) taken from
+//     the row quantities of pass 1.
 int oracle_attn_bwd(const oracle_params_t* p, const double* q, const double* k, const double* v,
                     const double* dout, double* dq, double* dk, double* dv, int nthreads) {
   const int NS = n_sequences(p), Hq = p->heads_q, Hkv = p->heads_kv, D = p->head_dim;
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv) return 1;
   const int G = Hq / Hkv;
-  parallel_for(NS * Hkv, nthreads, [&](int item) {
-    const int n = item / Hkv, g = item % Hkv;
-    const int L = seq_len(p, n);
+  const int chunks = row_chunks(p);
+  // Row statistics, laid out like lse.
+  int64_t n_rows = 0;
+  for (int n = 0; n < NS; ++n) n_rows += (int64_t)seq_len(p, n) * Hq;
+  std::vector<double> row_m(n_rows), row_l(n_rows), row_delta(n_rows);
+
+  parallel_for(NS * Hq * chunks, nthreads, [&](int item) {
+    const int n = item / (Hq * chunks), h = (item / chunks) % Hq, c = item % chunks;
+    const int L = seq_len(p, n), g = h / G;
     std::vector<double> s(L > 0 ? L : 1), dp(L > 0 ? L : 1);
-    for (int j = 0; j < L; ++j) {
+    for (int i = c * kRowChunk; i < L && i < (c + 1) * kRowChunk; ++i) {
+      double* dqi = dq + row_off(p, n, h, Hq, i);
+      for (int t = 0; t < D; ++t) dqi[t] = 0.0;
+      const int64_t r = lse_off(p, n, h, i);
+      const double m = row_scores(p, q, k, n, h, i, s);
+      row_m[r] = m;
+      row_l[r] = 0.0;
+      row_delta[r] = 0.0;
+      if (m == kNegInf) continue;
+      double l = 0.0;
+      for (int j = 0; j < L; ++j)
+        if (s[j] != kNegInf) l += std::exp(s[j] - m);
+      const double* doi = dout + row_off(p, n, h, Hq, i);
+      double delta = 0.0;
+      for (int j = 0; j < L; ++j) {
+        if (s[j] == kNegInf) { s[j] = 0.0; dp[j] = 0.0; continue; }
+        s[j] = std::exp(s[j] - m) / l;  // P_ij
+        dp[j] = dot(doi, v + row_off(p, n, g, Hkv, j), D);
+        delta += s[j] * dp[j];
+      }
+      for (int j = 0; j < L; ++j) {
+        if (s[j] == 0.0) continue;
+        const double ds = s[j] * (dp[j] - delta);
+        const double* kj = k + row_off(p, n, g, Hkv, j);
+        for (int t = 0; t < D; ++t) dqi[t] += p->scale * ds * kj[t];
+      }
+      row_l[r] = l;
+      row_delta[r] = delta;
+    }
+  });
+
+  parallel_for(NS * Hkv * chunks, nthreads, [&](int item) {
+    const int n = item / (Hkv * chunks), g = (item / chunks) % Hkv, c = item % chunks;
+    const int L = seq_len(p, n);
+    for (int j = c * kRowChunk; j < L && j < (c + 1) * kRowChunk; ++j) {
       double* dkj = dk + row_off(p, n, g, Hkv, j);
       double* dvj = dv + row_off(p, n, g, Hkv, j);
       for (int t = 0; t < D; ++t) dkj[t] = dvj[t] = 0.0;
-    }
-    for (int h = g * G; h < (g + 1) * G; ++h) {
-      for (int i = 0; i < L; ++i) {
-        double* dqi = dq + row_off(p, n, h, Hq, i);
-        for (int t = 0; t < D; ++t) dqi[t] = 0.0;
-        const double m = row_scores(p, q, k, n, h, i, s);
-        if (m == kNegInf) continue;
-        double l = 0.0;
-        for (int j = 0; j < L; ++j)
-          if (s[j] != kNegInf) l += std::exp(s[j] - m);
-        const double* qi = q + row_off(p, n, h, Hq, i);
-        const double* doi = dout + row_off(p, n, h, Hq, i);
-        // P_ij (stored over s) and dP_ij = dO_i . v_j; delta_i = sum_j P_ij dP_ij
-        double delta = 0.0;
-        for (int j = 0; j < L; ++j) {
-          if (s[j] == kNegInf) { s[j] = 0.0; dp[j] = 0.0; continue; }
-          s[j] = std::exp(s[j] - m) / l;
-          dp[j] = dot(doi, v + row_off(p, n, g, Hkv, j), D);
-          delta += s[j] * dp[j];
-        }
-        for (int j = 0; j < L; ++j) {
-          const double pij = s[j];
-          if (pij == 0.0) continue;
-          const double ds = pij * (dp[j] - delta);
-          const double* kj = k + row_off(p, n, g, Hkv, j);
-          double* dkj = dk + row_off(p, n, g, Hkv, j);
-          double* dvj = dv + row_off(p, n, g, Hkv, j);
+      const double* kj = k + row_off(p, n, g, Hkv, j);
+      const double* vj = v + row_off(p, n, g, Hkv, j);
+      for (int h = g * G; h < (g + 1) * G; ++h) {
+        for (int i = 0; i < L; ++i) {
+          if (!keep(p, i, j, L)) continue;
+          const int64_t r = lse_off(p, n, h, i);
+          if (row_m[r] == kNegInf) continue;
+          const double* qi = q + row_off(p, n, h, Hq, i);
+          const double* doi = dout + row_off(p, n, h, Hq, i);
+          const double pij = std::exp(p->scale * dot(qi, kj, D) - row_m[r]) / row_l[r];
+          const double ds = pij * (dot(doi, vj, D) - row_delta[r]);
           for (int t = 0; t < D; ++t) {
-            dqi[t] += p->scale * ds * kj[t];
             dkj[t] += p->scale * ds * qi[t];
             dvj[t] += pij * doi[t];
           }

@@ -1,0 +1,100 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path through the C ABI
+binding, run the oracle on the same seeded inputs, compare element by element.
+
+Tolerances (written here, used by every GPU test):
+  float32 I/O : max |gpu - oracle| <= 1e-3 on O, LSE, dQ, dK, dV (the 1e-3
+                alignment bar of the zwxr.cn CANN ops-nn article, section 3.4,
+                read as an absolute bound).
+  bfloat16 I/O: max |gpu - oracle| <= 2e-2 and ||gpu - oracle||_2 / ||oracle||_2
+                <= 1e-2 per tensor; LSE max-abs <= 2e-2.  The kernels round
+                bf16 operands to the nearest value and accumulate in float32.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from bwd_flashattention_fwd_sm_gb300 import BlockMask, SeqLens, attn_bwd, attn_fwd, get_status
+from bwd_flashattention_fwd_sm_gb300 import workloads as W
+
+TOL_F32 = 1e-3
+TOL_BF16_ABS = 2e-2
+TOL_BF16_REL = 1e-2
+
+
+def compare(name, got, ref, dtype):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, f"{name}: shape {got.shape} vs {ref.shape}"
+    inf_ref = np.isneginf(ref)
+    assert np.array_equal(np.isneginf(got), inf_ref), f"{name}: -inf positions differ"
+    fin = ~inf_ref
+    g, r = got[fin], ref[fin]
+    assert np.all(np.isfinite(g)), f"{name}: non-finite values"
+    if g.size == 0:
+        return 0.0, 0.0
+    err = np.abs(g - r)
+    max_abs = float(err.max())
+    nrm = float(np.linalg.norm(r))
+    rel = float(np.linalg.norm(g - r) / nrm) if nrm > 0 else float(np.linalg.norm(g - r))
+    if dtype == "f32":
+        assert max_abs <= TOL_F32, f"{name}: max-abs {max_abs:.3e} > {TOL_F32}"
+    else:
+        assert max_abs <= TOL_BF16_ABS, f"{name}: max-abs {max_abs:.3e} > {TOL_BF16_ABS}"
+        if not name.startswith("lse"):
+            assert rel <= TOL_BF16_REL, f"{name}: rel-L2 {rel:.3e} > {TOL_BF16_REL}"
+    return max_abs, rel
+
+
+def gpu_run(wl: W.Workload, inputs: dict, passes="fwd+bwd"):
+    """Run the CUDA path on `inputs` (CPU tensors); returns CPU float64 numpy results."""
+    dev = torch.device("cuda")
+    q, k, v, do = (inputs[n].to(dev) for n in ("q", "k", "v", "do"))
+    kw = {"scale": wl.scale}
+    if wl.mask == "causal":
+        kw["causal"] = True
+    if wl.mask == "block":
+        kw["block_mask"] = BlockMask.from_csr(inputs["block_mask"], device=dev)
+    if wl.varlen:
+        kw["seqlens"] = SeqLens(inputs["cu_seqlens"], device=dev)
+        kw["seqlen"] = wl.seqlen
+    o, lse = attn_fwd(q, k, v, **kw)
+    out = {"o": o, "lse": lse}
+    if "bwd" in passes:
+        dq, dk, dv = attn_bwd(q, k, v, o, do, lse, **kw)
+        out.update(dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert get_status() == 0, "device status word set"
+    return {n: t.double().cpu().numpy() for n, t in out.items()}
+
+
+def oracle_kw(wl: W.Workload, inputs: dict):
+    kw = {"scale": wl.scale}
+    if wl.mask == "causal":
+        kw["causal"] = True
+    if wl.mask == "block":
+        kw["block_mask"] = inputs["block_mask"]
+    return kw
+
+
+def oracle_run(wl, inputs, passes="fwd+bwd", cu=None):
+    q, k, v, do = (inputs[n].double().numpy() for n in ("q", "k", "v", "do"))
+    kw = oracle_kw(wl, inputs)
+    if cu is not None:
+        kw["cu_seqlens"] = cu
+    o, lse = oracle.attn_fwd(q, k, v, **kw)
+    ref = {"o": o, "lse": lse}
+    if "bwd" in passes:
+        dq, dk, dv = oracle.attn_bwd(q, k, v, do, **kw)
+        ref.update(dq=dq, dk=dk, dv=dv)
+    return ref
+
+
+def check_all(wl, got, ref, names=("o", "lse", "dq", "dk", "dv")):
+    report = {}
+    for n in names:
+        if n in ref:
+            report[n] = compare(f"{n}[{wl.name}]", got[n], ref[n], wl.dtype)
+    return report
