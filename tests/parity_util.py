@@ -5,9 +5,12 @@ Tolerances (written here, used by every GPU test):
   float32 I/O : max |gpu - oracle| <= 1e-3 on O, LSE, dQ, dK, dV (the 1e-3
                 alignment bar of the zwxr.cn CANN ops-nn article, section 3.4,
                 read as an absolute bound).
-  bfloat16 I/O: max |gpu - oracle| <= 2e-2 and ||gpu - oracle||_2 / ||oracle||_2
-                <= 1e-2 per tensor; LSE max-abs <= 2e-2.  The kernels round
-                bf16 operands to the nearest value and accumulate in float32.
+  bfloat16 I/O: |gpu - oracle| <= 2e-2 + 2^-7 |oracle| element-wise, and
+                ||gpu - oracle||_2 / ||oracle||_2 <= 1e-2 per tensor; LSE
+                (float32) max-abs <= 2e-2.  The 2e-2 bound is for unit-scale
+                values; a bf16 output of magnitude >= 4 cannot hold it by itself
+                (its spacing is 2^-5 and above), so each element also gets one
+                bf16 unit in the last place of its own magnitude (2^-7 |x| bounds it).
 """
 
 from __future__ import annotations
@@ -22,6 +25,7 @@ from bwd_flashattention_fwd_sm_gb300 import workloads as W
 TOL_F32 = 1e-3
 TOL_BF16_ABS = 2e-2
 TOL_BF16_REL = 1e-2
+TOL_BF16_ULP = 2.0 ** -7
 
 
 def compare(name, got, ref, dtype):
@@ -41,10 +45,14 @@ def compare(name, got, ref, dtype):
     rel = float(np.linalg.norm(g - r) / nrm) if nrm > 0 else float(np.linalg.norm(g - r))
     if dtype == "f32":
         assert max_abs <= TOL_F32, f"{name}: max-abs {max_abs:.3e} > {TOL_F32}"
-    else:
+    elif name.startswith("lse"):
         assert max_abs <= TOL_BF16_ABS, f"{name}: max-abs {max_abs:.3e} > {TOL_BF16_ABS}"
-        if not name.startswith("lse"):
-            assert rel <= TOL_BF16_REL, f"{name}: rel-L2 {rel:.3e} > {TOL_BF16_REL}"
+    else:
+        bound = TOL_BF16_ABS + TOL_BF16_ULP * np.abs(r)
+        worst = int(np.argmax(err - bound))
+        assert np.all(err <= bound), (f"{name}: |err| {err[worst]:.3e} > {bound[worst]:.3e} at value "
+                                      f"{r[worst]:.4f} (max-abs {max_abs:.3e})")
+        assert rel <= TOL_BF16_REL, f"{name}: rel-L2 {rel:.3e} > {TOL_BF16_REL}"
     return max_abs, rel
 
 
