@@ -174,6 +174,12 @@ def run_ours(args, wl, rank, world, dist):
     step_ev = [(ev(), ev()) for _ in range(args.steps)]
     fwd_ev = [(ev(), ev()) for _ in range(args.steps)]
     bwd_ev = [(ev(), ev()) for _ in range(args.steps)]
+    # torch creates the CUDA event behind an Event on its first record: record
+    # each once so that the library's timing hook receives real handles.
+    for pair in fwd_ev + bwd_ev:
+        for e in pair:
+            e.record(stream)
+    torch.cuda.synchronize()
     clocks = ClockSampler(gpu_identity(torch)) if rank == 0 else None
     if dist is not None:
         dist.barrier()

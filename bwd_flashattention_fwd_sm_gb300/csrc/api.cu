@@ -79,9 +79,11 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
-// Which kernel family serves these parameters.
-bool use_tensor_cores(const attn_params_t* p) {
-  return tc_available() && p->dtype == ATTN_BF16 && p->head_dim == 128;
+// Which kernel family serves these parameters: the tensor-core kernels for bf16
+// with head_dim 128, the float32-arithmetic kernels for float32 I/O.
+bool use_tensor_cores(const attn_params_t* p, bool backward) {
+  const bool avail = backward ? tc_bwd_available() : tc_fwd_available();
+  return avail && p->dtype == ATTN_BF16 && p->head_dim == 128;
 }
 
 struct Problem {
@@ -223,8 +225,7 @@ KParams base_kparams(const attn_params_t* p, const Problem& pr) {
 Layout layout_for(const attn_params_t* p, const Problem& pr, bool backward) {
   Layout L;
   std::memset(&L, 0, sizeof(L));
-  const bool tc = use_tensor_cores(p);
-  L.tile_rows = tc ? 128 : 64;
+  L.tile_rows = use_tensor_cores(p, backward) ? 128 : 64;
   KParams k = base_kparams(p, pr);
   L.n_units = count_units(k, p->cu_seqlens_host, backward, L.tile_rows);
   size_t off = 0;
@@ -318,7 +319,7 @@ attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, con
   if (e != cudaSuccess) return cuda_fail(e, "work-list launch");
   if (g_timing_events[0][0] && (e = cudaEventRecord(g_timing_events[0][0], st)) != cudaSuccess)
     return cuda_fail(e, "timing event");
-  if (use_tensor_cores(p)) e = launch_tc_fwd(kp, sms, st);
+  if (use_tensor_cores(p, false)) e = launch_tc_fwd(kp, sms, st);
   else e = launch_simt_fwd(kp, p->dtype == ATTN_BF16, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   if (g_timing_events[0][1] && (e = cudaEventRecord(g_timing_events[0][1], st)) != cudaSuccess)
@@ -377,7 +378,7 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, con
   if (e != cudaSuccess) return cuda_fail(e, "preprocess launch");
   if (g_timing_events[1][0] && (e = cudaEventRecord(g_timing_events[1][0], st)) != cudaSuccess)
     return cuda_fail(e, "timing event");
-  if (use_tensor_cores(p)) e = launch_tc_bwd(kp, sms, st);
+  if (use_tensor_cores(p, true)) e = launch_tc_bwd(kp, sms, st);
   else e = launch_simt_bwd(kp, bf16, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   if (g_timing_events[1][1] && (e = cudaEventRecord(g_timing_events[1][1], st)) != cudaSuccess)

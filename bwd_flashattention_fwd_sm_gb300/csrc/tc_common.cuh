@@ -1,0 +1,186 @@
+// Pieces shared by the tensor-core forward and backward kernels: tile loads
+// through TMA and the lists of score tiles a unit visits.
+#pragma once
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace gbattn {
+
+constexpr int kTile = 128;                       // rows of a Q tile / keys of a K,V tile
+constexpr int kHeadDim = 128;
+constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // bf16 128 x 128 = 32 KiB
+constexpr uint32_t kHalfTileBytes = kTileBytes / 2;    // one 128 x 64 box (128-byte rows)
+
+// Loads rows [row, row + rows) x all 128 columns of one head as two 64-column
+// boxes (each rows x 128 bytes, 128-byte swizzled) at dst and dst + box_bytes.
+__device__ __forceinline__ void tma_tile(void* dst, const CUtensorMap* map, int rows_inner, uint64_t* bar,
+                                         int row, int head, int b, uint32_t box_bytes) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    void* d = static_cast<char*>(dst) + c * box_bytes;
+    if (rows_inner) ptx::tma_load_4d(d, map, bar, c * 64, row, head, b);
+    else ptx::tma_load_4d(d, map, bar, c * 64, head, row, b);
+  }
+}
+
+// Row coordinate and batch coordinate of position `pos` of a sequence in a tile map.
+__device__ __forceinline__ int map_row(const SeqInfo& s, int pos) { return (int)(s.tok0 + pos); }
+
+// The score tiles a forward unit (one 128-row query tile) visits, in ascending
+// key order, with a 4-bit mask of which 64x64 sub-blocks are listed:
+//   bit 0 (rows 0-63, keys 0-63), bit 1 (rows 0-63, keys 64-127),
+//   bit 2 (rows 64-127, keys 0-63), bit 3 (rows 64-127, keys 64-127).
+// Dense and causal units visit tiles 0 .. n-1 with all four bits set.
+struct KvTileList {
+  int mode;      // kMaskNone / kMaskCausal: dense range; kMaskBlock: merged lists
+  int n_dense;   // dense range length
+  int it;
+  const int* col;
+  int ia, ea, ib, eb;  // block lists of the two 64-row query blocks
+  int nblk;            // 64-blocks in the sequence (columns beyond are ignored)
+
+  __device__ void init(const KParams& p, int len, int q0) {
+    mode = p.mask;
+    it = 0;
+    nblk = (len + 63) / 64;
+    if (mode == kMaskNone) {
+      n_dense = (len + kTile - 1) / kTile;
+    } else if (mode == kMaskCausal) {
+      const int qlast = min(len, q0 + kTile) - 1;
+      n_dense = qlast / kTile + 1;
+    } else {
+      col = p.col_idx;
+      const int rb0 = q0 / 64, rb1 = rb0 + 1;
+      ia = p.row_ptr[rb0];
+      ea = p.row_ptr[rb0 + 1];
+      if (rb1 < p.n_row_blocks && rb1 * 64 < len) {
+        ib = p.row_ptr[rb1];
+        eb = p.row_ptr[rb1 + 1];
+      } else {
+        ib = eb = 0;
+      }
+    }
+  }
+
+  // Next tile: key tile index and sub-block bits.  False when exhausted.
+  __device__ bool next(int& kt, int& bits) {
+    if (mode != kMaskBlock) {
+      if (it >= n_dense) return false;
+      kt = it++;
+      bits = 0xF;
+      return true;
+    }
+    const int a = (ia < ea && col[ia] < nblk) ? col[ia] : INT_MAX;
+    const int b = (ib < eb && col[ib] < nblk) ? col[ib] : INT_MAX;
+    const int m = a < b ? a : b;
+    if (m == INT_MAX) return false;
+    kt = m >> 1;
+    bits = 0;
+    while (ia < ea && col[ia] < nblk && (col[ia] >> 1) == kt) {
+      bits |= 1 << (col[ia] & 1);
+      ++ia;
+    }
+    while (ib < eb && col[ib] < nblk && (col[ib] >> 1) == kt) {
+      bits |= 4 << (col[ib] & 1);
+      ++ib;
+    }
+    return true;
+  }
+};
+
+}  // namespace gbattn
+
+namespace gbattn {
+
+// The 64-row query blocks a backward unit (one 128-key tile) visits for one
+// query head, ascending, with a 2-bit mask of which 64x64 sub-blocks are listed:
+//   bit 0 (keys 0-63 of the tile), bit 1 (keys 64-127).
+// Dense units visit every query block; causal units start at the block holding
+// the tile's first key; block-sparse units take the union of the two key
+// blocks' transposed (per key block) lists.
+struct QBlockList {
+  int mode;
+  int first, count, it;      // dense / causal range
+  const int* row;            // transposed lists (query blocks per key block)
+  int a0, ea, b0, eb, ia, ib;
+  int nblk;
+
+  __device__ void init(const KParams& p, int len, int kt) {
+    mode = p.mask;
+    nblk = (len + 63) / 64;
+    it = 0;
+    a0 = ea = b0 = eb = 0;
+    row = nullptr;
+    if (mode == kMaskNone) {
+      first = 0;
+      count = nblk;
+    } else if (mode == kMaskCausal) {
+      first = 2 * kt;
+      count = nblk > first ? nblk - first : 0;
+    } else {
+      row = p.csc_idx;
+      const int cb0 = 2 * kt, cb1 = cb0 + 1;
+      a0 = p.csc_ptr[cb0];
+      ea = p.csc_ptr[cb0 + 1];
+      if (cb1 < p.n_col_blocks && cb1 * 64 < len) {
+        b0 = p.csc_ptr[cb1];
+        eb = p.csc_ptr[cb1 + 1];
+      } else {
+        b0 = eb = 0;
+      }
+    }
+    restart();
+  }
+
+  __device__ void restart() {
+    it = 0;
+    ia = a0;
+    ib = b0;
+  }
+
+  __device__ bool next(int& qb, int& bits) {
+    if (mode != kMaskBlock) {
+      if (it >= count) return false;
+      qb = first + it++;
+      bits = 3;
+      return true;
+    }
+    const int a = (ia < ea && row[ia] < nblk) ? row[ia] : INT_MAX;
+    const int b = (ib < eb && row[ib] < nblk) ? row[ib] : INT_MAX;
+    const int m = a < b ? a : b;
+    if (m == INT_MAX) return false;
+    qb = m;
+    bits = (a == m ? 1 : 0) | (b == m ? 2 : 0);
+    if (a == m) ++ia;
+    if (b == m) ++ib;
+    return true;
+  }
+};
+
+// Steps of a backward unit: every query head of the KV head's group, each with
+// its query-block list.
+struct BwdSteps {
+  QBlockList list;
+  int group, hh;
+
+  __device__ void init(const KParams& p, int len, int kt) {
+    list.init(p, len, kt);
+    group = p.group;
+    hh = 0;
+  }
+  // Next step: query head offset in the group, query block, sub-block bits.
+  __device__ bool next(int& head_off, int& qb, int& bits) {
+    while (hh < group) {
+      if (list.next(qb, bits)) {
+        head_off = hh;
+        return true;
+      }
+      ++hh;
+      list.restart();
+    }
+    return false;
+  }
+};
+
+}  // namespace gbattn

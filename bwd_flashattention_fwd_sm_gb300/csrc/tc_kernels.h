@@ -5,8 +5,9 @@
 
 namespace gbattn {
 
-// True when this build carries the tensor-core kernels.
-bool tc_available();
+// True when this build carries the tensor-core forward / backward kernels.
+bool tc_fwd_available();
+bool tc_bwd_available();
 
 // bf16, head_dim 128.  Work list of 128-row units already built in p.units.
 cudaError_t launch_tc_fwd(const KParams& p, int sms, cudaStream_t st);

@@ -1,0 +1,25 @@
+// Host-side TMA descriptor construction for 128-row x 64-column bf16 tiles
+// (128-byte swizzle) of q-like and kv-like tensors.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace gbattn {
+
+// Where a tile's rows sit among the tensor map's dimensions.
+//   rows_inner = 1: dims (d, position, head, batch)  -- head-major storage
+//   rows_inner = 0: dims (d, head, position, batch)  -- position-major storage
+//                   (also packed variable-length tensors: position = token, batch = 1)
+struct TileMap {
+  CUtensorMap map;
+  int rows_inner;
+};
+
+// Builds the map for the q-like (kv = false) or kv-like (kv = true) tensor at
+// `base`, with boxes of `box_rows` positions x 64 columns.
+cudaError_t make_tile_map(TileMap* out, const void* base, const KParams& p, bool kv, int box_rows = 128);
+
+}  // namespace gbattn
