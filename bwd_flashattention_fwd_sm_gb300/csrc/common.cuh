@@ -60,6 +60,7 @@ struct KParams {
 
   const Unit* units;
   int n_units;
+  int* unit_counter;    // persistent kernels: next unit to take (zeroed by the work-list build)
 
   int* status;               // device status word
   unsigned long long wait_limit_ns;  // bounded-wait limit for pipeline barriers

@@ -121,7 +121,10 @@ __global__ void __launch_bounds__(kThreads) k_build_worklist(KParams p, int back
     prefix[n] = base;
     base += cdiv(seq_info(p, n).len, tile_rows);
   }
-  if (tid == 0) prefix[n_seqs] = total;
+  if (tid == 0) {
+    prefix[n_seqs] = total;
+    if (p.unit_counter) *p.unit_counter = 0;
+  }
   for (int i = tid; i < kBuckets; i += kThreads) hist[i] = 0;
   __syncthreads();
 

@@ -184,3 +184,79 @@ struct BwdSteps {
 };
 
 }  // namespace gbattn
+
+namespace gbattn {
+
+// The score tiles a 256-row forward unit (two 128-row query tiles, four 64-row
+// query blocks) visits: the ascending union over its query blocks, each with an
+// 8-bit mask of listed 64x64 sub-blocks, bit 2r + c for query block r (0-3) and
+// key half c (0-1).  Query tile q uses bits 4q..4q+3 and skips a tile whose
+// four bits are all clear.  Dense and causal units list every key tile up to
+// the last one any of their rows sees; a query tile past the sequence end, or
+// (causal) whose rows all precede a key tile, gets clear bits for it.
+struct KvTileList2 {
+  int mode, n_dense, it, len, q0;
+  const int* col;
+  int s[4], e[4];
+  int nblk;
+
+  __device__ void init(const KParams& p, int len_, int q0_) {
+    mode = p.mask;
+    len = len_;
+    q0 = q0_;
+    it = 0;
+    nblk = (len + 63) / 64;
+    const int last = min(len, q0 + 2 * kTile) - 1;
+    if (mode == kMaskNone) {
+      n_dense = (len + kTile - 1) / kTile;
+    } else if (mode == kMaskCausal) {
+      n_dense = last / kTile + 1;
+    } else {
+      n_dense = 0;
+      col = p.col_idx;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int rb = q0 / 64 + r;
+        if (rb < p.n_row_blocks && rb * 64 < len) {
+          s[r] = p.row_ptr[rb];
+          e[r] = p.row_ptr[rb + 1];
+        } else {
+          s[r] = e[r] = 0;
+        }
+      }
+    }
+  }
+
+  __device__ bool next(int& kt, int& bits) {
+    if (mode != kMaskBlock) {
+      if (it >= n_dense) return false;
+      kt = it++;
+      bits = 0;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int r0 = q0 + q * kTile;
+        if (r0 >= len) continue;
+        const int rl = min(len, r0 + kTile) - 1;
+        if (mode == kMaskCausal && kt * kTile > rl) continue;
+        bits |= 0xF << (4 * q);
+      }
+      return true;
+    }
+    int m = INT_MAX;
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      if (s[r] < e[r] && col[s[r]] < nblk) m = min(m, col[s[r]]);
+    if (m == INT_MAX) return false;
+    kt = m >> 1;
+    bits = 0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      while (s[r] < e[r] && col[s[r]] < nblk && (col[s[r]] >> 1) == kt) {
+        bits |= 1 << (2 * r + (col[s[r]] & 1));
+        ++s[r];
+      }
+    return true;
+  }
+};
+
+}  // namespace gbattn

@@ -66,4 +66,32 @@ cudaError_t make_tile_map(TileMap* out, const void* base, const KParams& p, bool
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_acc_map(TileMap* out, float* base, const KParams& p, int box_rows) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const long long D = p.head_dim, H = p.heads_q, E = 4;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
+  if (p.varlen) {
+    out->rows_inner = 0;
+    dims[0] = D; dims[1] = H; dims[2] = p.total_tokens; dims[3] = 1;
+    strides[0] = D * E;
+    strides[1] = H * D * E;
+    strides[2] = H * D * E * (p.total_tokens > 0 ? p.total_tokens : 1);
+    box[0] = (cuuint32_t)D; box[1] = 1; box[2] = box_rows; box[3] = 1;
+  } else {
+    out->rows_inner = 1;
+    dims[0] = D; dims[1] = p.seqlen; dims[2] = H; dims[3] = p.batch;
+    strides[0] = D * E;
+    strides[1] = (long long)p.seqlen * D * E;
+    strides[2] = H * p.seqlen * D * E;
+    box[0] = (cuuint32_t)D; box[1] = box_rows; box[2] = 1; box[3] = 1;
+  }
+  std::memset(&out->map, 0, sizeof(out->map));
+  CUresult r = enc(&out->map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace gbattn

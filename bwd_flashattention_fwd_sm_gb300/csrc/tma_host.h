@@ -22,4 +22,9 @@ struct TileMap {
 // `base`, with boxes of `box_rows` positions x 64 columns.
 cudaError_t make_tile_map(TileMap* out, const void* base, const KParams& p, bool kv, int box_rows = 128);
 
+// Map of the float32 dQ accumulator (rows laid out like a contiguous q) for
+// TMA reduce-adds of 64-row x 128-column tiles (no swizzle, 512-byte rows).
+//   fixed length: dims (d, position, head, batch); variable: (d, head, token, 1).
+cudaError_t make_acc_map(TileMap* out, float* base, const KParams& p, int box_rows);
+
 }  // namespace gbattn
