@@ -28,6 +28,7 @@ ATTN_MASK_CAUSAL = 1
 ATTN_MASK_BLOCK = 2
 
 SIZE_MAX = ctypes.c_size_t(-1).value
+NOALLOC_SCRATCH_BYTES = 32 << 20  # ATTN_NOALLOC_SCRATCH_BYTES in include/gbattn.h
 
 I32P = ctypes.POINTER(ctypes.c_int32)
 
@@ -78,6 +79,7 @@ SIGNATURES = {
     "attn_bwd_workspace_size": (ctypes.c_size_t, [_PP]),
     "attn_fwd": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
     "attn_bwd": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
+    "attn_bwd_noalloc": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "attn_get_status": (ctypes.c_int, [_VP]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_last_error": (ctypes.c_char_p, []),

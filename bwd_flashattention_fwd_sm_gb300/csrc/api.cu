@@ -270,6 +270,11 @@ attn_status_t cuda_fail(cudaError_t e, const char* what) {
 
 }  // namespace
 
+namespace gbattn {
+// Lets other translation units of the library report an argument error.
+void set_last_error_text(const char* text) { g_last_error = text; }
+}  // namespace gbattn
+
 extern "C" {
 
 size_t attn_fwd_workspace_size(const attn_params_t* p) {
