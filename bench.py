@@ -121,6 +121,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(value, dist, device=None):
+    """The largest `value` over all ranks (the job is as slow as its slowest rank)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(work_per_rank_step, world, steps, seconds):
+    """Work of all ranks over the slowest rank's time (weak scaling: each rank runs
+    the full per-GPU workload)."""
+    return world * work_per_rank_step * steps / seconds
+
+
 def gpu_identity(torch):
     try:
         uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
@@ -207,14 +223,10 @@ def run_ours(args, wl, rank, world, dist):
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     fwd_ms = [a.elapsed_time(b) for a, b in fwd_ev]
     bwd_ms = [a.elapsed_time(b) for a, b in bwd_ev]
-    total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     ms_per_step = total_ms / args.steps
     step_flops = fwd_flops + bwd_flops
-    value = world * step_flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_rate(step_flops, world, args.steps, total_ms * 1e-3) / 1e12
 
     # End to end through the public API with host buffers: pinned inputs copied
     # in, outputs copied back, every step.
@@ -244,13 +256,9 @@ def run_ours(args, wl, rank, world, dist):
     for _ in range(e2e_steps):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dist, dev)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
-    e2e_value = world * step_flops * e2e_steps / e2e_s / 1e12
+    e2e_value = whole_job_rate(step_flops, world, e2e_steps, e2e_s) / 1e12
 
     peaks, peak_src = load_peaks()
     peak = peak_value(peaks, "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]

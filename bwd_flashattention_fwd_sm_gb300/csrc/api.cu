@@ -186,7 +186,7 @@ attn_status_t validate_params(const attn_params_t* p, Problem* pr) {
 struct Layout {
   int tile_rows;       // rows per work unit (query rows fwd, key rows bwd)
   long long n_units;
-  size_t units, sched, csc_ptr, csc_idx, dq_acc, delta, total;
+  size_t counter, units, sched, csc_ptr, csc_idx, dq_acc, delta, total;
 };
 
 KParams base_kparams(const attn_params_t* p, const Problem& pr) {
@@ -225,10 +225,14 @@ KParams base_kparams(const attn_params_t* p, const Problem& pr) {
 Layout layout_for(const attn_params_t* p, const Problem& pr, bool backward) {
   Layout L;
   std::memset(&L, 0, sizeof(L));
-  L.tile_rows = use_tensor_cores(p, backward) ? 128 : 64;
+  // tensor cores: forward units are 256 query rows (two 128-row tiles sharing
+  // each K/V tile), backward units 128 keys; float32 path: 64 rows
+  L.tile_rows = use_tensor_cores(p, backward) ? (backward ? 128 : 256) : 64;
   KParams k = base_kparams(p, pr);
   L.n_units = count_units(k, p->cu_seqlens_host, backward, L.tile_rows);
   size_t off = 0;
+  L.counter = off;
+  off = align_up(off + sizeof(int), 256);
   L.units = off;
   off = align_up(off + sizeof(Unit) * (size_t)L.n_units, 256);
   L.sched = off;
@@ -318,6 +322,7 @@ attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, con
   kp.status = status;
   kp.units = reinterpret_cast<const Unit*>(ws + L.units);
   kp.n_units = (int)L.n_units;
+  kp.unit_counter = reinterpret_cast<int*>(ws + L.counter);
 
   cudaError_t e = launch_build_worklist(kp, false, L.tile_rows, reinterpret_cast<Unit*>(ws + L.units),
                                         (int)L.n_units, reinterpret_cast<int*>(ws + L.sched), st);
@@ -368,6 +373,7 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, con
   kp.delta = reinterpret_cast<float*>(ws + L.delta);
   kp.units = reinterpret_cast<const Unit*>(ws + L.units);
   kp.n_units = (int)L.n_units;
+  kp.unit_counter = reinterpret_cast<int*>(ws + L.counter);
 
   cudaError_t e = cudaSuccess;
   if (p->mask == ATTN_MASK_BLOCK) {

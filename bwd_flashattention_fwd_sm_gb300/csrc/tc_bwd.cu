@@ -1,29 +1,36 @@
-// Backward attention on the fifth-generation tensor cores (sm_103a).
+// Backward attention on the fifth-generation tensor cores (sm_103a): persistent
+// CTAs, dQ reduced through TMA.
 //
 // The forward drops the attention matrix, so the backward recomputes it block
-// by block and produces three gradients; walking the keys' blocks gathers dK and
+// by block and produces three gradients; walking the key blocks gathers dK and
 // dV, while dQ accumulates in the opposite direction and many blocks add into
 // the same rows (smzdm contest article "杀进决赛!这 28 支队伍把算子优化卷疯了!",
-// section 03).  This kernel keeps one 128-key tile of K and V on chip, walks the
-// query blocks (of every query head of the KV head's group) that see it, and
-// accumulates dK and dV in tensor memory; each block's dQ share is added into a
-// float32 accumulator with atomic adds.
+// section 03).  A unit keeps one 128-key tile of K and V on chip, walks the
+// 64-row query blocks (of every query head of the KV head's group) that see it,
+// and accumulates dK and dV in tensor memory.
 //
-// Per 64-row query block i (all five products on the tensor cores, bf16 operands,
-// float32 accumulation in tensor memory):
+// Per query block i (five tcgen05 products, bf16 operands, float32 accumulation):
 //   S^T  = K Q_i^T            P^T = exp(S^T * scale - LSE_i)   (masked: 0)
 //   dP^T = V dO_i^T           dS^T = P^T o (dP^T - D_i),  D_i = <dO_i, O_i>
 //   dV  += P^T dO_i           (P^T read from tensor memory)
 //   dK  += dS^T Q_i           (dS^T from shared memory)
-//   dQ_i^T = K^T dS^T         -> float32 atomics into the accumulator
+//   dQ_i^T = K^T dS^T         -> staged in shared memory, added into the float32
+//                                accumulator by one TMA reduce-add (the L2 adds)
+//
+// CTAs are persistent (one per SM): the TMA warp takes the next unit from an
+// atomic counter over the cost-ordered work list (zwxr.cn CANN ops-nn article,
+// section 4.2: whoever finishes first takes the next block) and hands it to the
+// other roles through a two-slot ring in shared memory.
 //
 // Warp roles (320 threads):
-//   warps 0-3  thread t owns key row t: P^T, dS^T, then the dK epilogue
-//   warps 4-7  thread t owns head-dim column t of dQ_i^T: atomics; dV epilogue
-//   warp 8     TMA producer (K, V once; Q_i, dO_i double-buffered) + LSE, D rows
+//   warps 0-3  thread t owns key row t: P^T and dS^T; dK epilogue
+//   warps 4-7  thread t owns head-dim column t of dQ_i^T: staging + TMA reduce;
+//              dV epilogue
+//   warp 8     TMA producer (K, V per unit; Q_i, dO_i in a 3-stage ring; LSE, D rows)
 //   warp 9     tensor-core issuer (one thread)
-// Every wait is bounded; a CTA that gives up records ATTN_ERR_DEVICE_TIMEOUT,
-// drains its copies and tensor-core work, frees tensor memory and returns.
+// Every mbarrier wait is bounded; a CTA that gives up records
+// ATTN_ERR_DEVICE_TIMEOUT, drains its copies and tensor-core work, frees tensor
+// memory and returns.
 #include <cuda.h>
 
 #include "tc_common.cuh"
@@ -34,77 +41,89 @@ namespace gbattn {
 
 namespace {
 
-constexpr int kQB = 64;                          // query rows per step
-constexpr uint32_t kQBoxBytes = kQB * 128;       // 64 rows x 64 bf16 columns (128-byte rows)
-constexpr uint32_t kQTileBytes = 2 * kQBoxBytes; // 64 x 128 bf16
-constexpr uint32_t kDsBytes = kTile * kQB * 2;   // dS^T: 128 key rows x 64 bf16 query columns
-constexpr int kBwdThreads = 320;
+constexpr int kQB = 64;                           // query rows per step
+constexpr uint32_t kQBoxBytes = kQB * 128;        // 64 rows x 64 bf16 (128-byte rows)
+constexpr uint32_t kQTileBytes = 2 * kQBoxBytes;  // 64 x 128 bf16
+constexpr uint32_t kDsBytes = kTile * kQB * 2;    // dS^T: 128 key rows x 64 bf16 query columns
+constexpr int kStages = 3;  // Q_i / dO_i ring: loads run two steps ahead of the products
+constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
-// dV [0,128) dK [128,256) S^T buffers [256,320) [320,384) dP^T [384,448) dQ^T [448,512)
+// dV [0,128) dK [128,256) S^T [256,320) [320,384) dP^T [384,448) dQ^T [448,512)
 constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384, kColDQ = 448;
 
 struct BwdArgs {
-  CUtensorMap tq, tk, tv, tdo;
-  int q_rows_inner, kv_rows_inner;
+  CUtensorMap tq, tk, tv, tdo, tacc;
+  int q_rows_inner, kv_rows_inner, acc_rows_inner;
   KParams p;
 };
 
-struct BwdSmem {
+struct Smem {
   uint8_t k[kTileBytes];
   uint8_t v[kTileBytes];
-  uint8_t q[2][kQTileBytes];   // Q_i stages; dK staging in the epilogue
-  uint8_t dO[2][kQTileBytes];  // dO_i stages; dV staging in the epilogue
-  uint8_t ds[2][kDsBytes];     // dS^T buffers (128-byte swizzled rows)
-  float lse2[2][kQB];          // LSE * log2(e) of the stage's query rows (+inf: no key)
-  float dlt[2][kQB];           // D of the stage's query rows
-  uint64_t kv_full, qdo_full[2], qdo_empty[2], st_full[2], pt_full[2], dp_full, dp_free;
-  uint64_t ds_full[2], ds_free[2], dq_full, dq_free, mma_done, drain;
+  uint8_t q[kStages][kQTileBytes];
+  uint8_t dO[kStages][kQTileBytes];
+  uint8_t ds[2][kDsBytes];   // dS^T (128-byte swizzled rows)
+  float dq[kQB * kHeadDim];  // dQ_i staging, row-major [query][head dim]
+  float lse2[kStages][kQB];  // LSE * log2(e) of the stage's query rows (+inf: no key)
+  float dlt[kStages][kQB];   // D of the stage's query rows
+  uint64_t unit_full[2], unit_empty[2];
+  uint64_t kv_full, kv_empty, qdo_full[kStages], qdo_empty[kStages];
+  uint64_t st_full[2], pt_full[2], dp_full, dp_free, ds_full[2], ds_free[2], dq_full, dq_free;
+  uint64_t acc_done, acc_free, drain;
+  int unit_slot[2][4];
   uint32_t tmem_base;
   ptx::Abort abort;
 };
 
-__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, BwdSmem& sm, const KParams& p) {
-  bool ok = ptx::mbar_wait(bar, parity, &sm.abort, p.status, p.wait_limit_ns);
-  return __all_sync(0xffffffffu, ok);
-}
+static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory per CTA is at most 227 KiB");
 
-__device__ __forceinline__ bool wait_one(uint64_t* bar, uint32_t parity, BwdSmem& sm, const KParams& p) {
-  return ptx::mbar_wait(bar, parity, &sm.abort, p.status, p.wait_limit_ns);
-}
-
-__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity, const KParams& p) {
-  ptx::Abort none;
-  none.flag = 0;
-  ptx::mbar_wait(bar, parity, &none, p.status, p.wait_limit_ns);
-}
-
-__device__ __forceinline__ void red_add_f32(float* addr, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
-}
-
-// Writes 32 float32 accumulator columns (x scale) of this thread's row as bf16
-// into a 256-byte-row staging tile, 16-byte chunk c of row r at chunk c ^ (r & 15).
-__device__ __forceinline__ void stage_row_chunks(uint8_t* stage, int r, int cc, const uint32_t (&v)[32],
-                                                 float scale) {
-#pragma unroll
-  for (int w4 = 0; w4 < 4; ++w4) {
-    uint4 o;
-    o.x = ptx::pack_bf16x2(__uint_as_float(v[w4 * 8 + 0]) * scale, __uint_as_float(v[w4 * 8 + 1]) * scale);
-    o.y = ptx::pack_bf16x2(__uint_as_float(v[w4 * 8 + 2]) * scale, __uint_as_float(v[w4 * 8 + 3]) * scale);
-    o.z = ptx::pack_bf16x2(__uint_as_float(v[w4 * 8 + 4]) * scale, __uint_as_float(v[w4 * 8 + 5]) * scale);
-    o.w = ptx::pack_bf16x2(__uint_as_float(v[w4 * 8 + 6]) * scale, __uint_as_float(v[w4 * 8 + 7]) * scale);
-    const int ch = cc * 4 + w4;
-    *reinterpret_cast<uint4*>(stage + r * 256 + ((ch ^ (r & 15)) * 16)) = o;
+struct Waiter {
+  Smem& sm;
+  const KParams& p;
+  __device__ bool one(uint64_t* bar, uint32_t parity) {
+    return ptx::mbar_wait(bar, parity, &sm.abort, p.status, p.wait_limit_ns);
   }
+  __device__ bool warp(uint64_t* bar, uint32_t parity) {
+    const bool ok = one(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+  }
+  __device__ void drain(uint64_t* bar, uint32_t parity) {
+    ptx::Abort none;
+    none.flag = 0;
+    ptx::mbar_wait(bar, parity, &none, p.status, p.wait_limit_ns);
+  }
+};
+
+__device__ __forceinline__ bool read_unit(const Smem& sm, int slot, Unit& un) {
+  const volatile int* s = sm.unit_slot[slot];
+  un.seq = s[0];
+  un.head = s[1];
+  un.tile = s[2];
+  return s[3] != 0;
 }
 
-// One warp: reads its 32 rows of a 128-column accumulator from tensor memory
-// (or zeros), scales, rounds to bf16 and writes them to global memory rows
-// k0 + row (row < len) of head g through a staging tile.
-__device__ __forceinline__ void write_kv_rows(uint32_t taddr_row, bool have, float scale, uint8_t* stage,
-                                              int wq, int lane, const KParams& p, const SeqInfo& si, int g,
-                                              int k0, void* out) {
-  const int r = wq * 32 + lane;
+// AND of `pred` over the 128 threads of the dQ warps (named barrier 1); every
+// one of them reaches it once per step, whatever its own waits returned.
+__device__ __forceinline__ bool dq_group_all(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void dq_group_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// One warp writes its 32 key rows of a 128-column accumulator (x scale, bf16)
+// straight from tensor memory to global memory rows k0 + row < len of head g.
+__device__ __forceinline__ void store_kv_rows(uint32_t taddr_row, bool have, float scale, int row,
+                                              const KParams& p, const SeqInfo& si, int g, int k0, void* out) {
+  const bool ok = k0 + row < si.len;
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + (ok ? kv_off(p, si, g, k0 + row) : 0);
 #pragma unroll
   for (int cc = 0; cc < 4; ++cc) {
     uint32_t v[32];
@@ -115,45 +134,48 @@ __device__ __forceinline__ void write_kv_rows(uint32_t taddr_row, bool have, flo
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = 0u;
     }
-    stage_row_chunks(stage, r, cc, v, scale);
-  }
-  __syncwarp();
-  __nv_bfloat16* O = static_cast<__nv_bfloat16*>(out);
-#pragma unroll 4
-  for (int it = 0; it < 16; ++it) {
-    const int row = wq * 32 + it * 2 + (lane >> 4), ch = lane & 15;
-    if (k0 + row < si.len) {
-      const uint4 v4 = *reinterpret_cast<const uint4*>(stage + row * 256 + ((ch ^ (row & 15)) * 16));
-      *reinterpret_cast<uint4*>(O + kv_off(p, si, g, k0 + row) + ch * 8) = v4;
+    if (ok) {
+#pragma unroll
+      for (int w4 = 0; w4 < 4; ++w4) {
+        uint4 o;
+        o.x = ptx::pack_bf16x2(__uint_as_float(v[w4 * 8 + 0]) * scale, __uint_as_float(v[w4 * 8 + 1]) * scale);
+        o.y = ptx::pack_bf16x2(__uint_as_float(v[w4 * 8 + 2]) * scale, __uint_as_float(v[w4 * 8 + 3]) * scale);
+        o.z = ptx::pack_bf16x2(__uint_as_float(v[w4 * 8 + 4]) * scale, __uint_as_float(v[w4 * 8 + 5]) * scale);
+        o.w = ptx::pack_bf16x2(__uint_as_float(v[w4 * 8 + 6]) * scale, __uint_as_float(v[w4 * 8 + 7]) * scale);
+        *reinterpret_cast<uint4*>(dst + cc * 32 + w4 * 8) = o;
+      }
     }
   }
 }
 
-__global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd(const __grid_constant__ BwdArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  BwdSmem& sm = *reinterpret_cast<BwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const KParams& p = a.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Unit u = p.units[blockIdx.x];
-  const SeqInfo si = seq_info(p, u.seq);
-  const int g = u.head;
-  const int kt = u.tile, k0 = kt * kTile;
+  Waiter W{sm, p};
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(&sm.kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&sm.qdo_full[s], 2);  // TMA transaction arrival + LSE/D rows written
       ptx::mbar_init(&sm.qdo_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(&sm.unit_full[s], 1);
+      ptx::mbar_init(&sm.unit_empty[s], 9);  // MMA thread + 4 P/dS warps + 4 dQ warps
       ptx::mbar_init(&sm.st_full[s], 1);
       ptx::mbar_init(&sm.pt_full[s], 4);
       ptx::mbar_init(&sm.ds_full[s], 4);
       ptx::mbar_init(&sm.ds_free[s], 1);
     }
+    ptx::mbar_init(&sm.kv_full, 1);
+    ptx::mbar_init(&sm.kv_empty, 1);
     ptx::mbar_init(&sm.dp_full, 1);
     ptx::mbar_init(&sm.dp_free, 4);
     ptx::mbar_init(&sm.dq_full, 1);
     ptx::mbar_init(&sm.dq_free, 4);
-    ptx::mbar_init(&sm.mma_done, 1);
+    ptx::mbar_init(&sm.acc_done, 1);
+    ptx::mbar_init(&sm.acc_free, 8);  // dK writers (4 warps) + dV writers (4 warps)
     ptx::mbar_init(&sm.drain, 1);
     sm.abort.flag = 0;
     ptx::fence_mbar_init();
@@ -166,34 +188,52 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd(const __grid_constant
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-
-  BwdSteps steps;
-  steps.init(p, si.len, kt);
-  int n_steps = 0;
-  {
-    BwdSteps t = steps;
-    int hh, qb, bits;
-    while (t.next(hh, qb, bits)) ++n_steps;
-  }
   const bool elem_causal = p.mask == kMaskCausal || (p.mask == kMaskBlock && p.causal_in_block);
 
   if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    int last_phase[2] = {-1, -1};
-    if (n_steps > 0) {
+    // ================================================================ producer
+    uint32_t n_units = 0, n_steps = 0;
+    int last_qdo_phase[kStages] = {-1, -1, -1};
+    bool kv_loaded = false;
+    uint32_t last_kv_phase = 0;
+    for (;;) {
+      const int slot = n_units & 1;
+      if (!W.warp(&sm.unit_empty[slot], ((n_units >> 1) & 1) ^ 1)) break;
+      int idx = 0;
+      if (lane == 0) idx = atomicAdd(p.unit_counter, 1);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      const bool valid = idx < p.n_units;
+      Unit un{0, 0, 0, 0};
+      if (valid) un = p.units[idx];
       if (lane == 0) {
-        ptx::tma_prefetch_desc(&a.tq);
-        ptx::tma_prefetch_desc(&a.tdo);
+        volatile int* s = sm.unit_slot[slot];
+        s[0] = un.seq;
+        s[1] = un.head;
+        s[2] = un.tile;
+        s[3] = valid ? 1 : 0;
+        ptx::mbar_arrive(&sm.unit_full[slot]);
+      }
+      if (!valid) break;
+      const SeqInfo si = seq_info(p, un.seq);
+      const int g = un.head, k0 = un.tile * kTile;
+      // K and V of the unit, once the previous unit's products are done with them
+      if (!W.warp(&sm.kv_empty, (n_units & 1) ^ 1)) break;
+      if (lane == 0) {
         ptx::mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
         tma_tile(sm.k, &a.tk, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b, kHalfTileBytes);
         tma_tile(sm.v, &a.tv, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b, kHalfTileBytes);
       }
-      BwdSteps t = steps;
-      int hh, qb, bits, i = 0;
-      while (t.next(hh, qb, bits)) {
-        const int st = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (!wait_warp(&sm.qdo_empty[st], ph ^ 1, sm, p)) break;
+      kv_loaded = true;
+      last_kv_phase = n_units & 1;
+      ++n_units;
+      BwdSteps steps;
+      steps.init(p, si.len, un.tile);
+      int hh, qb, bits;
+      bool ok = true;
+      while (steps.next(hh, qb, bits)) {
+        const int st = n_steps % kStages;
+        const uint32_t ph = (n_steps / kStages) & 1;
+        if (!W.warp(&sm.qdo_empty[st], ph ^ 1)) { ok = false; break; }
         const int h = g * p.group + hh, q0 = qb * kQB;
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(&sm.qdo_full[st], 2 * kQTileBytes);
@@ -215,84 +255,103 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd(const __grid_constant
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sm.qdo_full[st]);
-        last_phase[st] = (int)ph;
-        ++i;
+        last_qdo_phase[st] = (int)ph;
+        ++n_steps;
       }
-      if (lane == 0) {
-        wait_drain(&sm.kv_full, 0, p);
-        for (int s = 0; s < 2; ++s)
-          if (last_phase[s] >= 0) wait_drain(&sm.qdo_full[s], (uint32_t)last_phase[s], p);
-      }
+      if (!ok) break;
+    }
+    if (lane == 0) {
+      if (kv_loaded) W.drain(&sm.kv_full, last_kv_phase);
+      for (int s = 0; s < kStages; ++s)
+        if (last_qdo_phase[s] >= 0) W.drain(&sm.qdo_full[s], (uint32_t)last_qdo_phase[s]);
     }
   } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+    // ================================================================ MMA issuer
     if (lane == 0) {
-      if (n_steps > 0) {
-        constexpr uint32_t id_st = ptx::idesc_bf16(128, 64, false, false);   // S^T, dP^T
-        constexpr uint32_t id_acc = ptx::idesc_bf16(128, 128, false, true);  // dV, dK
-        constexpr uint32_t id_dq = ptx::idesc_bf16(128, 64, true, true);     // dQ^T
-        const uint32_t k_addr = ptx::smem_u32(sm.k), v_addr = ptx::smem_u32(sm.v);
-        bool ok = wait_one(&sm.kv_full, 0, sm, p);
+      constexpr uint32_t id_st = ptx::idesc_bf16(128, 64, false, false);   // S^T, dP^T
+      constexpr uint32_t id_acc = ptx::idesc_bf16(128, 128, false, true);  // dV, dK
+      constexpr uint32_t id_dq = ptx::idesc_bf16(128, 64, true, true);     // dQ^T
+      const uint32_t k_addr = ptx::smem_u32(sm.k), v_addr = ptx::smem_u32(sm.v);
+      uint32_t n_units = 0, gi = 0;  // gi: global step counter (all units)
+      bool ok = true;
+
+      auto issue_s = [&](uint32_t i) -> bool {  // S^T_i = K Q_i^T
+        const int st = i & 1, qs = i % kStages;
+        if (!W.one(&sm.qdo_full[qs], (i / kStages) & 1)) return false;
         ptx::tc_fence_after();
-
-        // S^T_i = K Q_i^T: A = K (key rows, head dim contiguous), B = Q_i (query rows).
-        auto issue_s = [&](int i) -> bool {
-          const int st = i & 1;
-          if (!wait_one(&sm.qdo_full[st], (i >> 1) & 1, sm, p)) return false;
-          ptx::tc_fence_after();
-          const uint32_t q_addr = ptx::smem_u32(sm.q[st]);
+        const uint32_t q_addr = ptx::smem_u32(sm.q[qs]);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = ptx::sdesc_sw128(k_addr + (kk >> 2) * kHalfTileBytes + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = ptx::sdesc_sw128(q_addr + (kk >> 2) * kQBoxBytes + (kk & 3) * 32, 16, 1024);
-            ptx::mma_ss(tmem + kColS + st * 64, ad, bd, id_st, kk > 0 ? 1u : 0u);
-          }
-          ptx::mma_commit(&sm.st_full[st]);
-          return true;
-        };
-        // dP^T_i = V dO_i^T (the stage is already known to be loaded).
-        auto issue_dp = [&](int i) -> bool {
-          const int st = i & 1;
-          if (i > 0 && !wait_one(&sm.dp_free, (i - 1) & 1, sm, p)) return false;
-          ptx::tc_fence_after();
-          const uint32_t do_addr = ptx::smem_u32(sm.dO[st]);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = ptx::sdesc_sw128(k_addr + (kk >> 2) * kHalfTileBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = ptx::sdesc_sw128(q_addr + (kk >> 2) * kQBoxBytes + (kk & 3) * 32, 16, 1024);
+          ptx::mma_ss(tmem + kColS + st * 64, ad, bd, id_st, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(&sm.st_full[st]);
+        return true;
+      };
+      auto issue_dp = [&](uint32_t i) -> bool {  // dP^T_i = V dO_i^T (stage known loaded)
+        const int qs = i % kStages;
+        if (i > 0 && !W.one(&sm.dp_free, (i - 1) & 1)) return false;
+        ptx::tc_fence_after();
+        const uint32_t do_addr = ptx::smem_u32(sm.dO[qs]);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = ptx::sdesc_sw128(v_addr + (kk >> 2) * kHalfTileBytes + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = ptx::sdesc_sw128(do_addr + (kk >> 2) * kQBoxBytes + (kk & 3) * 32, 16, 1024);
-            ptx::mma_ss(tmem + kColDP, ad, bd, id_st, kk > 0 ? 1u : 0u);
-          }
-          ptx::mma_commit(&sm.dp_full);
-          return true;
-        };
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = ptx::sdesc_sw128(v_addr + (kk >> 2) * kHalfTileBytes + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = ptx::sdesc_sw128(do_addr + (kk >> 2) * kQBoxBytes + (kk & 3) * 32, 16, 1024);
+          ptx::mma_ss(tmem + kColDP, ad, bd, id_st, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(&sm.dp_full);
+        return true;
+      };
 
-        ok = ok && issue_s(0) && issue_dp(0);
-        for (int i = 0; ok && i < n_steps; ++i) {
-          const int st = i & 1;
-          if (i + 1 < n_steps && !issue_s(i + 1)) { ok = false; break; }
-          // dV += P^T_i dO_i: A = P^T from tensor memory, B = dO_i as (head dim, query) MN-major.
-          if (!wait_one(&sm.pt_full[st], (i >> 1) & 1, sm, p)) { ok = false; break; }
+      for (;;) {
+        const int slot = n_units & 1;
+        if (!W.one(&sm.unit_full[slot], (n_units >> 1) & 1)) { ok = false; break; }
+        Unit un;
+        const bool valid = read_unit(sm, slot, un);
+        ptx::mbar_arrive(&sm.unit_empty[slot]);
+        if (!valid) break;
+        const SeqInfo si = seq_info(p, un.seq);
+        int n = 0;
+        {
+          BwdSteps t;
+          t.init(p, si.len, un.tile);
+          int hh, qb, bits;
+          while (t.next(hh, qb, bits)) ++n;
+        }
+        if (!W.one(&sm.kv_full, n_units & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+        if (n > 0) ok = issue_s(gi) && issue_dp(gi);
+        for (int s = 0; ok && s < n; ++s) {
+          const uint32_t i = gi + s;
+          const int st = i & 1, qs = i % kStages;
+          if (s + 1 < n && !issue_s(i + 1)) { ok = false; break; }
+          // dV += P^T_i dO_i: A = P^T from tensor memory, B = dO_i as (head dim, query) MN-major
+          if (!W.one(&sm.pt_full[st], (i >> 1) & 1)) { ok = false; break; }
+          // before the unit's first dV / dK product: the previous unit's epilogue
+          // has read both accumulators
+          if (s == 0 && !W.one(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
           ptx::tc_fence_after();
-          const uint32_t q_addr = ptx::smem_u32(sm.q[st]), do_addr = ptx::smem_u32(sm.dO[st]);
+          const uint32_t q_addr = ptx::smem_u32(sm.q[qs]), do_addr = ptx::smem_u32(sm.dO[qs]);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bd = ptx::sdesc_sw128(do_addr + kk * 2048, kQBoxBytes, 1024);
-            ptx::mma_ts(tmem + kColDV, tmem + kColS + st * 64 + kk * 8, bd, id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_ts(tmem + kColDV, tmem + kColS + st * 64 + kk * 8, bd, id_acc, (s > 0 || kk > 0) ? 1u : 0u);
           }
-          if (i + 1 < n_steps && !issue_dp(i + 1)) { ok = false; break; }
-          // dK += dS^T_i Q_i: A = dS^T (key rows, query contiguous), B = Q_i MN-major.
-          if (!wait_one(&sm.ds_full[st], (i >> 1) & 1, sm, p)) { ok = false; break; }
+          if (s + 1 < n && !issue_dp(i + 1)) { ok = false; break; }
+          // dK += dS^T_i Q_i: A = dS^T (key rows, query contiguous), B = Q_i MN-major
+          if (!W.one(&sm.ds_full[st], (i >> 1) & 1)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t ds_addr = ptx::smem_u32(sm.ds[st]);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = ptx::sdesc_sw128(ds_addr + kk * 32, 16, 1024);
             const uint64_t bd = ptx::sdesc_sw128(q_addr + kk * 2048, kQBoxBytes, 1024);
-            ptx::mma_ss(tmem + kColDK, ad, bd, id_acc, (i > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_ss(tmem + kColDK, ad, bd, id_acc, (s > 0 || kk > 0) ? 1u : 0u);
           }
           // dQ_i^T = K^T dS^T_i: A = K^T (head dim contiguous: MN-major), B = dS^T as
-          // (query, key) with query contiguous: MN-major.
-          if (i > 0 && !wait_one(&sm.dq_free, (i - 1) & 1, sm, p)) { ok = false; break; }
+          // (query, key) with query contiguous: MN-major
+          if (i > 0 && !W.one(&sm.dq_free, (i - 1) & 1)) { ok = false; break; }
           ptx::tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -301,135 +360,177 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd(const __grid_constant
             ptx::mma_ss(tmem + kColDQ, ad, bd, id_dq, kk > 0 ? 1u : 0u);
           }
           ptx::mma_commit(&sm.dq_full);
-          ptx::mma_commit(&sm.qdo_empty[st]);
+          ptx::mma_commit(&sm.qdo_empty[qs]);
           ptx::mma_commit(&sm.ds_free[st]);
         }
+        if (!ok) break;
+        if (n == 0 && !W.one(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
+        gi += n;
+        ptx::mma_commit(&sm.kv_empty);
+        ptx::mma_commit(&sm.acc_done);
+        ++n_units;
       }
-      ptx::mma_commit(&sm.mma_done);
+      (void)ok;
       ptx::mma_commit(&sm.drain);
-      wait_drain(&sm.drain, 0, p);
+      W.drain(&sm.drain, 0);
     }
   } else if (warp < 4) {
-    // ------------------------------------------------------------ P^T / dS^T warps
+    // ================================================================ P^T / dS^T warps
     const int t = threadIdx.x;  // key row in the tile = TMEM lane
-    const int kj = k0 + t;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const float c = p.scale_log2;
     const int key_half = t >= 64 ? 1 : 0;
-    bool ok = true;
-    BwdSteps s = steps;
-    int hh, qb, bits, i = 0;
-    while (s.next(hh, qb, bits)) {
-      const int st = i & 1;
-      const int q0 = qb * kQB;
-      if (!wait_warp(&sm.qdo_full[st], (i >> 1) & 1, sm, p) || !wait_warp(&sm.st_full[st], (i >> 1) & 1, sm, p)) {
-        ok = false;
-        break;
-      }
-      ptx::tc_fence_after();
-      uint32_t sr[64];
-      ptx::tmem_ld32(tmem + lane_base + kColS + st * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      ptx::tmem_ld32(tmem + lane_base + kColS + st * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      ptx::tmem_ld_wait();
-      const bool need_mask = (k0 + kTile > si.len) || (elem_causal && q0 < k0 + kTile - 1) || bits != 3;
-      const bool row_listed = (bits >> key_half) & 1;
-      float pv[64];
-      uint32_t pk[32];
+    uint32_t n_units = 0, i = 0;
+    for (;;) {
+      const int slot = n_units & 1;
+      if (!W.warp(&sm.unit_full[slot], (n_units >> 1) & 1)) break;
+      Unit un;
+      const bool valid = read_unit(sm, slot, un);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sm.unit_empty[slot]);
+      if (!valid) break;
+      const SeqInfo si = seq_info(p, un.seq);
+      const int k0 = un.tile * kTile, kj = k0 + t;
+      BwdSteps steps;
+      steps.init(p, si.len, un.tile);
+      int hh, qb, bits, n = 0;
+      bool ok = true;
+      while (steps.next(hh, qb, bits)) {
+        const int st = i & 1, qs = i % kStages;
+        const int q0 = qb * kQB;
+        if (!W.warp(&sm.qdo_full[qs], (i / kStages) & 1) || !W.warp(&sm.st_full[st], (i >> 1) & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+        uint32_t sr[64];
+        ptx::tmem_ld32(tmem + lane_base + kColS + st * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+        ptx::tmem_ld32(tmem + lane_base + kColS + st * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+        ptx::tmem_ld_wait();
+        const bool need_mask = (k0 + kTile > si.len) || (elem_causal && q0 < k0 + kTile - 1) || bits != 3;
+        const bool row_listed = (bits >> key_half) & 1;
+        float pv[64];
+        uint32_t pk[32];
 #pragma unroll
-      for (int cc = 0; cc < 64; ++cc) {
-        bool keep = true;
-        if (need_mask) {
-          keep = row_listed && kj < si.len;
-          if (elem_causal) keep = keep && kj <= q0 + cc;
+        for (int cc = 0; cc < 64; ++cc) {
+          bool keep = true;
+          if (need_mask) {
+            keep = row_listed && kj < si.len;
+            if (elem_causal) keep = keep && kj <= q0 + cc;
+          }
+          pv[cc] = keep ? fast_exp2(fmaf(__uint_as_float(sr[cc]), c, -sm.lse2[qs][cc])) : 0.f;
         }
-        pv[cc] = keep ? fast_exp2(__uint_as_float(sr[cc]) * c - sm.lse2[st][cc]) : 0.f;
-      }
 #pragma unroll
-      for (int w = 0; w < 32; ++w) pk[w] = ptx::pack_bf16x2(pv[2 * w], pv[2 * w + 1]);
-      ptx::tmem_st32(tmem + lane_base + kColS + st * 64, pk);
-      ptx::tmem_st_wait();
+        for (int w = 0; w < 32; ++w) pk[w] = ptx::pack_bf16x2(pv[2 * w], pv[2 * w + 1]);
+        ptx::tmem_st32(tmem + lane_base + kColS + st * 64, pk);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.pt_full[st]);
+
+        if (!W.warp(&sm.dp_full, i & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+        uint32_t dr[64];
+        ptx::tmem_ld32(tmem + lane_base + kColDP, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+        ptx::tmem_ld32(tmem + lane_base + kColDP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+        ptx::tmem_ld_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.dp_free);
+
+        if (!W.warp(&sm.ds_free[st], ((i >> 1) & 1) ^ 1)) { ok = false; break; }
+        uint8_t* dsrow = sm.ds[st] + t * 128;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          float d[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int cc = ch * 8 + e;
+            d[e] = pv[cc] * (__uint_as_float(dr[cc]) - sm.dlt[qs][cc]);
+          }
+          uint4 o;
+          o.x = ptx::pack_bf16x2(d[0], d[1]);
+          o.y = ptx::pack_bf16x2(d[2], d[3]);
+          o.z = ptx::pack_bf16x2(d[4], d[5]);
+          o.w = ptx::pack_bf16x2(d[6], d[7]);
+          *reinterpret_cast<uint4*>(dsrow + ((ch ^ (t & 7)) * 16)) = o;
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.ds_full[st]);
+        ++i;
+        ++n;
+      }
+      if (!ok) break;
+      // dK epilogue
+      if (!W.warp(&sm.acc_done, n_units & 1)) break;
+      ptx::tc_fence_after();
+      store_kv_rows(tmem + lane_base + kColDK, n > 0, p.scale, t, p, si, un.head, k0, p.dk);
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&sm.pt_full[st]);
-
-      if (!wait_warp(&sm.dp_full, i & 1, sm, p)) {
-        ok = false;
-        break;
-      }
-      ptx::tc_fence_after();
-      uint32_t dr[64];
-      ptx::tmem_ld32(tmem + lane_base + kColDP, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
-      ptx::tmem_ld32(tmem + lane_base + kColDP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
-      ptx::tmem_ld_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&sm.dp_free);
-
-      if (!wait_warp(&sm.ds_free[st], ((i >> 1) & 1) ^ 1, sm, p)) {
-        ok = false;
-        break;
-      }
-      uint8_t* dsrow = sm.ds[st] + t * 128;
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        uint4 o;
-        float d[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int cc = ch * 8 + e;
-          d[e] = pv[cc] * (__uint_as_float(dr[cc]) - sm.dlt[st][cc]);
-        }
-        o.x = ptx::pack_bf16x2(d[0], d[1]);
-        o.y = ptx::pack_bf16x2(d[2], d[3]);
-        o.z = ptx::pack_bf16x2(d[4], d[5]);
-        o.w = ptx::pack_bf16x2(d[6], d[7]);
-        *reinterpret_cast<uint4*>(dsrow + ((ch ^ (t & 7)) * 16)) = o;
-      }
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&sm.ds_full[st]);
-      ++i;
-    }
-    // dK epilogue
-    if (ok && wait_warp(&sm.mma_done, 0, sm, p) && !sm.abort.flag) {
-      ptx::tc_fence_after();
-      write_kv_rows(tmem + lane_base + kColDK, n_steps > 0, p.scale, sm.q[0], warp, lane, p, si, g, k0, p.dk);
+      if (lane == 0) ptx::mbar_arrive(&sm.acc_free);
+      ++n_units;
     }
   } else {
-    // ------------------------------------------------------------ dQ warps
+    // ================================================================ dQ warps
+    // These four warps also meet at named barrier 1, which has no time limit, so
+    // every wait's outcome is first made the same for all 128 threads
+    // (dq_group_all) and the group leaves its loops together.
     const int wq = warp - 4;
     const int d = wq * 32 + lane;  // head-dim column = TMEM lane
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    bool ok = true;
-    BwdSteps s = steps;
-    int hh, qb, bits, i = 0;
-    while (s.next(hh, qb, bits)) {
-      if (!wait_warp(&sm.dq_full, i & 1, sm, p)) {
-        ok = false;
-        break;
+    const bool issuer = threadIdx.x == 128;
+    uint32_t n_units = 0, i = 0;
+    bool group_ok = true;
+    for (;;) {
+      const int slot = n_units & 1;
+      if (!dq_group_all(W.warp(&sm.unit_full[slot], (n_units >> 1) & 1))) break;
+      Unit un;
+      const bool valid = read_unit(sm, slot, un);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sm.unit_empty[slot]);
+      if (!valid) break;
+      const SeqInfo si = seq_info(p, un.seq);
+      const int g = un.head, k0 = un.tile * kTile;
+      BwdSteps steps;
+      steps.init(p, si.len, un.tile);
+      int hh, qb, bits, n = 0;
+      while (steps.next(hh, qb, bits)) {
+        if (!dq_group_all(W.warp(&sm.dq_full, i & 1))) { group_ok = false; break; }
+        ptx::tc_fence_after();
+        uint32_t vr[64];
+        ptx::tmem_ld32(tmem + lane_base + kColDQ, *reinterpret_cast<uint32_t(*)[32]>(&vr[0]));
+        ptx::tmem_ld32(tmem + lane_base + kColDQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&vr[32]));
+        ptx::tmem_ld_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.dq_free);
+        // the staging tile is free once the previous reduce has read it
+        if (issuer) ptx::bulk_wait_group_read<0>();
+        dq_group_sync();
+#pragma unroll
+        for (int cc = 0; cc < 64; ++cc) sm.dq[cc * kHeadDim + d] = __uint_as_float(vr[cc]);
+        ptx::fence_proxy_async_smem();
+        dq_group_sync();
+        if (issuer) {
+          const int h = g * p.group + hh, q0 = qb * kQB;
+          // rows past the sequence end carry exact zeros (their P is 0); the map
+          // clips rows past the tensor end
+          if (a.acc_rows_inner) ptx::tma_reduce_add_4d(&a.tacc, sm.dq, 0, (int)(si.tok0 + q0), h, si.b);
+          else ptx::tma_reduce_add_4d(&a.tacc, sm.dq, 0, h, (int)(si.tok0 + q0), 0);
+          ptx::bulk_commit_group();
+        }
+        ++i;
+        ++n;
       }
+      if (!group_ok) break;
+      // dV epilogue
+      if (!dq_group_all(W.warp(&sm.acc_done, n_units & 1))) break;
       ptx::tc_fence_after();
-      uint32_t vr[64];
-      ptx::tmem_ld32(tmem + lane_base + kColDQ, *reinterpret_cast<uint32_t(*)[32]>(&vr[0]));
-      ptx::tmem_ld32(tmem + lane_base + kColDQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&vr[32]));
-      ptx::tmem_ld_wait();
+      store_kv_rows(tmem + lane_base + kColDV, n > 0, 1.f, d, p, si, g, k0, p.dv);
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&sm.dq_free);
-      const int h = g * p.group + hh, q0 = qb * kQB;
-      const int nrows = min(kQB, si.len - q0);
-      float* base = p.dq_accum + dqacc_off(p, si, h, q0) + d;
-      const long long rstride = p.varlen ? (long long)p.heads_q * p.head_dim : p.head_dim;
-#pragma unroll
-      for (int cc = 0; cc < 64; ++cc)
-        if (cc < nrows) red_add_f32(base + cc * rstride, __uint_as_float(vr[cc]));
-      ++i;
+      if (lane == 0) ptx::mbar_arrive(&sm.acc_free);
+      ++n_units;
     }
-    // dV epilogue
-    if (ok && wait_warp(&sm.mma_done, 0, sm, p) && !sm.abort.flag) {
-      ptx::tc_fence_after();
-      write_kv_rows(tmem + lane_base + kColDV, n_steps > 0, 1.f, sm.dO[0], wq, lane, p, si, g, k0, p.dv);
-    }
+    if (issuer) ptx::bulk_wait_group<0>();
   }
 
   ptx::tc_fence_before();
@@ -445,26 +546,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) k_tc_bwd(const __grid_constant
 bool tc_bwd_available() { return true; }
 
 cudaError_t launch_tc_bwd(const KParams& p, int sms, cudaStream_t st) {
-  (void)sms;
   if (p.n_units == 0) return cudaSuccess;
   BwdArgs a;
-  TileMap mq, mk, mv, mdo;
+  TileMap mq, mk, mv, mdo, macc;
   cudaError_t e;
   if ((e = make_tile_map(&mq, p.q, p, false, kQB)) != cudaSuccess) return e;
   if ((e = make_tile_map(&mdo, p.dout, p, false, kQB)) != cudaSuccess) return e;
   if ((e = make_tile_map(&mk, p.k, p, true)) != cudaSuccess) return e;
   if ((e = make_tile_map(&mv, p.v, p, true)) != cudaSuccess) return e;
+  if ((e = make_acc_map(&macc, p.dq_accum, p, kQB)) != cudaSuccess) return e;
   a.tq = mq.map;
   a.tdo = mdo.map;
   a.tk = mk.map;
   a.tv = mv.map;
+  a.tacc = macc.map;
   a.q_rows_inner = mq.rows_inner;
   a.kv_rows_inner = mk.rows_inner;
+  a.acc_rows_inner = macc.rows_inner;
   a.p = p;
-  const size_t smem = sizeof(BwdSmem) + 1024;
+  const size_t smem = sizeof(Smem) + 1024;
   e = cudaFuncSetAttribute(k_tc_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_tc_bwd<<<p.n_units, kBwdThreads, smem, st>>>(a);
+  const int grid = p.n_units < sms ? p.n_units : sms;
+  k_tc_bwd<<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -27,68 +27,6 @@ __device__ __forceinline__ void tma_tile(void* dst, const CUtensorMap* map, int 
 // Row coordinate and batch coordinate of position `pos` of a sequence in a tile map.
 __device__ __forceinline__ int map_row(const SeqInfo& s, int pos) { return (int)(s.tok0 + pos); }
 
-// The score tiles a forward unit (one 128-row query tile) visits, in ascending
-// key order, with a 4-bit mask of which 64x64 sub-blocks are listed:
-//   bit 0 (rows 0-63, keys 0-63), bit 1 (rows 0-63, keys 64-127),
-//   bit 2 (rows 64-127, keys 0-63), bit 3 (rows 64-127, keys 64-127).
-// Dense and causal units visit tiles 0 .. n-1 with all four bits set.
-struct KvTileList {
-  int mode;      // kMaskNone / kMaskCausal: dense range; kMaskBlock: merged lists
-  int n_dense;   // dense range length
-  int it;
-  const int* col;
-  int ia, ea, ib, eb;  // block lists of the two 64-row query blocks
-  int nblk;            // 64-blocks in the sequence (columns beyond are ignored)
-
-  __device__ void init(const KParams& p, int len, int q0) {
-    mode = p.mask;
-    it = 0;
-    nblk = (len + 63) / 64;
-    if (mode == kMaskNone) {
-      n_dense = (len + kTile - 1) / kTile;
-    } else if (mode == kMaskCausal) {
-      const int qlast = min(len, q0 + kTile) - 1;
-      n_dense = qlast / kTile + 1;
-    } else {
-      col = p.col_idx;
-      const int rb0 = q0 / 64, rb1 = rb0 + 1;
-      ia = p.row_ptr[rb0];
-      ea = p.row_ptr[rb0 + 1];
-      if (rb1 < p.n_row_blocks && rb1 * 64 < len) {
-        ib = p.row_ptr[rb1];
-        eb = p.row_ptr[rb1 + 1];
-      } else {
-        ib = eb = 0;
-      }
-    }
-  }
-
-  // Next tile: key tile index and sub-block bits.  False when exhausted.
-  __device__ bool next(int& kt, int& bits) {
-    if (mode != kMaskBlock) {
-      if (it >= n_dense) return false;
-      kt = it++;
-      bits = 0xF;
-      return true;
-    }
-    const int a = (ia < ea && col[ia] < nblk) ? col[ia] : INT_MAX;
-    const int b = (ib < eb && col[ib] < nblk) ? col[ib] : INT_MAX;
-    const int m = a < b ? a : b;
-    if (m == INT_MAX) return false;
-    kt = m >> 1;
-    bits = 0;
-    while (ia < ea && col[ia] < nblk && (col[ia] >> 1) == kt) {
-      bits |= 1 << (col[ia] & 1);
-      ++ia;
-    }
-    while (ib < eb && col[ib] < nblk && (col[ib] >> 1) == kt) {
-      bits |= 4 << (col[ib] & 1);
-      ++ib;
-    }
-    return true;
-  }
-};
-
 }  // namespace gbattn
 
 namespace gbattn {
@@ -194,23 +132,23 @@ namespace gbattn {
 // four bits are all clear.  Dense and causal units list every key tile up to
 // the last one any of their rows sees; a query tile past the sequence end, or
 // (causal) whose rows all precede a key tile, gets clear bits for it.
+template <bool kSparse>
 struct KvTileList2 {
-  int mode, n_dense, it, len, q0;
+  int n_dense, it, len, q0;
   const int* col;
-  int s[4], e[4];
+  int s[kSparse ? 4 : 1], e[kSparse ? 4 : 1];
   int nblk;
+  bool causal;
 
   __device__ void init(const KParams& p, int len_, int q0_) {
-    mode = p.mask;
     len = len_;
     q0 = q0_;
     it = 0;
     nblk = (len + 63) / 64;
+    causal = p.mask == kMaskCausal;
     const int last = min(len, q0 + 2 * kTile) - 1;
-    if (mode == kMaskNone) {
-      n_dense = (len + kTile - 1) / kTile;
-    } else if (mode == kMaskCausal) {
-      n_dense = last / kTile + 1;
+    if constexpr (!kSparse) {
+      n_dense = causal ? last / kTile + 1 : (len + kTile - 1) / kTile;
     } else {
       n_dense = 0;
       col = p.col_idx;
@@ -228,7 +166,7 @@ struct KvTileList2 {
   }
 
   __device__ bool next(int& kt, int& bits) {
-    if (mode != kMaskBlock) {
+    if constexpr (!kSparse) {
       if (it >= n_dense) return false;
       kt = it++;
       bits = 0;
@@ -237,25 +175,26 @@ struct KvTileList2 {
         const int r0 = q0 + q * kTile;
         if (r0 >= len) continue;
         const int rl = min(len, r0 + kTile) - 1;
-        if (mode == kMaskCausal && kt * kTile > rl) continue;
+        if (causal && kt * kTile > rl) continue;
         bits |= 0xF << (4 * q);
       }
       return true;
+    } else {
+      int m = INT_MAX;
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        if (s[r] < e[r] && col[s[r]] < nblk) m = min(m, col[s[r]]);
+      if (m == INT_MAX) return false;
+      kt = m >> 1;
+      bits = 0;
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        while (s[r] < e[r] && col[s[r]] < nblk && (col[s[r]] >> 1) == kt) {
+          bits |= 1 << (2 * r + (col[s[r]] & 1));
+          ++s[r];
+        }
+      return true;
     }
-    int m = INT_MAX;
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-      if (s[r] < e[r] && col[s[r]] < nblk) m = min(m, col[s[r]]);
-    if (m == INT_MAX) return false;
-    kt = m >> 1;
-    bits = 0;
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-      while (s[r] < e[r] && col[s[r]] < nblk && (col[s[r]] >> 1) == kt) {
-        bits |= 1 << (2 * r + (col[s[r]] & 1));
-        ++s[r];
-      }
-    return true;
   }
 };
 

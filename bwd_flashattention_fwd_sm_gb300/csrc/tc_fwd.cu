@@ -1,24 +1,34 @@
-// Forward attention on the fifth-generation tensor cores (sm_103a).
+// Forward attention on the fifth-generation tensor cores (sm_103a):
+// persistent CTAs, two query tiles per CTA sharing every K/V tile.
 //
-// One CTA computes one 128-row query tile of one head (zwxr.cn CANN ops-nn
-// fused-attention article, sections 3.2-3.3: the outer loop takes a query block,
-// the inner loop streams key/value blocks, and a running max and sum correct
-// the softmax across blocks, so the score matrix never leaves the chip; smzdm
-// contest article, section 03, on FlashAttention as tiling plus fusion).
+// The method is the block-by-block attention of the zwxr.cn CANN ops-nn
+// fused-attention article (sections 3.2-3.3): query blocks outside, key/value
+// blocks streamed inside, a running max and sum correcting the softmax, the
+// score matrix never leaving the chip (smzdm contest article, section 03).
 //
-// Warp roles (192 threads):
-//   warp 4     TMA producer: Q once, then K_j and V_j into a two-stage ring
-//              (prefetch the next block while the current one is used: zwxr.cn
-//              article, section 4.1, double buffering).
-//   warp 5     tensor-core issuer: S_j = Q K_j^T into tensor memory (two S
-//              buffers), then O += P_j V_j with P read from tensor memory.  The
-//              matrix products run on the matrix unit (smzdm article, the team
-//              that moved the matmul to the cube unit).
-//   warps 0-3  softmax: thread r owns query row r (TMEM lane r).  It reads S_j,
-//              masks, updates the running max m and sum l, writes P_j as bf16
-//              over S_j in tensor memory (P is never written to shared or global
-//              memory: zwxr.cn article, section 5.4), rescales O when m grew by
-//              more than 2^8, and finally writes O / l and LSE.
+// GB300 mapping.  A unit is 256 query rows of one head: two 128-row tiles Q0,
+// Q1 whose S = Q K^T products share each K/V tile fetched by TMA.  Each query
+// tile has its own softmax warpgroup, S buffer and O accumulator in tensor
+// memory (S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512) columns; P_q is
+// written back as bf16 over S_q and read by the P V product from tensor
+// memory, so P never leaves the SM: zwxr.cn article, section 5.4).  The
+// tensor core alternates between the two tiles: while warpgroup 0 turns S0
+// into P0, the tensor core runs P1 V and the next Q1 K^T, and the other way
+// round, so matrix work overlaps the exponentials.
+//
+// Work distribution.  CTAs are persistent (one per SM); the TMA warp takes the
+// next unit from an atomic counter over the cost-ordered work list and hands
+// it to the other roles through a two-slot ring in shared memory, so long
+// units start first and no SM idles while work remains (zwxr.cn article,
+// section 4.2: whoever finishes first takes the next block; smzdm article,
+// section 02, on uneven work).
+//
+// Warp roles (320 threads):
+//   warps 0-3 / 4-7  softmax for query tile 0 / 1: thread r owns row r (the
+//                    whole 128-column S row in registers; max and sum in 8
+//                    independent partials to keep dependency chains short)
+//   warp 8           TMA producer and unit fetcher
+//   warp 9           tensor-core issuer
 // Every wait is bounded; a CTA that gives up records ATTN_ERR_DEVICE_TIMEOUT,
 // drains its copies and tensor-core work, frees tensor memory and returns.
 #include <cuda.h>
@@ -32,10 +42,9 @@ namespace gbattn {
 namespace {
 
 constexpr int kStages = 2;
-constexpr int kFwdThreads = 192;
+constexpr int kThreads = 320;
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the row max grows by more than 2^8
-constexpr uint32_t kTmemCols = 512;   // S0 [0,128) S1 [128,256) O [256,384)
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kTmemCols = 512;
 
 struct FwdArgs {
   CUtensorMap tq, tk, tv;
@@ -43,56 +52,77 @@ struct FwdArgs {
   KParams p;
 };
 
-struct FwdSmem {
-  uint8_t q[kTileBytes];  // Q tile; O staging in the epilogue
+struct Smem {
+  uint8_t q[2][kTileBytes];
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
-  uint64_t q_full, k_full[kStages], v_full[kStages], kv_empty[kStages];
-  uint64_t s_full[2], p_full[2], o_ready, o_final, drain;
+  uint64_t unit_full[2], unit_empty[2];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t s_full[2], p_full[2], o_final[2], o_free[2];
+  uint64_t drain;
+  int unit_slot[2][4];  // seq, head, 256-row tile, valid
   uint32_t tmem_base;
   ptx::Abort abort;
 };
 
-__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, FwdSmem& sm, const KParams& p) {
-  bool ok = ptx::mbar_wait(bar, parity, &sm.abort, p.status, p.wait_limit_ns);
-  return __all_sync(0xffffffffu, ok);
+static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory per CTA is at most 227 KiB");
+
+struct Waiter {
+  Smem& sm;
+  const KParams& p;
+  __device__ bool one(uint64_t* bar, uint32_t parity) {
+    return ptx::mbar_wait(bar, parity, &sm.abort, p.status, p.wait_limit_ns);
+  }
+  __device__ bool warp(uint64_t* bar, uint32_t parity) {
+    const bool ok = one(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+  }
+  __device__ void drain(uint64_t* bar, uint32_t parity) {
+    ptx::Abort none;
+    none.flag = 0;
+    ptx::mbar_wait(bar, parity, &none, p.status, p.wait_limit_ns);
+  }
+};
+
+// Reads unit slot `u` (after its full barrier); false for the end sentinel.
+__device__ __forceinline__ bool read_unit(const Smem& sm, int slot, Unit& un) {
+  const volatile int* s = sm.unit_slot[slot];
+  un.seq = s[0];
+  un.head = s[1];
+  un.tile = s[2];
+  return s[3] != 0;
 }
 
-// Wait that ignores the abort flag (used only to drain in-flight work).
-__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity, FwdSmem& sm, const KParams& p) {
-  ptx::Abort none;
-  none.flag = 0;
-  ptx::mbar_wait(bar, parity, &none, p.status, p.wait_limit_ns);
-}
-
-__global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant__ FwdArgs a) {
+template <bool kSparse>
+__global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  FwdSmem& sm = *reinterpret_cast<FwdSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const KParams& p = a.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Unit u = p.units[blockIdx.x];
-  const SeqInfo si = seq_info(p, u.seq);
-  const int h = u.head, g = h / p.group;
-  const int q0 = u.tile * kTile;
+  Waiter W{sm, p};
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(&sm.q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&sm.unit_full[i], 1);
+      ptx::mbar_init(&sm.unit_empty[i], 9);  // MMA warp + 8 softmax warps
+      ptx::mbar_init(&sm.q_full[i], 1);
+      ptx::mbar_init(&sm.q_empty[i], 1);
+      ptx::mbar_init(&sm.s_full[i], 1);
+      ptx::mbar_init(&sm.p_full[i], 4);
+      ptx::mbar_init(&sm.o_final[i], 1);
+      ptx::mbar_init(&sm.o_free[i], 4);
+    }
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&sm.k_full[s], 1);
       ptx::mbar_init(&sm.v_full[s], 1);
       ptx::mbar_init(&sm.kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(&sm.s_full[b], 1);
-      ptx::mbar_init(&sm.p_full[b], 4);
-    }
-    ptx::mbar_init(&sm.o_ready, 1);
-    ptx::mbar_init(&sm.o_final, 1);
     ptx::mbar_init(&sm.drain, 1);
     sm.abort.flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     ptx::tmem_alloc(&sm.tmem_base, kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -100,246 +130,367 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-
-  KvTileList tiles;
-  tiles.init(p, si.len, q0);
-  int n_tiles = 0;
-  {
-    KvTileList t = tiles;
-    int kt, bits;
-    while (t.next(kt, bits)) ++n_tiles;
-  }
-
-  if (warp == 4) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && n_tiles > 0) {
-      ptx::tma_prefetch_desc(&a.tq);
-      ptx::tma_prefetch_desc(&a.tk);
-      ptx::tma_prefetch_desc(&a.tv);
-      ptx::mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
-      tma_tile(sm.q, &a.tq, a.q_rows_inner, &sm.q_full, map_row(si, q0), h, si.b, kHalfTileBytes);
-      int last_phase[kStages];
-      for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
-      KvTileList t = tiles;
-      int kt, bits, j = 0;
-      while (t.next(kt, bits)) {
-        const int st = j % kStages;
-        const uint32_t ph = (j / kStages) & 1;
-        if (!ptx::mbar_wait(&sm.kv_empty[st], ph ^ 1, &sm.abort, p.status, p.wait_limit_ns)) break;
-        ptx::mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
-        tma_tile(sm.k[st], &a.tk, a.kv_rows_inner, &sm.k_full[st], map_row(si, kt * kTile), g, si.b,
-                 kHalfTileBytes);
-        ptx::mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
-        tma_tile(sm.v[st], &a.tv, a.kv_rows_inner, &sm.v_full[st], map_row(si, kt * kTile), g, si.b,
-                 kHalfTileBytes);
-        last_phase[st] = (int)ph;
-        ++j;
+  if (warp == 8) {
+    // ================================================================ producer
+    uint32_t n_units_seen = 0, n_q_loads[2] = {0, 0}, n_kv = 0;
+    int last_q_phase[2] = {-1, -1}, last_kv_phase[kStages] = {-1, -1};
+    bool ok = true;
+    for (;;) {
+      const int slot = n_units_seen & 1;
+      // claim the slot (its previous unit has been read by every role)
+      if (!W.warp(&sm.unit_empty[slot], ((n_units_seen >> 1) & 1) ^ 1)) { ok = false; break; }
+      int idx = 0;
+      if (lane == 0) idx = atomicAdd(p.unit_counter, 1);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      const bool valid = idx < p.n_units;
+      Unit un{0, 0, 0, 0};
+      if (valid) un = p.units[idx];
+      if (lane == 0) {
+        volatile int* s = sm.unit_slot[slot];
+        s[0] = un.seq;
+        s[1] = un.head;
+        s[2] = un.tile;
+        s[3] = valid ? 1 : 0;
+        ptx::mbar_arrive(&sm.unit_full[slot]);
       }
-      // every copy this thread started has landed before the CTA winds down
-      wait_drain(&sm.q_full, 0, sm, p);
+      ++n_units_seen;
+      if (!valid) break;
+
+      const SeqInfo si = seq_info(p, un.seq);
+      const int h = un.head, g = h / p.group, q0 = un.tile * 2 * kTile;
+      // which query tiles have work, for the Q loads
+      bool act[2] = {false, false};
+      {
+        KvTileList2<kSparse> t;
+        t.init(p, si.len, q0);
+        int kt, bits;
+        while (t.next(kt, bits)) {
+          act[0] |= (bits & 0xF) != 0;
+          act[1] |= (bits & 0xF0) != 0;
+        }
+      }
+      for (int q = 0; q < 2 && ok; ++q) {
+        if (!act[q]) continue;
+        const uint32_t c = n_q_loads[q];
+        if (!W.warp(&sm.q_empty[q], ((c & 1) ^ 1))) { ok = false; break; }
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&sm.q_full[q], kTileBytes);
+          tma_tile(sm.q[q], &a.tq, a.q_rows_inner, &sm.q_full[q], map_row(si, q0 + q * kTile), h, si.b,
+                   kHalfTileBytes);
+        }
+        last_q_phase[q] = c & 1;
+        ++n_q_loads[q];
+      }
+      if (!ok) break;
+      KvTileList2<kSparse> t;
+      t.init(p, si.len, q0);
+      int kt, bits;
+      while (t.next(kt, bits)) {
+        const int st = n_kv % kStages;
+        const uint32_t ph = (n_kv / kStages) & 1;
+        if (!W.warp(&sm.kv_empty[st], ph ^ 1)) { ok = false; break; }
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+          tma_tile(sm.k[st], &a.tk, a.kv_rows_inner, &sm.k_full[st], map_row(si, kt * kTile), g, si.b,
+                   kHalfTileBytes);
+          ptx::mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+          tma_tile(sm.v[st], &a.tv, a.kv_rows_inner, &sm.v_full[st], map_row(si, kt * kTile), g, si.b,
+                   kHalfTileBytes);
+        }
+        last_kv_phase[st] = (int)ph;
+        ++n_kv;
+      }
+      if (!ok) break;
+    }
+    (void)ok;
+    if (lane == 0) {
+      for (int q = 0; q < 2; ++q)
+        if (last_q_phase[q] >= 0) W.drain(&sm.q_full[q], (uint32_t)last_q_phase[q]);
       for (int s = 0; s < kStages; ++s)
-        if (last_phase[s] >= 0) {
-          wait_drain(&sm.k_full[s], (uint32_t)last_phase[s], sm, p);
-          wait_drain(&sm.v_full[s], (uint32_t)last_phase[s], sm, p);
+        if (last_kv_phase[s] >= 0) {
+          W.drain(&sm.k_full[s], (uint32_t)last_kv_phase[s]);
+          W.drain(&sm.v_full[s], (uint32_t)last_kv_phase[s]);
         }
     }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_tiles > 0) {
+  } else if (warp == 9) {
+    // ================================================================ MMA issuer
+    // One thread runs this role; it takes part in the unit ring on its own.
+    if (lane == 0) {
       constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_pv = ptx::idesc_bf16(128, 128, false, true);
-      const uint32_t q_addr = ptx::smem_u32(sm.q);
-      bool ok = ptx::mbar_wait(&sm.q_full, 0, &sm.abort, p.status, p.wait_limit_ns);
-      ptx::tc_fence_after();
+      uint32_t n_units_seen = 0, n_q[2] = {0, 0}, n_p[2] = {0, 0}, n_o[2] = {0, 0};
+      uint32_t n_k = 0, n_v = 0;
+      bool ok = true;
+      for (;;) {
+        const int slot = n_units_seen & 1;
+        if (!W.one(&sm.unit_full[slot], (n_units_seen >> 1) & 1)) { ok = false; break; }
+        Unit un;
+        const bool valid = read_unit(sm, slot, un);
+        ptx::mbar_arrive(&sm.unit_empty[slot]);
+        ++n_units_seen;
+        if (!valid) break;
 
-      // o_ready completes after every P V product (the softmax waits on it only
-      // right after seeing S_j, when it is at most one phase behind); o_final
-      // completes once, after the last one.
-      auto issue_pv = [&](int i, bool last) -> bool {
-        const int b = i & 1, st = i % kStages;
-        if (!ptx::mbar_wait(&sm.p_full[b], (i >> 1) & 1, &sm.abort, p.status, p.wait_limit_ns)) return false;
-        if (!ptx::mbar_wait(&sm.v_full[st], (i / kStages) & 1, &sm.abort, p.status, p.wait_limit_ns))
-          return false;
-        ptx::tc_fence_after();
-        const uint32_t v_addr = ptx::smem_u32(sm.v[st]);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // B = V as (N = head dim, K = keys), head dim contiguous: MN-major.
-          const uint64_t bdesc = ptx::sdesc_sw128(v_addr + kk * 2048, kHalfTileBytes, 1024);
-          ptx::mma_ts(tmem + kColO, tmem + b * 128 + kk * 8, bdesc, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+        const SeqInfo si = seq_info(p, un.seq);
+        KvTileList2<kSparse> tl;
+        tl.init(p, si.len, un.tile * 2 * kTile);
+        int n_act[2] = {0, 0};
+        {
+          KvTileList2<kSparse> t = tl;
+          int kt, bits;
+          while (t.next(kt, bits)) {
+            n_act[0] += (bits & 0xF) != 0;
+            n_act[1] += (bits & 0xF0) != 0;
+          }
         }
-        ptx::mma_commit(&sm.kv_empty[st]);
-        ptx::mma_commit(&sm.o_ready);
-        if (last) ptx::mma_commit(&sm.o_final);
-        return true;
-      };
+        int s_issued[2] = {0, 0}, pv_issued[2] = {0, 0};
+        // S_q = Q_q K^T into S_q; after the unit's last one, Q_q may be refilled.
+        auto issue_s = [&](int q, uint32_t k_addr) -> bool {
+          if (s_issued[q] == 0) {
+            if (!W.one(&sm.q_full[q], n_q[q] & 1)) return false;
+            ++n_q[q];
+            ptx::tc_fence_after();
+          }
+          const uint32_t q_addr = ptx::smem_u32(sm.q[q]);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
+            ptx::mma_ss(tmem + q * 128, ptx::sdesc_sw128(q_addr + off, 16, 1024),
+                        ptx::sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(&sm.s_full[q]);
+          if (++s_issued[q] == n_act[q]) ptx::mma_commit(&sm.q_empty[q]);
+          return true;
+        };
 
-      KvTileList t = tiles;
-      int kt, bits, j = 0;
-      while (ok && t.next(kt, bits)) {
-        const int b = j & 1, st = j % kStages;
-        if (!ptx::mbar_wait(&sm.k_full[st], (j / kStages) & 1, &sm.abort, p.status, p.wait_limit_ns)) {
-          ok = false;
-          break;
+        KvTileList2<kSparse> t = tl;
+        int kt, bits;
+        bool have = t.next(kt, bits);
+        uint32_t cur_stage = 0;
+        int cur_bits = bits;
+        if (have) {  // prologue: S of the first tile
+          cur_stage = n_k % kStages;
+          if (!W.one(&sm.k_full[cur_stage], (n_k / kStages) & 1)) { ok = false; break; }
+          ++n_k;
+          ptx::tc_fence_after();
+          for (int q = 0; q < 2 && ok; ++q)
+            if ((bits >> (4 * q)) & 0xF) ok = issue_s(q, ptx::smem_u32(sm.k[cur_stage]));
+          if (!ok) break;
         }
-        ptx::tc_fence_after();
-        const uint32_t k_addr = ptx::smem_u32(sm.k[st]);
+        while (have) {
+          int nkt, nbits = 0;
+          const bool nhave = t.next(nkt, nbits);
+          const uint32_t nst = n_k % kStages;
+          bool k_next_ready = false;  // K of the next tile is waited for only when first needed
+          if (!W.one(&sm.v_full[cur_stage], (n_v / kStages) & 1)) { ok = false; break; }
+          ++n_v;
+          ptx::tc_fence_after();
+          const uint32_t v_addr = ptx::smem_u32(sm.v[cur_stage]);
+          for (int q = 0; q < 2 && ok; ++q) {
+            if ((cur_bits >> (4 * q)) & 0xF) {
+              // O_q += P_q V.  Before the unit's first product, the previous unit's
+              // epilogue must have read O_q.
+              if (!W.one(&sm.p_full[q], n_p[q] & 1)) { ok = false; break; }
+              ++n_p[q];
+              if (pv_issued[q] == 0 && !W.one(&sm.o_free[q], (n_o[q] & 1) ^ 1)) { ok = false; break; }
+              ptx::tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
-          ptx::mma_ss(tmem + b * 128, ptx::sdesc_sw128(q_addr + off, 16, 1024),
-                      ptx::sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < 8; ++kk) {
+                // B = V as (N = head dim, K = keys), head dim contiguous: MN-major.
+                const uint64_t bdesc = ptx::sdesc_sw128(v_addr + kk * 2048, kHalfTileBytes, 1024);
+                ptx::mma_ts(tmem + 256 + q * 128, tmem + q * 128 + kk * 8, bdesc, idesc_pv,
+                            (pv_issued[q] > 0 || kk > 0) ? 1u : 0u);
+              }
+              if (++pv_issued[q] == n_act[q]) {
+                ptx::mma_commit(&sm.o_final[q]);
+                ++n_o[q];
+              }
+            }
+            // S_q of the next tile: the S_q buffer held P_q, consumed by the product above
+            if (nhave && ((nbits >> (4 * q)) & 0xF)) {
+              if (!k_next_ready) {
+                if (!W.one(&sm.k_full[nst], (n_k / kStages) & 1)) { ok = false; break; }
+                ++n_k;
+                k_next_ready = true;
+                ptx::tc_fence_after();
+              }
+              if (!issue_s(q, ptx::smem_u32(sm.k[nst]))) ok = false;
+            }
+          }
+          // a tile whose K nobody here needed still has to be consumed from the ring
+          if (ok && nhave && !k_next_ready) {
+            if (!W.one(&sm.k_full[nst], (n_k / kStages) & 1)) ok = false;
+            ++n_k;
+          }
+          if (!ok) break;
+          ptx::mma_commit(&sm.kv_empty[cur_stage]);
+          have = nhave;
+          cur_bits = nbits;
+          cur_stage = nst;
         }
-        ptx::mma_commit(&sm.s_full[b]);
-        if (j > 0 && !issue_pv(j - 1, false)) {
-          ok = false;
-          break;
-        }
-        ++j;
+        if (!ok) break;
       }
-      if (ok && j > 0) issue_pv(j - 1, true);
-      // every tensor-core operation issued so far is finished before tensor memory is freed
+      (void)ok;
       ptx::mma_commit(&sm.drain);
-      wait_drain(&sm.drain, 0, sm, p);
+      W.drain(&sm.drain, 0);
     }
-  } else {
-    // ------------------------------------------------------------ softmax warps
-    const int r = threadIdx.x;  // row in the tile = TMEM lane
-    const int qi = q0 + r;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  } else if (warp < 8) {
+    // ================================================================ softmax
+    const int q = warp >> 2;          // query tile of this warpgroup
+    const int wq = warp & 3;          // warp within the group = TMEM lane quarter
+    const int r = wq * 32 + lane;     // row in the query tile = TMEM lane
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    const uint32_t col_s = q * 128, col_o = 256 + q * 128;
     const bool elem_causal = p.mask == kMaskCausal || (p.mask == kMaskBlock && p.causal_in_block);
     const float c = p.scale_log2;
     const int row_half = r >= 64 ? 2 : 0;
-    float m_used = -INFINITY, l = 0.f;
+    uint32_t n_units_seen = 0, n_s = 0, n_o = 0;
     bool ok = true;
-    int j = 0;
-    {
-      KvTileList t = tiles;
-      int kt, bits;
-      while (t.next(kt, bits)) {
-        const int b = j & 1;
-        if (!wait_warp(&sm.s_full[b], (j >> 1) & 1, sm, p)) {
-          ok = false;
-          break;
-        }
+    for (;;) {
+      const int slot = n_units_seen & 1;
+      if (!W.warp(&sm.unit_full[slot], (n_units_seen >> 1) & 1)) { ok = false; break; }
+      Unit un;
+      const bool valid = read_unit(sm, slot, un);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sm.unit_empty[slot]);
+      ++n_units_seen;
+      if (!valid) break;
+
+      const SeqInfo si = seq_info(p, un.seq);
+      const int h = un.head;
+      const int q0 = un.tile * 2 * kTile + q * kTile;  // this tile's first row
+      const int qi = q0 + r;
+      float m_used = -INFINITY, l = 0.f;
+      int n_done = 0;
+      KvTileList2<kSparse> t;
+      t.init(p, si.len, un.tile * 2 * kTile);
+      int kt, bits8;
+      while (t.next(kt, bits8)) {
+        const int bits = (bits8 >> (4 * q)) & 0xF;
+        if (!bits) continue;
+        if (!W.warp(&sm.s_full[q], n_s & 1)) { ok = false; break; }
+        ++n_s;
         ptx::tc_fence_after();
+        const int k0 = kt * kTile;
+        const bool need_mask = (k0 + kTile > si.len) || (elem_causal && k0 + kTile - 1 > q0) || bits != 0xF;
+        // Visibility of key k of this tile from this row: k < thr (sequence end and,
+        // for causal rows, the diagonal) and the row block's listed 64-key halves.
+        int thr = si.len - k0;
+        if (elem_causal) thr = min(thr, qi - k0 + 1);
+        const bool lo_ok = (bits >> row_half) & 1, hi_ok = (bits >> (row_half + 1)) & 1;
+        // x = S * scale * log2(e) for the whole row, read from tensor memory at once
         uint32_t sr[128];
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
-          ptx::tmem_ld32(tmem + lane_base + b * 128 + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
+          ptx::tmem_ld32(tmem + lane_base + col_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
         ptx::tmem_ld_wait();
-        const int k0 = kt * kTile;
-        const bool need_mask = (k0 + kTile > si.len) || (elem_causal && k0 + kTile - 1 > q0) || bits != 0xF;
-        float x[128];
-        float mx = -INFINITY;
-        if (need_mask) {
+        float mx8[8];
 #pragma unroll
-          for (int k = 0; k < 128; ++k) {
-            const int kj = k0 + k;
-            bool keep = kj < si.len && ((bits >> (row_half + (k >= 64 ? 1 : 0))) & 1);
-            if (elem_causal) keep = keep && kj <= qi;
-            x[k] = keep ? __uint_as_float(sr[k]) * c : -INFINITY;
-            mx = fmaxf(mx, x[k]);
-          }
-        } else {
+        for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
 #pragma unroll
-          for (int k = 0; k < 128; ++k) {
-            x[k] = __uint_as_float(sr[k]) * c;
-            mx = fmaxf(mx, x[k]);
-          }
+        for (int k = 0; k < 128; ++k) {
+          float x = __uint_as_float(sr[k]) * c;
+          if (need_mask && !(k < thr && (k < 64 ? lo_ok : hi_ok))) x = -INFINITY;
+          sr[k] = __float_as_uint(x);
+          mx8[k & 7] = fmaxf(mx8[k & 7], x);
         }
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_new = fmaxf(m_used, mx);
         const bool resc = m_new > m_used + kRescaleLog2;
         float alpha = 1.f;
         if (resc) {
-          alpha = fast_exp2(m_used - m_new);  // 0 when m_used is -inf
+          alpha = fast_exp2(m_used - m_new);
           l *= alpha;
           m_used = m_new;
         }
         const float mu = m_used == -INFINITY ? 0.f : m_used;
-        uint32_t pk[64];
-        float rs = 0.f;
+        // P = exp2(x - m) as bf16 pairs, written over S_q 8 columns (16 keys) at a time
+        float rs8[4];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const float p0 = fast_exp2(x[2 * i] - mu), p1 = fast_exp2(x[2 * i + 1] - mu);
-          rs += p0 + p1;
-          pk[i] = ptx::pack_bf16x2(p0, p1);
-        }
-        l += rs;
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
-          // O holds sum_{t<j} P_t V_t once the previous product is done; rescale it
-          if (!wait_warp(&sm.o_ready, (j - 1) & 1, sm, p)) {
-            ok = false;
-            break;
+        for (int u = 0; u < 4; ++u) rs8[u] = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int k = cc * 16 + 2 * i;
+            const float p0 = fast_exp2(__uint_as_float(sr[k]) - mu);
+            const float p1 = fast_exp2(__uint_as_float(sr[k + 1]) - mu);
+            rs8[i & 3] += p0 + p1;
+            pk[i] = ptx::pack_bf16x2(p0, p1);
           }
-          ptx::tc_fence_after();
+          ptx::tmem_st8(tmem + lane_base + col_s + cc * 8, pk);
+        }
+        const float rs = (rs8[0] + rs8[1]) + (rs8[2] + rs8[3]);
+        // S_q of this tile was issued after the previous P_q V product and its
+        // completion covers that product, so O_q is stable here; the next product
+        // waits for p_full, so rescaling O_q now (after P is written) is in time.
+        if (n_done > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t orr[32];
-            ptx::tmem_ld32(tmem + lane_base + kColO + cc * 32, orr);
+            ptx::tmem_ld32(tmem + lane_base + col_o + cc * 32, orr);
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-            ptx::tmem_st32(tmem + lane_base + kColO + cc * 32, orr);
+            ptx::tmem_st32(tmem + lane_base + col_o + cc * 32, orr);
           }
         }
-        ptx::tmem_st32(tmem + lane_base + b * 128, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        ptx::tmem_st32(tmem + lane_base + b * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+        l += rs;
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm.p_full[b]);
-        ++j;
+        if (lane == 0) ptx::mbar_arrive(&sm.p_full[q]);
+        ++n_done;
       }
-    }
-    if (ok && j > 0) ok = wait_warp(&sm.o_final, 0, sm, p);
-    ok = ok && !sm.abort.flag;
-    if (ok) {
-      ptx::tc_fence_after();
-      // O / l to bf16, staged in shared memory (the Q buffer: every S product is
-      // done once the last P V product is), 16-byte chunk c of row r at chunk c ^ (r & 15).
-      uint8_t* stage = sm.q;
+      if (!ok) break;
+      if (q0 >= si.len) continue;  // this query tile lies past the sequence end
+      // epilogue: O_q / l straight from tensor memory to global memory
+      if (n_done > 0) {
+        if (!W.warp(&sm.o_final[q], n_o & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+      }
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
+      const bool row_ok = qi < si.len;
+      __nv_bfloat16* orow = O + (row_ok ? q_off(p, si, h, qi) : 0);
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t orr[32];
-        if (j > 0) {
-          ptx::tmem_ld32(tmem + lane_base + kColO + cc * 32, orr);
+        if (n_done > 0) {
+          ptx::tmem_ld32(tmem + lane_base + col_o + cc * 32, orr);
           ptx::tmem_ld_wait();
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) orr[i] = 0u;
         }
+        if (row_ok) {
 #pragma unroll
-        for (int w4 = 0; w4 < 4; ++w4) {
-          uint4 v4;
-          v4.x = ptx::pack_bf16x2(__uint_as_float(orr[w4 * 8 + 0]) * inv, __uint_as_float(orr[w4 * 8 + 1]) * inv);
-          v4.y = ptx::pack_bf16x2(__uint_as_float(orr[w4 * 8 + 2]) * inv, __uint_as_float(orr[w4 * 8 + 3]) * inv);
-          v4.z = ptx::pack_bf16x2(__uint_as_float(orr[w4 * 8 + 4]) * inv, __uint_as_float(orr[w4 * 8 + 5]) * inv);
-          v4.w = ptx::pack_bf16x2(__uint_as_float(orr[w4 * 8 + 6]) * inv, __uint_as_float(orr[w4 * 8 + 7]) * inv);
-          const int ch = cc * 4 + w4;
-          *reinterpret_cast<uint4*>(stage + r * 256 + ((ch ^ (r & 15)) * 16)) = v4;
+          for (int w4 = 0; w4 < 4; ++w4) {
+            uint4 v4;
+            v4.x = ptx::pack_bf16x2(__uint_as_float(orr[w4 * 8 + 0]) * inv, __uint_as_float(orr[w4 * 8 + 1]) * inv);
+            v4.y = ptx::pack_bf16x2(__uint_as_float(orr[w4 * 8 + 2]) * inv, __uint_as_float(orr[w4 * 8 + 3]) * inv);
+            v4.z = ptx::pack_bf16x2(__uint_as_float(orr[w4 * 8 + 4]) * inv, __uint_as_float(orr[w4 * 8 + 5]) * inv);
+            v4.w = ptx::pack_bf16x2(__uint_as_float(orr[w4 * 8 + 6]) * inv, __uint_as_float(orr[w4 * 8 + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + cc * 32 + w4 * 8) = v4;
+          }
         }
       }
-      if (qi < si.len)
+      if (n_done > 0) {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.o_free[q]);
+        ++n_o;
+      }
+      if (row_ok)
         p.lse[row_index(p, si, h, qi)] = l > 0.f ? (m_used + fast_log2(l)) * 0.69314718055994530942f : -INFINITY;
-      __syncwarp();
-      // each warp copies its own 32 rows out: two full 256-byte rows per instruction
-      __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
-#pragma unroll 4
-      for (int it = 0; it < 16; ++it) {
-        const int row = warp * 32 + it * 2 + (lane >> 4), ch = lane & 15;
-        if (q0 + row < si.len) {
-          const uint4 v4 = *reinterpret_cast<const uint4*>(stage + row * 256 + ((ch ^ (row & 15)) * 16));
-          *reinterpret_cast<uint4*>(O + q_off(p, si, h, q0 + row) + ch * 8) = v4;
-        }
-      }
     }
+    (void)ok;
   }
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
@@ -350,7 +501,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) k_tc_fwd(const __grid_constant
 bool tc_fwd_available() { return true; }
 
 cudaError_t launch_tc_fwd(const KParams& p, int sms, cudaStream_t st) {
-  (void)sms;
   if (p.n_units == 0) return cudaSuccess;
   FwdArgs a;
   TileMap mq, mk, mv;
@@ -364,10 +514,12 @@ cudaError_t launch_tc_fwd(const KParams& p, int sms, cudaStream_t st) {
   a.q_rows_inner = mq.rows_inner;
   a.kv_rows_inner = mk.rows_inner;
   a.p = p;
-  const size_t smem = sizeof(FwdSmem) + 1024;
-  e = cudaFuncSetAttribute(k_tc_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = sizeof(Smem) + 1024;
+  const int grid = p.n_units < sms ? p.n_units : sms;
+  auto kernel = p.mask == kMaskBlock ? k_tc_fwd<true> : k_tc_fwd<false>;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_tc_fwd<<<p.n_units, kFwdThreads, smem, st>>>(a);
+  kernel<<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
