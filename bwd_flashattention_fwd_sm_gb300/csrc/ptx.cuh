@@ -33,6 +33,18 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Per-warpgroup register budget changes; every warp of the warpgroup executes
+// the same one.  The budgets after the changes must add up to at most the
+// registers the CTA was launched with.
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------

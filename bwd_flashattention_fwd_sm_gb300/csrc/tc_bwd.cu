@@ -23,9 +23,12 @@
 // other roles through a two-slot ring in shared memory.
 //
 // Warp roles (320 threads):
-//   warps 0-3  thread t owns key row t: P^T and dS^T; dK epilogue
-//   warps 4-7  thread t owns head-dim column t of dQ_i^T: staging + TMA reduce;
-//              dV epilogue
+//   warps 0-7  compute: warp w covers TMEM lane quarter w % 4 (key rows, or head-
+//              dim columns for dQ^T) and query columns 32 (w / 4) .. +31 of the
+//              step.  Per step: P^T, dS^T, then the previous step's dQ^T
+//              (read from tensor memory one step late, so the dK and dQ products
+//              never hold these warps up) staged in shared memory and added by a
+//              TMA reduce.  Unit epilogue: warps 0-3 dK, warps 4-7 dV.
 //   warp 8     TMA producer (K, V per unit; Q_i, dO_i in a 3-stage ring; LSE, D rows)
 //   warp 9     tensor-core issuer (one thread)
 // Every mbarrier wait is bounded; a CTA that gives up records
@@ -64,8 +67,8 @@ struct Smem {
   uint8_t dO[kStages][kQTileBytes];
   uint8_t ds[2][kDsBytes];   // dS^T (128-byte swizzled rows)
   float dq[kQB * kHeadDim];  // dQ_i staging, row-major [query][head dim]
-  float lse2[kStages][kQB];  // LSE * log2(e) of the stage's query rows (+inf: no key)
-  float dlt[kStages][kQB];   // D of the stage's query rows
+  float nlse2[kStages][kQB];  // -LSE * log2(e) of the stage's query rows (-inf: no key / past the end)
+  float ndlt[kStages][kQB];   // -D of the stage's query rows
   uint64_t unit_full[2], unit_empty[2];
   uint64_t kv_full, kv_empty, qdo_full[kStages], qdo_empty[kStages];
   uint64_t st_full[2], pt_full[2], dp_full, dp_free, ds_full[2], ds_free[2], dq_full, dq_free;
@@ -102,21 +105,22 @@ __device__ __forceinline__ bool read_unit(const Smem& sm, int slot, Unit& un) {
   return s[3] != 0;
 }
 
-// AND of `pred` over the 128 threads of the dQ warps (named barrier 1); every
-// one of them reaches it once per step, whatever its own waits returned.
-__device__ __forceinline__ bool dq_group_all(bool pred) {
+// AND of `pred` over the 256 compute threads (named barrier 1).  Named barriers
+// have no time limit, so every compute thread reaches this exactly once per step
+// and per unit whatever its own waits returned, and the group acts on the result.
+__device__ __forceinline__ bool group_all(bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "bar.red.and.pred q, 1, 256, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"(pred ? 1u : 0u)
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ void dq_group_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // One warp writes its 32 key rows of a 128-column accumulator (x scale, bf16)
 // straight from tensor memory to global memory rows k0 + row < len of head g.
@@ -162,20 +166,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&sm.unit_full[s], 1);
-      ptx::mbar_init(&sm.unit_empty[s], 9);  // MMA thread + 4 P/dS warps + 4 dQ warps
+      ptx::mbar_init(&sm.unit_empty[s], 9);  // MMA thread + 8 compute warps
       ptx::mbar_init(&sm.st_full[s], 1);
-      ptx::mbar_init(&sm.pt_full[s], 4);
-      ptx::mbar_init(&sm.ds_full[s], 4);
+      ptx::mbar_init(&sm.pt_full[s], 8);
+      ptx::mbar_init(&sm.ds_full[s], 8);
       ptx::mbar_init(&sm.ds_free[s], 1);
     }
     ptx::mbar_init(&sm.kv_full, 1);
     ptx::mbar_init(&sm.kv_empty, 1);
     ptx::mbar_init(&sm.dp_full, 1);
-    ptx::mbar_init(&sm.dp_free, 4);
+    ptx::mbar_init(&sm.dp_free, 8);
     ptx::mbar_init(&sm.dq_full, 1);
-    ptx::mbar_init(&sm.dq_free, 4);
+    ptx::mbar_init(&sm.dq_free, 8);
     ptx::mbar_init(&sm.acc_done, 1);
-    ptx::mbar_init(&sm.acc_free, 8);  // dK writers (4 warps) + dV writers (4 warps)
+    ptx::mbar_init(&sm.acc_free, 8);  // dK writers (warps 0-3) + dV writers (warps 4-7)
     ptx::mbar_init(&sm.drain, 1);
     sm.abort.flag = 0;
     ptx::fence_mbar_init();
@@ -243,15 +247,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
           const int c = lane + 32 * c2, qi = q0 + c;
-          float l2 = INFINITY, dl = 0.f;
+          float nl2 = -INFINITY, ndl = 0.f;
           if (qi < si.len) {
             const long long ri = row_index(p, si, h, qi);
             const float L = p.lse[ri];
-            l2 = L == -INFINITY ? INFINITY : L * 1.4426950408889634f;
-            dl = p.delta[ri];
+            nl2 = L == -INFINITY ? -INFINITY : -L * 1.4426950408889634f;
+            ndl = -p.delta[ri];
           }
-          sm.lse2[st][c] = l2;
-          sm.dlt[st][c] = dl;
+          sm.nlse2[st][c] = nl2;
+          sm.ndlt[st][c] = ndl;
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sm.qdo_full[st]);
@@ -335,8 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
           const uint32_t q_addr = ptx::smem_u32(sm.q[qs]), do_addr = ptx::smem_u32(sm.dO[qs]);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
+            // P^T of query columns 16 kk .. +15: the compute warps of column half
+            // kk / 2 write their 16 packed columns at 32 (kk / 2) within the S^T buffer
+            const uint32_t a_col = kColS + st * 64 + 32 * (kk >> 1) + (kk & 1) * 8;
             const uint64_t bd = ptx::sdesc_sw128(do_addr + kk * 2048, kQBoxBytes, 1024);
-            ptx::mma_ts(tmem + kColDV, tmem + kColS + st * 64 + kk * 8, bd, id_acc, (s > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_ts(tmem + kColDV, tmem + a_col, bd, id_acc, (s > 0 || kk > 0) ? 1u : 0u);
           }
           if (s + 1 < n && !issue_dp(i + 1)) { ok = false; break; }
           // dK += dS^T_i Q_i: A = dS^T (key rows, query contiguous), B = Q_i MN-major
@@ -374,162 +381,164 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       ptx::mma_commit(&sm.drain);
       W.drain(&sm.drain, 0);
     }
-  } else if (warp < 4) {
-    // ================================================================ P^T / dS^T warps
-    const int t = threadIdx.x;  // key row in the tile = TMEM lane
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  } else {
+    // ================================================================ compute warps
+    const int qr = warp & 3, ch = warp >> 2;  // TMEM lane quarter, query-column half
+    const int t = qr * 32 + lane;              // key row (S^T, dP^T) / head-dim column (dQ^T)
+    const uint32_t lane_base = (uint32_t)(qr * 32) << 16;
     const float c = p.scale_log2;
     const int key_half = t >= 64 ? 1 : 0;
+    const bool issuer = threadIdx.x == 0;      // issues the dQ reduce-adds
     uint32_t n_units = 0, i = 0;
+    bool ok = true;
+    // the previous step's dQ^T is read and reduced one step late
+    bool dq_pending = false;
+    int pend_h = 0, pend_q0 = 0, pend_b = 0;
+    long long pend_tok0 = 0;
+
+    // dQ^T of step j: tensor memory -> staging [query][head dim] -> TMA reduce-add
+    auto flush_dq = [&](uint32_t j, bool mine_ok) -> bool {
+      if (!group_all(mine_ok && W.warp(&sm.dq_full, j & 1))) return false;
+      ptx::tc_fence_after();
+      uint32_t vr[32];
+      ptx::tmem_ld32(tmem + lane_base + kColDQ + 32 * ch, vr);
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sm.dq_free);
+      if (issuer) ptx::bulk_wait_group_read<0>();  // the staging tile has been read
+      group_sync();
+#pragma unroll
+      for (int cc = 0; cc < 32; ++cc) sm.dq[(32 * ch + cc) * kHeadDim + t] = __uint_as_float(vr[cc]);
+      ptx::fence_proxy_async_smem();
+      group_sync();
+      if (issuer) {
+        // rows past the sequence end carry exact zeros (their P is 0); the map
+        // clips rows past the tensor end
+        if (a.acc_rows_inner) ptx::tma_reduce_add_4d(&a.tacc, sm.dq, 0, (int)(pend_tok0 + pend_q0), pend_h, pend_b);
+        else ptx::tma_reduce_add_4d(&a.tacc, sm.dq, 0, pend_h, (int)(pend_tok0 + pend_q0), 0);
+        ptx::bulk_commit_group();
+      }
+      return true;
+    };
+
     for (;;) {
       const int slot = n_units & 1;
-      if (!W.warp(&sm.unit_full[slot], (n_units >> 1) & 1)) break;
+      if (!group_all(W.warp(&sm.unit_full[slot], (n_units >> 1) & 1))) { ok = false; break; }
       Unit un;
       const bool valid = read_unit(sm, slot, un);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&sm.unit_empty[slot]);
       if (!valid) break;
       const SeqInfo si = seq_info(p, un.seq);
-      const int k0 = un.tile * kTile, kj = k0 + t;
+      const int g = un.head, k0 = un.tile * kTile, kj = k0 + t;
       BwdSteps steps;
       steps.init(p, si.len, un.tile);
       int hh, qb, bits, n = 0;
-      bool ok = true;
       while (steps.next(hh, qb, bits)) {
         const int st = i & 1, qs = i % kStages;
         const int q0 = qb * kQB;
-        if (!W.warp(&sm.qdo_full[qs], (i / kStages) & 1) || !W.warp(&sm.st_full[st], (i >> 1) & 1)) { ok = false; break; }
-        ptx::tc_fence_after();
-        uint32_t sr[64];
-        ptx::tmem_ld32(tmem + lane_base + kColS + st * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        ptx::tmem_ld32(tmem + lane_base + kColS + st * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-        ptx::tmem_ld_wait();
-        const bool need_mask = (k0 + kTile > si.len) || (elem_causal && q0 < k0 + kTile - 1) || bits != 3;
-        const bool row_listed = (bits >> key_half) & 1;
-        float pv[64];
-        uint32_t pk[32];
+        bool mine = W.warp(&sm.qdo_full[qs], (i / kStages) & 1) && W.warp(&sm.st_full[st], (i >> 1) & 1);
+        float pv[32];
+        if (mine) {
+          // P^T = exp2(S^T * scale * log2 e - LSE * log2 e) for 32 query columns
+          ptx::tc_fence_after();
+          uint32_t sr[32];
+          ptx::tmem_ld32(tmem + lane_base + kColS + st * 64 + 32 * ch, sr);
+          ptx::tmem_ld_wait();
+          const bool need_mask = (k0 + kTile > si.len) || (elem_causal && q0 < k0 + kTile - 1) || bits != 3;
+          // visible: key listed for this query block, inside the sequence and
+          // (causal) not after the query: q0 + 32 ch + cc >= kj
+          const bool row_ok = ((bits >> key_half) & 1) && kj < si.len;
+          const int lo = elem_causal ? kj - q0 - 32 * ch : -1;
+          uint32_t pk[16];
+          const float2 c2 = make_float2(c, c);
+          const float2* nl2 = reinterpret_cast<const float2*>(&sm.nlse2[qs][32 * ch]);
 #pragma unroll
-        for (int cc = 0; cc < 64; ++cc) {
-          bool keep = true;
+          for (int w = 0; w < 16; ++w) {
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * w]), __uint_as_float(sr[2 * w + 1])), c2, nl2[w]);
+            pv[2 * w] = fast_exp2(x.x);
+            pv[2 * w + 1] = fast_exp2(x.y);
+          }
           if (need_mask) {
-            keep = row_listed && kj < si.len;
-            if (elem_causal) keep = keep && kj <= q0 + cc;
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc)
+              if (!(row_ok && cc >= lo)) pv[cc] = 0.f;
           }
-          pv[cc] = keep ? fast_exp2(fmaf(__uint_as_float(sr[cc]), c, -sm.lse2[qs][cc])) : 0.f;
+#pragma unroll
+          for (int w = 0; w < 16; ++w) pk[w] = ptx::pack_bf16x2(pv[2 * w], pv[2 * w + 1]);
+          ptx::tmem_st16(tmem + lane_base + kColS + st * 64 + 32 * ch, pk);
+          ptx::tmem_st_wait();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&sm.pt_full[st]);
+          mine = W.warp(&sm.dp_full, i & 1);
         }
+        if (mine) {
+          ptx::tc_fence_after();
+          uint32_t dr[32];
+          ptx::tmem_ld32(tmem + lane_base + kColDP + 32 * ch, dr);
+          ptx::tmem_ld_wait();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&sm.dp_free);
+          mine = W.warp(&sm.ds_free[st], ((i >> 1) & 1) ^ 1);
+          if (mine) {
+            // dS^T = P^T o (dP^T - D), bf16, 128-byte swizzled row t of the dS^T tile
+            uint8_t* dsrow = sm.ds[st] + t * 128;
 #pragma unroll
-        for (int w = 0; w < 32; ++w) pk[w] = ptx::pack_bf16x2(pv[2 * w], pv[2 * w + 1]);
-        ptx::tmem_st32(tmem + lane_base + kColS + st * 64, pk);
-        ptx::tmem_st_wait();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm.pt_full[st]);
-
-        if (!W.warp(&sm.dp_full, i & 1)) { ok = false; break; }
-        ptx::tc_fence_after();
-        uint32_t dr[64];
-        ptx::tmem_ld32(tmem + lane_base + kColDP, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
-        ptx::tmem_ld32(tmem + lane_base + kColDP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
-        ptx::tmem_ld_wait();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm.dp_free);
-
-        if (!W.warp(&sm.ds_free[st], ((i >> 1) & 1) ^ 1)) { ok = false; break; }
-        uint8_t* dsrow = sm.ds[st] + t * 128;
+            const float2* nd2 = reinterpret_cast<const float2*>(&sm.ndlt[qs][32 * ch]);
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          float d[8];
+            for (int j = 0; j < 4; ++j) {
+              float d[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int cc = ch * 8 + e;
-            d[e] = pv[cc] * (__uint_as_float(dr[cc]) - sm.dlt[qs][cc]);
+              for (int e = 0; e < 8; e += 2) {
+                const int cc = j * 8 + e;
+                const float2 t2 = __fadd2_rn(make_float2(__uint_as_float(dr[cc]), __uint_as_float(dr[cc + 1])), nd2[cc >> 1]);
+                const float2 d2 = __fmul2_rn(make_float2(pv[cc], pv[cc + 1]), t2);
+                d[e] = d2.x;
+                d[e + 1] = d2.y;
+              }
+              uint4 o;
+              o.x = ptx::pack_bf16x2(d[0], d[1]);
+              o.y = ptx::pack_bf16x2(d[2], d[3]);
+              o.z = ptx::pack_bf16x2(d[4], d[5]);
+              o.w = ptx::pack_bf16x2(d[6], d[7]);
+              const int chunk = 4 * ch + j;
+              *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (t & 7)) * 16)) = o;
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&sm.ds_full[st]);
           }
-          uint4 o;
-          o.x = ptx::pack_bf16x2(d[0], d[1]);
-          o.y = ptx::pack_bf16x2(d[2], d[3]);
-          o.z = ptx::pack_bf16x2(d[4], d[5]);
-          o.w = ptx::pack_bf16x2(d[6], d[7]);
-          *reinterpret_cast<uint4*>(dsrow + ((ch ^ (t & 7)) * 16)) = o;
         }
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm.ds_full[st]);
+        // the previous step's dQ (also agrees on this step's outcome group-wide)
+        if (dq_pending) {
+          if (!flush_dq(i - 1, mine)) { ok = false; break; }
+        } else if (!group_all(mine)) {
+          ok = false;
+          break;
+        }
+        dq_pending = true;
+        pend_h = g * p.group + hh;
+        pend_q0 = q0;
+        pend_b = si.b;
+        pend_tok0 = si.tok0;
         ++i;
         ++n;
       }
       if (!ok) break;
-      // dK epilogue
-      if (!W.warp(&sm.acc_done, n_units & 1)) break;
+      // unit epilogue: warps 0-3 write dK (x scale), warps 4-7 dV
+      if (!group_all(W.warp(&sm.acc_done, n_units & 1))) { ok = false; break; }
       ptx::tc_fence_after();
-      store_kv_rows(tmem + lane_base + kColDK, n > 0, p.scale, t, p, si, un.head, k0, p.dk);
+      if (ch == 0) store_kv_rows(tmem + lane_base + kColDK, n > 0, p.scale, t, p, si, g, k0, p.dk);
+      else store_kv_rows(tmem + lane_base + kColDV, n > 0, 1.f, t, p, si, g, k0, p.dv);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&sm.acc_free);
       ++n_units;
     }
-  } else {
-    // ================================================================ dQ warps
-    // These four warps also meet at named barrier 1, which has no time limit, so
-    // every wait's outcome is first made the same for all 128 threads
-    // (dq_group_all) and the group leaves its loops together.
-    const int wq = warp - 4;
-    const int d = wq * 32 + lane;  // head-dim column = TMEM lane
-    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const bool issuer = threadIdx.x == 128;
-    uint32_t n_units = 0, i = 0;
-    bool group_ok = true;
-    for (;;) {
-      const int slot = n_units & 1;
-      if (!dq_group_all(W.warp(&sm.unit_full[slot], (n_units >> 1) & 1))) break;
-      Unit un;
-      const bool valid = read_unit(sm, slot, un);
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&sm.unit_empty[slot]);
-      if (!valid) break;
-      const SeqInfo si = seq_info(p, un.seq);
-      const int g = un.head, k0 = un.tile * kTile;
-      BwdSteps steps;
-      steps.init(p, si.len, un.tile);
-      int hh, qb, bits, n = 0;
-      while (steps.next(hh, qb, bits)) {
-        if (!dq_group_all(W.warp(&sm.dq_full, i & 1))) { group_ok = false; break; }
-        ptx::tc_fence_after();
-        uint32_t vr[64];
-        ptx::tmem_ld32(tmem + lane_base + kColDQ, *reinterpret_cast<uint32_t(*)[32]>(&vr[0]));
-        ptx::tmem_ld32(tmem + lane_base + kColDQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&vr[32]));
-        ptx::tmem_ld_wait();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm.dq_free);
-        // the staging tile is free once the previous reduce has read it
-        if (issuer) ptx::bulk_wait_group_read<0>();
-        dq_group_sync();
-#pragma unroll
-        for (int cc = 0; cc < 64; ++cc) sm.dq[cc * kHeadDim + d] = __uint_as_float(vr[cc]);
-        ptx::fence_proxy_async_smem();
-        dq_group_sync();
-        if (issuer) {
-          const int h = g * p.group + hh, q0 = qb * kQB;
-          // rows past the sequence end carry exact zeros (their P is 0); the map
-          // clips rows past the tensor end
-          if (a.acc_rows_inner) ptx::tma_reduce_add_4d(&a.tacc, sm.dq, 0, (int)(si.tok0 + q0), h, si.b);
-          else ptx::tma_reduce_add_4d(&a.tacc, sm.dq, 0, h, (int)(si.tok0 + q0), 0);
-          ptx::bulk_commit_group();
-        }
-        ++i;
-        ++n;
-      }
-      if (!group_ok) break;
-      // dV epilogue
-      if (!dq_group_all(W.warp(&sm.acc_done, n_units & 1))) break;
-      ptx::tc_fence_after();
-      store_kv_rows(tmem + lane_base + kColDV, n > 0, 1.f, d, p, si, g, k0, p.dv);
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&sm.acc_free);
-      ++n_units;
-    }
+    if (ok && dq_pending) flush_dq(i - 1, true);
     if (issuer) ptx::bulk_wait_group<0>();
   }
 

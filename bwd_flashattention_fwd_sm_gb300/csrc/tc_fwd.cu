@@ -23,12 +23,14 @@
 // section 4.2: whoever finishes first takes the next block; smzdm article,
 // section 02, on uneven work).
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads):
 //   warps 0-3 / 4-7  softmax for query tile 0 / 1: thread r owns row r (the
 //                    whole 128-column S row in registers; max and sum in 8
 //                    independent partials to keep dependency chains short)
 //   warp 8           TMA producer and unit fetcher
 //   warp 9           tensor-core issuer
+//   warps 10-11      idle (they complete the third warpgroup, whose registers
+//                    the softmax warpgroups borrow)
 // Every wait is bounded; a CTA that gives up records ATTN_ERR_DEVICE_TIMEOUT,
 // drains its copies and tensor-core work, frees tensor memory and returns.
 #include <cuda.h>
@@ -42,7 +44,11 @@ namespace gbattn {
 namespace {
 
 constexpr int kStages = 2;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // three full warpgroups
+// Register split: launched at 168 per thread (384 x 168 = 64512 registers); the
+// two softmax warpgroups raise theirs to 200, the producer/issuer warpgroup
+// lowers its to 96: 256 x 200 + 128 x 96 = 63488 <= 64512.
+constexpr uint32_t kRegsSoftmax = 200, kRegsControl = 96;
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the row max grows by more than 2^8
 constexpr uint32_t kTmemCols = 512;
 
@@ -94,6 +100,35 @@ __device__ __forceinline__ bool read_unit(const Smem& sm, int slot, Unit& un) {
   return s[3] != 0;
 }
 
+// P = exp2(s * c - mu) for one 128-key row (two elements per packed FFMA2 /
+// FADD2), rounded to bf16 pairs and stored to tensor memory at `taddr` 8
+// columns at a time; keys outside the visibility threshold get P = 0 when
+// kMask.  Returns the row sum of the float32 P values.
+template <bool kMask>
+__device__ __forceinline__ float write_p(const uint32_t (&sr)[128], float c, float mu, int thr, bool lo_ok,
+                                         bool hi_ok, uint32_t taddr) {
+  const float2 c2 = make_float2(c, c), nmu2 = make_float2(-mu, -mu);
+  float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int cc = 0; cc < 8; ++cc) {
+    uint32_t pk[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int k = cc * 16 + 2 * i;
+      const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2, nmu2);
+      float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+      if constexpr (kMask) {
+        if (!(k < thr && (k < 64 ? lo_ok : hi_ok))) pp.x = 0.f;
+        if (!(k + 1 < thr && (k + 1 < 64 ? lo_ok : hi_ok))) pp.y = 0.f;
+      }
+      rs2[i & 1] = __fadd2_rn(rs2[i & 1], pp);
+      pk[i] = ptx::pack_bf16x2(pp.x, pp.y);
+    }
+    ptx::tmem_st8(taddr + cc * 8, pk);
+  }
+  return (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
+}
+
 template <bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -130,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  if (warp >= 8) ptx::regs_decrease<kRegsControl>();
   if (warp == 8) {
     // ================================================================ producer
     uint32_t n_units_seen = 0, n_q_loads[2] = {0, 0}, n_kv = 0;
@@ -335,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     }
   } else if (warp < 8) {
     // ================================================================ softmax
+    ptx::regs_increase<kRegsSoftmax>();
     const int q = warp >> 2;          // query tile of this warpgroup
     const int wq = warp & 3;          // warp within the group = TMEM lane quarter
     const int r = wq * 32 + lane;     // row in the query tile = TMEM lane
@@ -377,24 +414,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         int thr = si.len - k0;
         if (elem_causal) thr = min(thr, qi - k0 + 1);
         const bool lo_ok = (bits >> row_half) & 1, hi_ok = (bits >> (row_half + 1)) & 1;
-        // x = S * scale * log2(e) for the whole row, read from tensor memory at once
+        // The whole 128-column S row, read from tensor memory at once.
         uint32_t sr[128];
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
           ptx::tmem_ld32(tmem + lane_base + col_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
         ptx::tmem_ld_wait();
-        float mx8[8];
+        // x = s * scale * log2(e) = s' * |c| with s' = s or -s by the sign of the
+        // scale, so the row max of x is |c| times the max of s' (8 partials keep the
+        // dependency chains short).  Masked keys are left out.
+        if (c < 0.f) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx8[u] = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < 128; ++k) {
-          float x = __uint_as_float(sr[k]) * c;
-          if (need_mask && !(k < thr && (k < 64 ? lo_ok : hi_ok))) x = -INFINITY;
-          sr[k] = __float_as_uint(x);
-          mx8[k & 7] = fmaxf(mx8[k & 7], x);
+          for (int k = 0; k < 128; ++k) sr[k] ^= 0x80000000u;
         }
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float ca = fabsf(c);
+        float e8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) e8[u] = -INFINITY;
+        if (!need_mask) {
+#pragma unroll
+          for (int k = 0; k < 128; ++k) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 128; ++k)
+            if (k < thr && (k < 64 ? lo_ok : hi_ok)) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+        }
+        const float ext = fmaxf(fmaxf(fmaxf(e8[0], e8[1]), fmaxf(e8[2], e8[3])),
+                                fmaxf(fmaxf(e8[4], e8[5]), fmaxf(e8[6], e8[7])));
+        const float mx = ext == -INFINITY ? -INFINITY : ext * ca;
         const float m_new = fmaxf(m_used, mx);
         const bool resc = m_new > m_used + kRescaleLog2;
         float alpha = 1.f;
@@ -404,24 +451,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
           m_used = m_new;
         }
         const float mu = m_used == -INFINITY ? 0.f : m_used;
-        // P = exp2(x - m) as bf16 pairs, written over S_q 8 columns (16 keys) at a time
-        float rs8[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) rs8[u] = 0.f;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint32_t pk[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int k = cc * 16 + 2 * i;
-            const float p0 = fast_exp2(__uint_as_float(sr[k]) - mu);
-            const float p1 = fast_exp2(__uint_as_float(sr[k + 1]) - mu);
-            rs8[i & 3] += p0 + p1;
-            pk[i] = ptx::pack_bf16x2(p0, p1);
-          }
-          ptx::tmem_st8(tmem + lane_base + col_s + cc * 8, pk);
-        }
-        const float rs = (rs8[0] + rs8[1]) + (rs8[2] + rs8[3]);
+        // P = exp2(s' |c| - m) as bf16 pairs, written over S_q 8 columns at a time
+        const float rs = need_mask ? write_p<true>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s)
+                                   : write_p<false>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s);
         // S_q of this tile was issued after the previous P_q V product and its
         // completion covers that product, so O_q is stable here; the next product
         // waits for p_full, so rescaling O_q now (after P is written) is in time.
