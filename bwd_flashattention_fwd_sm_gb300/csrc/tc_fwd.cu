@@ -64,7 +64,7 @@ struct Smem {
   uint8_t v[kStages][kTileBytes];
   uint64_t unit_full[2], unit_empty[2];
   uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[kStages], v_full[kStages], kv_empty[kStages];
+  uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
   uint64_t s_full[2], p_full[2], o_final[2], o_free[2];
   uint64_t drain;
   int unit_slot[2][4];  // seq, head, 256-row tile, valid
@@ -151,7 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&sm.k_full[s], 1);
       ptx::mbar_init(&sm.v_full[s], 1);
-      ptx::mbar_init(&sm.kv_empty[s], 1);
+      ptx::mbar_init(&sm.k_empty[s], 1);
+      ptx::mbar_init(&sm.v_empty[s], 1);
     }
     ptx::mbar_init(&sm.drain, 1);
     sm.abort.flag = 0;
@@ -168,8 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
   if (warp >= 8) ptx::regs_decrease<kRegsControl>();
   if (warp == 8) {
     // ================================================================ producer
-    uint32_t n_units_seen = 0, n_q_loads[2] = {0, 0}, n_kv = 0;
-    int last_q_phase[2] = {-1, -1}, last_kv_phase[kStages] = {-1, -1};
+    uint32_t n_units_seen = 0, n_q_loads[2] = {0, 0}, n_k = 0, n_v = 0;
+    int last_q_phase[2] = {-1, -1}, last_k_phase[kStages] = {-1, -1}, last_v_phase[kStages] = {-1, -1};
     bool ok = true;
     for (;;) {
       const int slot = n_units_seen & 1;
@@ -218,23 +219,47 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         ++n_q_loads[q];
       }
       if (!ok) break;
+      // K runs one tile ahead of V: K is released as soon as the S products of
+      // its tile are done, V only after the P V products, so loading K(j+1)
+      // before V(j) gives it the longest lead.
+      auto load_k = [&](int kt_) -> bool {
+        const int st = n_k % kStages;
+        const uint32_t ph = (n_k / kStages) & 1;
+        if (!W.warp(&sm.k_empty[st], ph ^ 1)) return false;
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+          tma_tile(sm.k[st], &a.tk, a.kv_rows_inner, &sm.k_full[st], map_row(si, kt_ * kTile), g, si.b,
+                   kHalfTileBytes);
+        }
+        last_k_phase[st] = (int)ph;
+        ++n_k;
+        return true;
+      };
+      auto load_v = [&](int kt_) -> bool {
+        const int st = n_v % kStages;
+        const uint32_t ph = (n_v / kStages) & 1;
+        if (!W.warp(&sm.v_empty[st], ph ^ 1)) return false;
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+          tma_tile(sm.v[st], &a.tv, a.kv_rows_inner, &sm.v_full[st], map_row(si, kt_ * kTile), g, si.b,
+                   kHalfTileBytes);
+        }
+        last_v_phase[st] = (int)ph;
+        ++n_v;
+        return true;
+      };
       KvTileList2<kSparse> t;
       t.init(p, si.len, q0);
       int kt, bits;
-      while (t.next(kt, bits)) {
-        const int st = n_kv % kStages;
-        const uint32_t ph = (n_kv / kStages) & 1;
-        if (!W.warp(&sm.kv_empty[st], ph ^ 1)) { ok = false; break; }
-        if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
-          tma_tile(sm.k[st], &a.tk, a.kv_rows_inner, &sm.k_full[st], map_row(si, kt * kTile), g, si.b,
-                   kHalfTileBytes);
-          ptx::mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
-          tma_tile(sm.v[st], &a.tv, a.kv_rows_inner, &sm.v_full[st], map_row(si, kt * kTile), g, si.b,
-                   kHalfTileBytes);
-        }
-        last_kv_phase[st] = (int)ph;
-        ++n_kv;
+      bool have = t.next(kt, bits);
+      if (have && !load_k(kt)) { ok = false; break; }
+      while (have) {
+        int nkt, nbits;
+        const bool nhave = t.next(nkt, nbits);
+        if (nhave && !load_k(nkt)) { ok = false; break; }
+        if (!load_v(kt)) { ok = false; break; }
+        have = nhave;
+        kt = nkt;
       }
       if (!ok) break;
     }
@@ -242,11 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     if (lane == 0) {
       for (int q = 0; q < 2; ++q)
         if (last_q_phase[q] >= 0) W.drain(&sm.q_full[q], (uint32_t)last_q_phase[q]);
-      for (int s = 0; s < kStages; ++s)
-        if (last_kv_phase[s] >= 0) {
-          W.drain(&sm.k_full[s], (uint32_t)last_kv_phase[s]);
-          W.drain(&sm.v_full[s], (uint32_t)last_kv_phase[s]);
-        }
+      for (int s = 0; s < kStages; ++s) {
+        if (last_k_phase[s] >= 0) W.drain(&sm.k_full[s], (uint32_t)last_k_phase[s]);
+        if (last_v_phase[s] >= 0) W.drain(&sm.v_full[s], (uint32_t)last_v_phase[s]);
+      }
     }
   } else if (warp == 9) {
     // ================================================================ MMA issuer
@@ -311,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
           for (int q = 0; q < 2 && ok; ++q)
             if ((bits >> (4 * q)) & 0xF) ok = issue_s(q, ptx::smem_u32(sm.k[cur_stage]));
           if (!ok) break;
+          ptx::mma_commit(&sm.k_empty[cur_stage]);  // K of tile 0 is free once its S products are done
         }
         while (have) {
           int nkt, nbits = 0;
@@ -358,7 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
             ++n_k;
           }
           if (!ok) break;
-          ptx::mma_commit(&sm.kv_empty[cur_stage]);
+          ptx::mma_commit(&sm.v_empty[cur_stage]);             // V of this tile: P V products issued
+          if (nhave) ptx::mma_commit(&sm.k_empty[nst]);        // K of the next tile: S products issued
           have = nhave;
           cur_bits = nbits;
           cur_stage = nst;
