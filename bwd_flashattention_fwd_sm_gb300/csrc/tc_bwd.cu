@@ -271,19 +271,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
     }
   } else if (warp == 9) {
     // ================================================================ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t id_st = ptx::idesc_bf16(128, 64, false, false);   // S^T, dP^T
-      constexpr uint32_t id_acc = ptx::idesc_bf16(128, 128, false, true);  // dV, dK
-      constexpr uint32_t id_dq = ptx::idesc_bf16(128, 64, true, true);     // dQ^T
-      const uint32_t k_addr = ptx::smem_u32(sm.k), v_addr = ptx::smem_u32(sm.v);
-      uint32_t n_units = 0, gi = 0;  // gi: global step counter (all units)
-      bool ok = true;
+    // The whole warp runs the control flow in step; one elected lane issues the
+    // tensor-core instructions and commits (a lone diverged thread is starved of
+    // issue slots by the compute warps on its sub-partition).  elect.sync on the
+    // full, converged warp picks the same lane every time, so each commit covers
+    // every product issued before it.
+    constexpr uint32_t id_st = ptx::idesc_bf16(128, 64, false, false);   // S^T, dP^T
+    constexpr uint32_t id_acc = ptx::idesc_bf16(128, 128, false, true);  // dV, dK
+    constexpr uint32_t id_dq = ptx::idesc_bf16(128, 64, true, true);     // dQ^T
+    const uint32_t k_addr = ptx::smem_u32(sm.k), v_addr = ptx::smem_u32(sm.v);
+    uint32_t n_units = 0, gi = 0;  // gi: global step counter (all units)
+    bool ok = true;
 
-      auto issue_s = [&](uint32_t i) -> bool {  // S^T_i = K Q_i^T
-        const int st = i & 1, qs = i % kStages;
-        if (!W.one(&sm.qdo_full[qs], (i / kStages) & 1)) return false;
-        ptx::tc_fence_after();
-        const uint32_t q_addr = ptx::smem_u32(sm.q[qs]);
+    auto issue_s = [&](uint32_t i) -> bool {  // S^T_i = K Q_i^T
+      const int st = i & 1, qs = i % kStages;
+      if (!W.warp(&sm.qdo_full[qs], (i / kStages) & 1)) return false;
+      ptx::tc_fence_after();
+      const uint32_t q_addr = ptx::smem_u32(sm.q[qs]);
+      if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t ad = ptx::sdesc_sw128(k_addr + (kk >> 2) * kHalfTileBytes + (kk & 3) * 32, 16, 1024);
@@ -291,13 +296,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
           ptx::mma_ss(tmem + kColS + st * 64, ad, bd, id_st, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(&sm.st_full[st]);
-        return true;
-      };
-      auto issue_dp = [&](uint32_t i) -> bool {  // dP^T_i = V dO_i^T (stage known loaded)
-        const int qs = i % kStages;
-        if (i > 0 && !W.one(&sm.dp_free, (i - 1) & 1)) return false;
-        ptx::tc_fence_after();
-        const uint32_t do_addr = ptx::smem_u32(sm.dO[qs]);
+      }
+      __syncwarp();
+      return true;
+    };
+    auto issue_dp = [&](uint32_t i) -> bool {  // dP^T_i = V dO_i^T (stage known loaded)
+      const int qs = i % kStages;
+      if (i > 0 && !W.warp(&sm.dp_free, (i - 1) & 1)) return false;
+      ptx::tc_fence_after();
+      const uint32_t do_addr = ptx::smem_u32(sm.dO[qs]);
+      if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t ad = ptx::sdesc_sw128(v_addr + (kk >> 2) * kHalfTileBytes + (kk & 3) * 32, 16, 1024);
@@ -305,38 +313,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
           ptx::mma_ss(tmem + kColDP, ad, bd, id_st, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(&sm.dp_full);
-        return true;
-      };
+      }
+      __syncwarp();
+      return true;
+    };
 
-      for (;;) {
-        const int slot = n_units & 1;
-        if (!W.one(&sm.unit_full[slot], (n_units >> 1) & 1)) { ok = false; break; }
-        Unit un;
-        const bool valid = read_unit(sm, slot, un);
-        ptx::mbar_arrive(&sm.unit_empty[slot]);
-        if (!valid) break;
-        const SeqInfo si = seq_info(p, un.seq);
-        int n = 0;
-        {
-          BwdSteps t;
-          t.init(p, si.len, un.tile);
-          int hh, qb, bits;
-          while (t.next(hh, qb, bits)) ++n;
-        }
-        if (!W.one(&sm.kv_full, n_units & 1)) { ok = false; break; }
+    for (;;) {
+      const int slot = n_units & 1;
+      if (!W.warp(&sm.unit_full[slot], (n_units >> 1) & 1)) { ok = false; break; }
+      Unit un;
+      const bool valid = read_unit(sm, slot, un);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sm.unit_empty[slot]);
+      if (!valid) break;
+      const SeqInfo si = seq_info(p, un.seq);
+      int n = 0;
+      {
+        BwdSteps t;
+        t.init(p, si.len, un.tile);
+        int hh, qb, bits;
+        while (t.next(hh, qb, bits)) ++n;
+      }
+      if (!W.warp(&sm.kv_full, n_units & 1)) { ok = false; break; }
+      ptx::tc_fence_after();
+      if (n > 0) ok = issue_s(gi) && issue_dp(gi);
+      for (int s = 0; ok && s < n; ++s) {
+        const uint32_t i = gi + s;
+        const int st = i & 1, qs = i % kStages;
+        if (s + 1 < n && !issue_s(i + 1)) { ok = false; break; }
+        // dV += P^T_i dO_i: A = P^T from tensor memory, B = dO_i as (head dim, query) MN-major
+        if (!W.warp(&sm.pt_full[st], (i >> 1) & 1)) { ok = false; break; }
+        // before the unit's first dV / dK product: the previous unit's epilogue
+        // has read both accumulators
+        if (s == 0 && !W.warp(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
         ptx::tc_fence_after();
-        if (n > 0) ok = issue_s(gi) && issue_dp(gi);
-        for (int s = 0; ok && s < n; ++s) {
-          const uint32_t i = gi + s;
-          const int st = i & 1, qs = i % kStages;
-          if (s + 1 < n && !issue_s(i + 1)) { ok = false; break; }
-          // dV += P^T_i dO_i: A = P^T from tensor memory, B = dO_i as (head dim, query) MN-major
-          if (!W.one(&sm.pt_full[st], (i >> 1) & 1)) { ok = false; break; }
-          // before the unit's first dV / dK product: the previous unit's epilogue
-          // has read both accumulators
-          if (s == 0 && !W.one(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
-          ptx::tc_fence_after();
-          const uint32_t q_addr = ptx::smem_u32(sm.q[qs]), do_addr = ptx::smem_u32(sm.dO[qs]);
+        const uint32_t q_addr = ptx::smem_u32(sm.q[qs]), do_addr = ptx::smem_u32(sm.dO[qs]);
+        if (ptx::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             // P^T of query columns 16 kk .. +15: the compute warps of column half
@@ -345,21 +357,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
             const uint64_t bd = ptx::sdesc_sw128(do_addr + kk * 2048, kQBoxBytes, 1024);
             ptx::mma_ts(tmem + kColDV, tmem + a_col, bd, id_acc, (s > 0 || kk > 0) ? 1u : 0u);
           }
-          if (s + 1 < n && !issue_dp(i + 1)) { ok = false; break; }
-          // dK += dS^T_i Q_i: A = dS^T (key rows, query contiguous), B = Q_i MN-major
-          if (!W.one(&sm.ds_full[st], (i >> 1) & 1)) { ok = false; break; }
-          ptx::tc_fence_after();
-          const uint32_t ds_addr = ptx::smem_u32(sm.ds[st]);
+        }
+        __syncwarp();
+        if (s + 1 < n && !issue_dp(i + 1)) { ok = false; break; }
+        // dK += dS^T_i Q_i: A = dS^T (key rows, query contiguous), B = Q_i MN-major
+        if (!W.warp(&sm.ds_full[st], (i >> 1) & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t ds_addr = ptx::smem_u32(sm.ds[st]);
+        if (ptx::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = ptx::sdesc_sw128(ds_addr + kk * 32, 16, 1024);
             const uint64_t bd = ptx::sdesc_sw128(q_addr + kk * 2048, kQBoxBytes, 1024);
             ptx::mma_ss(tmem + kColDK, ad, bd, id_acc, (s > 0 || kk > 0) ? 1u : 0u);
           }
-          // dQ_i^T = K^T dS^T_i: A = K^T (head dim contiguous: MN-major), B = dS^T as
-          // (query, key) with query contiguous: MN-major
-          if (i > 0 && !W.one(&sm.dq_free, (i - 1) & 1)) { ok = false; break; }
-          ptx::tc_fence_after();
+        }
+        __syncwarp();
+        // dQ_i^T = K^T dS^T_i: A = K^T (head dim contiguous: MN-major), B = dS^T as
+        // (query, key) with query contiguous: MN-major
+        if (i > 0 && !W.warp(&sm.dq_free, (i - 1) & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t ad = ptx::sdesc_sw128(k_addr + kk * 2048, kHalfTileBytes, 1024);
@@ -370,17 +388,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
           ptx::mma_commit(&sm.qdo_empty[qs]);
           ptx::mma_commit(&sm.ds_free[st]);
         }
-        if (!ok) break;
-        if (n == 0 && !W.one(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
-        gi += n;
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (n == 0 && !W.warp(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
+      gi += n;
+      if (ptx::elect_one()) {
         ptx::mma_commit(&sm.kv_empty);
         ptx::mma_commit(&sm.acc_done);
-        ++n_units;
       }
-      (void)ok;
-      ptx::mma_commit(&sm.drain);
-      W.drain(&sm.drain, 0);
+      __syncwarp();
+      ++n_units;
     }
+    (void)ok;
+    __syncwarp();
+    if (ptx::elect_one()) ptx::mma_commit(&sm.drain);
+    __syncwarp();
+    if (lane == 0) W.drain(&sm.drain, 0);
+    __syncwarp();
   } else {
     // ================================================================ compute warps
     const int qr = warp & 3, ch = warp >> 2;  // TMEM lane quarter, query-column half

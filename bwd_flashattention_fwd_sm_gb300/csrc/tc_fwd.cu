@@ -274,43 +274,50 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     }
   } else if (warp == 9) {
     // ================================================================ MMA issuer
-    // One thread runs this role; it takes part in the unit ring on its own.
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idesc_pv = ptx::idesc_bf16(128, 128, false, true);
-      uint32_t n_units_seen = 0, n_q[2] = {0, 0}, n_p[2] = {0, 0}, n_o[2] = {0, 0};
-      uint32_t n_k = 0, n_v = 0;
-      bool ok = true;
-      for (;;) {
-        const int slot = n_units_seen & 1;
-        if (!W.one(&sm.unit_full[slot], (n_units_seen >> 1) & 1)) { ok = false; break; }
-        Unit un;
-        const bool valid = read_unit(sm, slot, un);
-        ptx::mbar_arrive(&sm.unit_empty[slot]);
-        ++n_units_seen;
-        if (!valid) break;
+    // The whole warp runs the control flow (waits, descriptors) in step; one
+    // elected lane issues the tensor-core instructions and their commits.  A
+    // lone diverged thread issuing them is starved of issue slots by the
+    // softmax warps on its sub-partition and leaves the tensor core idle.
+    // elect.sync on the full, converged warp picks the same lane every time, so
+    // each commit covers every product issued before it.
+    constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, false, false);
+    constexpr uint32_t idesc_pv = ptx::idesc_bf16(128, 128, false, true);
+    uint32_t n_units_seen = 0, n_q[2] = {0, 0}, n_p[2] = {0, 0}, n_o[2] = {0, 0};
+    uint32_t n_k = 0, n_v = 0;
+    bool ok = true;
+    for (;;) {
+      const int slot = n_units_seen & 1;
+      if (!W.warp(&sm.unit_full[slot], (n_units_seen >> 1) & 1)) { ok = false; break; }
+      Unit un;
+      const bool valid = read_unit(sm, slot, un);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sm.unit_empty[slot]);
+      ++n_units_seen;
+      if (!valid) break;
 
-        const SeqInfo si = seq_info(p, un.seq);
-        KvTileList2<kSparse> tl;
-        tl.init(p, si.len, un.tile * 2 * kTile);
-        int n_act[2] = {0, 0};
-        {
-          KvTileList2<kSparse> t = tl;
-          int kt, bits;
-          while (t.next(kt, bits)) {
-            n_act[0] += (bits & 0xF) != 0;
-            n_act[1] += (bits & 0xF0) != 0;
-          }
+      const SeqInfo si = seq_info(p, un.seq);
+      KvTileList2<kSparse> tl;
+      tl.init(p, si.len, un.tile * 2 * kTile);
+      int n_act[2] = {0, 0};
+      {
+        KvTileList2<kSparse> t = tl;
+        int kt, bits;
+        while (t.next(kt, bits)) {
+          n_act[0] += (bits & 0xF) != 0;
+          n_act[1] += (bits & 0xF0) != 0;
         }
-        int s_issued[2] = {0, 0}, pv_issued[2] = {0, 0};
-        // S_q = Q_q K^T into S_q; after the unit's last one, Q_q may be refilled.
-        auto issue_s = [&](int q, uint32_t k_addr) -> bool {
-          if (s_issued[q] == 0) {
-            if (!W.one(&sm.q_full[q], n_q[q] & 1)) return false;
-            ++n_q[q];
-            ptx::tc_fence_after();
-          }
-          const uint32_t q_addr = ptx::smem_u32(sm.q[q]);
+      }
+      int s_issued[2] = {0, 0}, pv_issued[2] = {0, 0};
+      // S_q = Q_q K^T into S_q; after the unit's last one, Q_q may be refilled.
+      auto issue_s = [&](int q, uint32_t k_addr) -> bool {
+        if (s_issued[q] == 0) {
+          if (!W.warp(&sm.q_full[q], n_q[q] & 1)) return false;
+          ++n_q[q];
+          ptx::tc_fence_after();
+        }
+        const uint32_t q_addr = ptx::smem_u32(sm.q[q]);
+        const bool last = ++s_issued[q] == n_act[q];
+        if (ptx::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
@@ -318,83 +325,94 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
                         ptx::sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
           }
           ptx::mma_commit(&sm.s_full[q]);
-          if (++s_issued[q] == n_act[q]) ptx::mma_commit(&sm.q_empty[q]);
-          return true;
-        };
-
-        KvTileList2<kSparse> t = tl;
-        int kt, bits;
-        bool have = t.next(kt, bits);
-        uint32_t cur_stage = 0;
-        int cur_bits = bits;
-        if (have) {  // prologue: S of the first tile
-          cur_stage = n_k % kStages;
-          if (!W.one(&sm.k_full[cur_stage], (n_k / kStages) & 1)) { ok = false; break; }
-          ++n_k;
-          ptx::tc_fence_after();
-          for (int q = 0; q < 2 && ok; ++q)
-            if ((bits >> (4 * q)) & 0xF) ok = issue_s(q, ptx::smem_u32(sm.k[cur_stage]));
-          if (!ok) break;
-          ptx::mma_commit(&sm.k_empty[cur_stage]);  // K of tile 0 is free once its S products are done
+          if (last) ptx::mma_commit(&sm.q_empty[q]);
         }
-        while (have) {
-          int nkt, nbits = 0;
-          const bool nhave = t.next(nkt, nbits);
-          const uint32_t nst = n_k % kStages;
-          bool k_next_ready = false;  // K of the next tile is waited for only when first needed
-          if (!W.one(&sm.v_full[cur_stage], (n_v / kStages) & 1)) { ok = false; break; }
-          ++n_v;
-          ptx::tc_fence_after();
-          const uint32_t v_addr = ptx::smem_u32(sm.v[cur_stage]);
-          for (int q = 0; q < 2 && ok; ++q) {
-            if ((cur_bits >> (4 * q)) & 0xF) {
-              // O_q += P_q V.  Before the unit's first product, the previous unit's
-              // epilogue must have read O_q.
-              if (!W.one(&sm.p_full[q], n_p[q] & 1)) { ok = false; break; }
-              ++n_p[q];
-              if (pv_issued[q] == 0 && !W.one(&sm.o_free[q], (n_o[q] & 1) ^ 1)) { ok = false; break; }
-              ptx::tc_fence_after();
+        __syncwarp();
+        return true;
+      };
+
+      KvTileList2<kSparse> t = tl;
+      int kt, bits;
+      bool have = t.next(kt, bits);
+      uint32_t cur_stage = 0;
+      int cur_bits = bits;
+      if (have) {  // prologue: S of the first tile
+        cur_stage = n_k % kStages;
+        if (!W.warp(&sm.k_full[cur_stage], (n_k / kStages) & 1)) { ok = false; break; }
+        ++n_k;
+        ptx::tc_fence_after();
+        for (int q = 0; q < 2 && ok; ++q)
+          if ((bits >> (4 * q)) & 0xF) ok = issue_s(q, ptx::smem_u32(sm.k[cur_stage]));
+        if (!ok) break;
+        // K of tile 0 is free once its S products are done
+        if (ptx::elect_one()) ptx::mma_commit(&sm.k_empty[cur_stage]);
+        __syncwarp();
+      }
+      while (have) {
+        int nkt, nbits = 0;
+        const bool nhave = t.next(nkt, nbits);
+        const uint32_t nst = n_k % kStages;
+        bool k_next_ready = false;  // K of the next tile is waited for only when first needed
+        if (!W.warp(&sm.v_full[cur_stage], (n_v / kStages) & 1)) { ok = false; break; }
+        ++n_v;
+        ptx::tc_fence_after();
+        const uint32_t v_addr = ptx::smem_u32(sm.v[cur_stage]);
+        for (int q = 0; q < 2 && ok; ++q) {
+          if ((cur_bits >> (4 * q)) & 0xF) {
+            // O_q += P_q V.  Before the unit's first product, the previous unit's
+            // epilogue must have read O_q.
+            if (!W.warp(&sm.p_full[q], n_p[q] & 1)) { ok = false; break; }
+            ++n_p[q];
+            if (pv_issued[q] == 0 && !W.warp(&sm.o_free[q], (n_o[q] & 1) ^ 1)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t acc0 = pv_issued[q] > 0 ? 1u : 0u;
+            const bool last = ++pv_issued[q] == n_act[q];
+            if (ptx::elect_one()) {
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
                 // B = V as (N = head dim, K = keys), head dim contiguous: MN-major.
                 const uint64_t bdesc = ptx::sdesc_sw128(v_addr + kk * 2048, kHalfTileBytes, 1024);
-                ptx::mma_ts(tmem + 256 + q * 128, tmem + q * 128 + kk * 8, bdesc, idesc_pv,
-                            (pv_issued[q] > 0 || kk > 0) ? 1u : 0u);
+                ptx::mma_ts(tmem + 256 + q * 128, tmem + q * 128 + kk * 8, bdesc, idesc_pv, kk > 0 ? 1u : acc0);
               }
-              if (++pv_issued[q] == n_act[q]) {
-                ptx::mma_commit(&sm.o_final[q]);
-                ++n_o[q];
-              }
+              if (last) ptx::mma_commit(&sm.o_final[q]);
             }
-            // S_q of the next tile: the S_q buffer held P_q, consumed by the product above
-            if (nhave && ((nbits >> (4 * q)) & 0xF)) {
-              if (!k_next_ready) {
-                if (!W.one(&sm.k_full[nst], (n_k / kStages) & 1)) { ok = false; break; }
-                ++n_k;
-                k_next_ready = true;
-                ptx::tc_fence_after();
-              }
-              if (!issue_s(q, ptx::smem_u32(sm.k[nst]))) ok = false;
+            __syncwarp();
+            if (last) ++n_o[q];
+          }
+          // S_q of the next tile: the S_q buffer held P_q, consumed by the product above
+          if (nhave && ((nbits >> (4 * q)) & 0xF)) {
+            if (!k_next_ready) {
+              if (!W.warp(&sm.k_full[nst], (n_k / kStages) & 1)) { ok = false; break; }
+              ++n_k;
+              k_next_ready = true;
+              ptx::tc_fence_after();
             }
+            if (!issue_s(q, ptx::smem_u32(sm.k[nst]))) ok = false;
           }
-          // a tile whose K nobody here needed still has to be consumed from the ring
-          if (ok && nhave && !k_next_ready) {
-            if (!W.one(&sm.k_full[nst], (n_k / kStages) & 1)) ok = false;
-            ++n_k;
-          }
-          if (!ok) break;
-          ptx::mma_commit(&sm.v_empty[cur_stage]);             // V of this tile: P V products issued
-          if (nhave) ptx::mma_commit(&sm.k_empty[nst]);        // K of the next tile: S products issued
-          have = nhave;
-          cur_bits = nbits;
-          cur_stage = nst;
+        }
+        // a tile whose K nobody here needed still has to be consumed from the ring
+        if (ok && nhave && !k_next_ready) {
+          if (!W.warp(&sm.k_full[nst], (n_k / kStages) & 1)) ok = false;
+          ++n_k;
         }
         if (!ok) break;
+        if (ptx::elect_one()) {
+          ptx::mma_commit(&sm.v_empty[cur_stage]);       // V of this tile: P V products issued
+          if (nhave) ptx::mma_commit(&sm.k_empty[nst]);  // K of the next tile: S products issued
+        }
+        __syncwarp();
+        have = nhave;
+        cur_bits = nbits;
+        cur_stage = nst;
       }
-      (void)ok;
-      ptx::mma_commit(&sm.drain);
-      W.drain(&sm.drain, 0);
+      if (!ok) break;
     }
+    (void)ok;
+    __syncwarp();
+    if (ptx::elect_one()) ptx::mma_commit(&sm.drain);
+    __syncwarp();
+    if (lane == 0) W.drain(&sm.drain, 0);
+    __syncwarp();
   } else if (warp < 8) {
     // ================================================================ softmax
     ptx::regs_increase<kRegsSoftmax>();
