@@ -28,8 +28,9 @@
 //                    whole 128-column S row in registers; max and sum in 8
 //                    independent partials to keep dependency chains short)
 //   warp 8           TMA producer and unit fetcher
-//   warp 9           tensor-core issuer
-//   warps 10-11      idle (they complete the third warpgroup, whose registers
+//   warps 9 / 10     tensor-core issuers for query tile 0 / 1 (each waits on
+//                    its own tile's barriers while the other's products run)
+//   warp 11          idle (it completes the third warpgroup, whose registers
 //                    the softmax warpgroups borrow)
 // Every wait is bounded; a CTA that gives up records ATTN_ERR_DEVICE_TIMEOUT,
 // drains its copies and tensor-core work, frees tensor memory and returns.
@@ -66,7 +67,7 @@ struct Smem {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
   uint64_t s_full[2], p_full[2], o_final[2], o_free[2];
-  uint64_t drain;
+  uint64_t drain[2];
   int unit_slot[2][4];  // seq, head, 256-row tile, valid
   uint32_t tmem_base;
   ptx::Abort abort;
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&sm.unit_full[i], 1);
-      ptx::mbar_init(&sm.unit_empty[i], 9);  // MMA warp + 8 softmax warps
+      ptx::mbar_init(&sm.unit_empty[i], 10);  // 2 MMA warps + 8 softmax warps
       ptx::mbar_init(&sm.q_full[i], 1);
       ptx::mbar_init(&sm.q_empty[i], 1);
       ptx::mbar_init(&sm.s_full[i], 1);
@@ -151,10 +152,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&sm.k_full[s], 1);
       ptx::mbar_init(&sm.v_full[s], 1);
-      ptx::mbar_init(&sm.k_empty[s], 1);
-      ptx::mbar_init(&sm.v_empty[s], 1);
+      ptx::mbar_init(&sm.k_empty[s], 2);  // one commit per MMA warp
+      ptx::mbar_init(&sm.v_empty[s], 2);
     }
-    ptx::mbar_init(&sm.drain, 1);
+    ptx::mbar_init(&sm.drain[0], 1);
+    ptx::mbar_init(&sm.drain[1], 1);
     sm.abort.flag = 0;
     ptx::fence_mbar_init();
   }
@@ -272,18 +274,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         if (last_v_phase[s] >= 0) W.drain(&sm.v_full[s], (uint32_t)last_v_phase[s]);
       }
     }
-  } else if (warp == 9) {
-    // ================================================================ MMA issuer
-    // The whole warp runs the control flow (waits, descriptors) in step; one
-    // elected lane issues the tensor-core instructions and their commits.  A
-    // lone diverged thread issuing them is starved of issue slots by the
-    // softmax warps on its sub-partition and leaves the tensor core idle.
-    // elect.sync on the full, converged warp picks the same lane every time, so
-    // each commit covers every product issued before it.
+  } else if (warp == 9 || warp == 10) {
+    // ================================================================ MMA issuers
+    // Warp 9 + q issues the products of query tile q: S_q = Q_q K^T and
+    // O_q += P_q V.  Each tcgen05.mma holds its issuing thread until the tensor
+    // core takes it, so a single issuer's barrier waits left the tensor core
+    // idle; with one issuer per tile, one waits while the other's products run.
+    // Both issuers walk every key tile of the unit and commit once per K / V
+    // stage (the empty barriers count two), so the ring stays in step even for
+    // tiles where one query tile has no visible keys.
+    // The whole warp runs the control flow; elect.sync on the full, converged
+    // warp picks the same lane every time, so each commit covers every product
+    // that lane issued before it.
+    const int q = warp - 9;
     constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, false, false);
     constexpr uint32_t idesc_pv = ptx::idesc_bf16(128, 128, false, true);
-    uint32_t n_units_seen = 0, n_q[2] = {0, 0}, n_p[2] = {0, 0}, n_o[2] = {0, 0};
-    uint32_t n_k = 0, n_v = 0;
+    const uint32_t q_addr = ptx::smem_u32(sm.q[q]);
+    const uint32_t t_s = tmem + q * 128, t_o = tmem + 256 + q * 128;
+    uint32_t n_units_seen = 0, n_q = 0, n_p = 0, n_o = 0, n_k = 0, n_v = 0;
     bool ok = true;
     for (;;) {
       const int slot = n_units_seen & 1;
@@ -298,31 +306,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       const SeqInfo si = seq_info(p, un.seq);
       KvTileList2<kSparse> tl;
       tl.init(p, si.len, un.tile * 2 * kTile);
-      int n_act[2] = {0, 0};
+      int n_act = 0;
       {
         KvTileList2<kSparse> t = tl;
         int kt, bits;
-        while (t.next(kt, bits)) {
-          n_act[0] += (bits & 0xF) != 0;
-          n_act[1] += (bits & 0xF0) != 0;
-        }
+        while (t.next(kt, bits)) n_act += ((bits >> (4 * q)) & 0xF) != 0;
       }
-      int s_issued[2] = {0, 0}, pv_issued[2] = {0, 0};
+      int s_issued = 0, pv_issued = 0;
       // S_q = Q_q K^T into S_q; after the unit's last one, Q_q may be refilled.
-      auto issue_s = [&](int q, uint32_t k_addr) -> bool {
-        if (s_issued[q] == 0) {
-          if (!W.warp(&sm.q_full[q], n_q[q] & 1)) return false;
-          ++n_q[q];
+      auto issue_s = [&](uint32_t k_addr) -> bool {
+        if (s_issued == 0) {
+          if (!W.warp(&sm.q_full[q], n_q & 1)) return false;
+          ++n_q;
           ptx::tc_fence_after();
         }
-        const uint32_t q_addr = ptx::smem_u32(sm.q[q]);
-        const bool last = ++s_issued[q] == n_act[q];
+        const bool last = ++s_issued == n_act;
         if (ptx::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
-            ptx::mma_ss(tmem + q * 128, ptx::sdesc_sw128(q_addr + off, 16, 1024),
-                        ptx::sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            ptx::mma_ss(t_s, ptx::sdesc_sw128(q_addr + off, 16, 1024), ptx::sdesc_sw128(k_addr + off, 16, 1024),
+                        idesc_s, kk > 0 ? 1u : 0u);
           }
           ptx::mma_commit(&sm.s_full[q]);
           if (last) ptx::mma_commit(&sm.q_empty[q]);
@@ -341,8 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         if (!W.warp(&sm.k_full[cur_stage], (n_k / kStages) & 1)) { ok = false; break; }
         ++n_k;
         ptx::tc_fence_after();
-        for (int q = 0; q < 2 && ok; ++q)
-          if ((bits >> (4 * q)) & 0xF) ok = issue_s(q, ptx::smem_u32(sm.k[cur_stage]));
+        if ((bits >> (4 * q)) & 0xF) ok = issue_s(ptx::smem_u32(sm.k[cur_stage]));
         if (!ok) break;
         // K of tile 0 is free once its S products are done
         if (ptx::elect_one()) ptx::mma_commit(&sm.k_empty[cur_stage]);
@@ -352,53 +355,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         int nkt, nbits = 0;
         const bool nhave = t.next(nkt, nbits);
         const uint32_t nst = n_k % kStages;
-        bool k_next_ready = false;  // K of the next tile is waited for only when first needed
         if (!W.warp(&sm.v_full[cur_stage], (n_v / kStages) & 1)) { ok = false; break; }
         ++n_v;
-        ptx::tc_fence_after();
-        const uint32_t v_addr = ptx::smem_u32(sm.v[cur_stage]);
-        for (int q = 0; q < 2 && ok; ++q) {
-          if ((cur_bits >> (4 * q)) & 0xF) {
-            // O_q += P_q V.  Before the unit's first product, the previous unit's
-            // epilogue must have read O_q.
-            if (!W.warp(&sm.p_full[q], n_p[q] & 1)) { ok = false; break; }
-            ++n_p[q];
-            if (pv_issued[q] == 0 && !W.warp(&sm.o_free[q], (n_o[q] & 1) ^ 1)) { ok = false; break; }
-            ptx::tc_fence_after();
-            const uint32_t acc0 = pv_issued[q] > 0 ? 1u : 0u;
-            const bool last = ++pv_issued[q] == n_act[q];
-            if (ptx::elect_one()) {
+        if ((cur_bits >> (4 * q)) & 0xF) {
+          // O_q += P_q V.  Before the unit's first product, the previous unit's
+          // epilogue must have read O_q.
+          if (!W.warp(&sm.p_full[q], n_p & 1)) { ok = false; break; }
+          ++n_p;
+          if (pv_issued == 0 && !W.warp(&sm.o_free[q], (n_o & 1) ^ 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t v_addr = ptx::smem_u32(sm.v[cur_stage]);
+          const uint32_t acc0 = pv_issued > 0 ? 1u : 0u;
+          const bool last = ++pv_issued == n_act;
+          if (ptx::elect_one()) {
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                // B = V as (N = head dim, K = keys), head dim contiguous: MN-major.
-                const uint64_t bdesc = ptx::sdesc_sw128(v_addr + kk * 2048, kHalfTileBytes, 1024);
-                ptx::mma_ts(tmem + 256 + q * 128, tmem + q * 128 + kk * 8, bdesc, idesc_pv, kk > 0 ? 1u : acc0);
-              }
-              if (last) ptx::mma_commit(&sm.o_final[q]);
+            for (int kk = 0; kk < 8; ++kk) {
+              // B = V as (N = head dim, K = keys), head dim contiguous: MN-major.
+              const uint64_t bdesc = ptx::sdesc_sw128(v_addr + kk * 2048, kHalfTileBytes, 1024);
+              ptx::mma_ts(t_o, t_s + kk * 8, bdesc, idesc_pv, kk > 0 ? 1u : acc0);
             }
-            __syncwarp();
-            if (last) ++n_o[q];
+            if (last) ptx::mma_commit(&sm.o_final[q]);
           }
-          // S_q of the next tile: the S_q buffer held P_q, consumed by the product above
-          if (nhave && ((nbits >> (4 * q)) & 0xF)) {
-            if (!k_next_ready) {
-              if (!W.warp(&sm.k_full[nst], (n_k / kStages) & 1)) { ok = false; break; }
-              ++n_k;
-              k_next_ready = true;
-              ptx::tc_fence_after();
-            }
-            if (!issue_s(q, ptx::smem_u32(sm.k[nst]))) ok = false;
-          }
+          __syncwarp();
+          if (last) ++n_o;
         }
-        // a tile whose K nobody here needed still has to be consumed from the ring
-        if (ok && nhave && !k_next_ready) {
-          if (!W.warp(&sm.k_full[nst], (n_k / kStages) & 1)) ok = false;
+        // S_q of the next tile: the S_q buffer held P_q, consumed by the product above
+        if (nhave) {
+          if (!W.warp(&sm.k_full[nst], (n_k / kStages) & 1)) { ok = false; break; }
           ++n_k;
+          ptx::tc_fence_after();
+          if (((nbits >> (4 * q)) & 0xF) && !issue_s(ptx::smem_u32(sm.k[nst]))) { ok = false; break; }
         }
-        if (!ok) break;
         if (ptx::elect_one()) {
-          ptx::mma_commit(&sm.v_empty[cur_stage]);       // V of this tile: P V products issued
-          if (nhave) ptx::mma_commit(&sm.k_empty[nst]);  // K of the next tile: S products issued
+          ptx::mma_commit(&sm.v_empty[cur_stage]);       // V of this tile: this warp's P V product issued
+          if (nhave) ptx::mma_commit(&sm.k_empty[nst]);  // K of the next tile: this warp's S product issued
         }
         __syncwarp();
         have = nhave;
@@ -409,9 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     }
     (void)ok;
     __syncwarp();
-    if (ptx::elect_one()) ptx::mma_commit(&sm.drain);
+    if (ptx::elect_one()) ptx::mma_commit(&sm.drain[q]);
     __syncwarp();
-    if (lane == 0) W.drain(&sm.drain, 0);
+    if (lane == 0) W.drain(&sm.drain[q], 0);
     __syncwarp();
   } else if (warp < 8) {
     // ================================================================ softmax
