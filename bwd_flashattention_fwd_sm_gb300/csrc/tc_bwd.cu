@@ -22,15 +22,22 @@
 // section 4.2: whoever finishes first takes the next block) and hands it to the
 // other roles through a two-slot ring in shared memory.
 //
-// Warp roles (320 threads):
-//   warps 0-7  compute: warp w covers TMEM lane quarter w % 4 (key rows, or head-
-//              dim columns for dQ^T) and query columns 32 (w / 4) .. +31 of the
-//              step.  Per step: P^T, dS^T, then the previous step's dQ^T
-//              (read from tensor memory one step late, so the dK and dQ products
-//              never hold these warps up) staged in shared memory and added by a
-//              TMA reduce.  Unit epilogue: warps 0-3 dK, warps 4-7 dV.
-//   warp 8     TMA producer (K, V per unit; Q_i, dO_i in a 3-stage ring; LSE, D rows)
-//   warp 9     tensor-core issuer (one thread)
+// Warp roles (448 threads):
+//   warps 0-7    compute: warp w covers TMEM lane quarter w % 4 (key rows) and
+//                query columns 32 (w / 4) .. +31 of the step.  Per step: P^T and
+//                dS^T.  Unit epilogue: warps 0-3 dK, warps 4-7 dV.
+//   warp 8       TMA producer (K, V per unit; Q_i, dO_i in a 3-stage ring; LSE, D rows)
+//   warp 9       tensor-core issuer for S^T, dP^T and dV (whole warp, one
+//                elected lane issues)
+//   warp 14      tensor-core issuer for dK and dQ^T.  tcgen05.mma holds its
+//                thread until the tensor core takes it, so with one issuer every
+//                barrier wait left the tensor core idle; with two, one waits
+//                while the other's products run.
+//   warps 10-13  dQ writers: warp w reads head-dim rows 32 (w % 4) .. +31 of
+//                dQ_i^T from tensor memory, stages them in shared memory as
+//                [query][head dim], and one thread adds the tile into the float32
+//                accumulator with a TMA reduce; this runs beside the next step's
+//                P^T / dS^T work instead of inside it.
 // Every mbarrier wait is bounded; a CTA that gives up records
 // ATTN_ERR_DEVICE_TIMEOUT, drains its copies and tensor-core work, frees tensor
 // memory and returns.
@@ -49,7 +56,7 @@ constexpr uint32_t kQBoxBytes = kQB * 128;        // 64 rows x 64 bf16 (128-byte
 constexpr uint32_t kQTileBytes = 2 * kQBoxBytes;  // 64 x 128 bf16
 constexpr uint32_t kDsBytes = kTile * kQB * 2;    // dS^T: 128 key rows x 64 bf16 query columns
 constexpr int kStages = 3;  // Q_i / dO_i ring: loads run two steps ahead of the products
-constexpr int kThreads = 320;
+constexpr int kThreads = 480;
 constexpr uint32_t kTmemCols = 512;
 // dV [0,128) dK [128,256) S^T [256,320) [320,384) dP^T [384,448) dQ^T [448,512)
 constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384, kColDQ = 448;
@@ -72,7 +79,7 @@ struct Smem {
   uint64_t unit_full[2], unit_empty[2];
   uint64_t kv_full, kv_empty, qdo_full[kStages], qdo_empty[kStages];
   uint64_t st_full[2], pt_full[2], dp_full, dp_free, ds_full[2], ds_free[2], dq_full, dq_free;
-  uint64_t acc_done, acc_free, drain;
+  uint64_t acc_done, acc_free, drain[2];
   int unit_slot[2][4];
   uint32_t tmem_base;
   ptx::Abort abort;
@@ -120,7 +127,20 @@ __device__ __forceinline__ bool group_all(bool pred) {
       : "memory");
   return r != 0;
 }
-__device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// The same over the 128 dQ-writer threads (named barrier 2).
+__device__ __forceinline__ bool dq_all(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 2, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void dq_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 // One warp writes its 32 key rows of a 128-column accumulator (x scale, bf16)
 // straight from tensor memory to global memory rows k0 + row < len of head g.
@@ -162,25 +182,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&sm.qdo_full[s], 2);  // TMA transaction arrival + LSE/D rows written
-      ptx::mbar_init(&sm.qdo_empty[s], 1);
+      ptx::mbar_init(&sm.qdo_empty[s], 2);  // one commit per MMA warp
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&sm.unit_full[s], 1);
-      ptx::mbar_init(&sm.unit_empty[s], 9);  // MMA thread + 8 compute warps
+      ptx::mbar_init(&sm.unit_empty[s], 14);  // 2 MMA warps + 8 compute warps + 4 dQ writers
       ptx::mbar_init(&sm.st_full[s], 1);
       ptx::mbar_init(&sm.pt_full[s], 8);
       ptx::mbar_init(&sm.ds_full[s], 8);
       ptx::mbar_init(&sm.ds_free[s], 1);
     }
     ptx::mbar_init(&sm.kv_full, 1);
-    ptx::mbar_init(&sm.kv_empty, 1);
+    ptx::mbar_init(&sm.kv_empty, 2);  // one commit per MMA warp
     ptx::mbar_init(&sm.dp_full, 1);
     ptx::mbar_init(&sm.dp_free, 8);
     ptx::mbar_init(&sm.dq_full, 1);
-    ptx::mbar_init(&sm.dq_free, 8);
-    ptx::mbar_init(&sm.acc_done, 1);
+    ptx::mbar_init(&sm.dq_free, 4);  // dQ writer warps
+    ptx::mbar_init(&sm.acc_done, 2);  // dV issuer + dK issuer
     ptx::mbar_init(&sm.acc_free, 8);  // dK writers (warps 0-3) + dV writers (warps 4-7)
-    ptx::mbar_init(&sm.drain, 1);
+    ptx::mbar_init(&sm.drain[0], 1);
+    ptx::mbar_init(&sm.drain[1], 1);
     sm.abort.flag = 0;
     ptx::fence_mbar_init();
   }
@@ -269,13 +290,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       for (int s = 0; s < kStages; ++s)
         if (last_qdo_phase[s] >= 0) W.drain(&sm.qdo_full[s], (uint32_t)last_qdo_phase[s]);
     }
-  } else if (warp == 9) {
-    // ================================================================ MMA issuer
+  } else if (warp == 9 || warp == 14) {
+    // ================================================================ MMA issuers
     // The whole warp runs the control flow in step; one elected lane issues the
     // tensor-core instructions and commits (a lone diverged thread is starved of
     // issue slots by the compute warps on its sub-partition).  elect.sync on the
     // full, converged warp picks the same lane every time, so each commit covers
-    // every product issued before it.
+    // every product that lane issued before it.  Both warps walk the same steps;
+    // barriers that free a resource both use (Q_i / dO_i stage, K / V tiles, the
+    // unit's accumulators) count one commit from each.
+    const int side = warp == 9 ? 0 : 1;  // 0: S^T, dP^T, dV   1: dK, dQ^T
     constexpr uint32_t id_st = ptx::idesc_bf16(128, 64, false, false);   // S^T, dP^T
     constexpr uint32_t id_acc = ptx::idesc_bf16(128, 128, false, true);  // dV, dK
     constexpr uint32_t id_dq = ptx::idesc_bf16(128, 64, true, true);     // dQ^T
@@ -336,59 +360,71 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       }
       if (!W.warp(&sm.kv_full, n_units & 1)) { ok = false; break; }
       ptx::tc_fence_after();
-      if (n > 0) ok = issue_s(gi) && issue_dp(gi);
-      for (int s = 0; ok && s < n; ++s) {
-        const uint32_t i = gi + s;
-        const int st = i & 1, qs = i % kStages;
-        if (s + 1 < n && !issue_s(i + 1)) { ok = false; break; }
-        // dV += P^T_i dO_i: A = P^T from tensor memory, B = dO_i as (head dim, query) MN-major
-        if (!W.warp(&sm.pt_full[st], (i >> 1) & 1)) { ok = false; break; }
-        // before the unit's first dV / dK product: the previous unit's epilogue
-        // has read both accumulators
-        if (s == 0 && !W.warp(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
-        ptx::tc_fence_after();
-        const uint32_t q_addr = ptx::smem_u32(sm.q[qs]), do_addr = ptx::smem_u32(sm.dO[qs]);
-        if (ptx::elect_one()) {
+      if (side == 0) {
+        if (n > 0) ok = issue_s(gi) && issue_dp(gi);
+        for (int s = 0; ok && s < n; ++s) {
+          const uint32_t i = gi + s;
+          const int st = i & 1, qs = i % kStages;
+          if (s + 1 < n && !issue_s(i + 1)) { ok = false; break; }
+          // dV += P^T_i dO_i: A = P^T from tensor memory, B = dO_i as (head dim, query) MN-major
+          if (!W.warp(&sm.pt_full[st], (i >> 1) & 1)) { ok = false; break; }
+          // before the unit's first dV product: the previous unit's epilogue has
+          // read the accumulators
+          if (s == 0 && !W.warp(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t do_addr = ptx::smem_u32(sm.dO[qs]);
+          if (ptx::elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // P^T of query columns 16 kk .. +15: the compute warps of column half
-            // kk / 2 write their 16 packed columns at 32 (kk / 2) within the S^T buffer
-            const uint32_t a_col = kColS + st * 64 + 32 * (kk >> 1) + (kk & 1) * 8;
-            const uint64_t bd = ptx::sdesc_sw128(do_addr + kk * 2048, kQBoxBytes, 1024);
-            ptx::mma_ts(tmem + kColDV, tmem + a_col, bd, id_acc, (s > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              // P^T of query columns 16 kk .. +15: the compute warps of column half
+              // kk / 2 write their 16 packed columns at 32 (kk / 2) within the S^T buffer
+              const uint32_t a_col = kColS + st * 64 + 32 * (kk >> 1) + (kk & 1) * 8;
+              const uint64_t bd = ptx::sdesc_sw128(do_addr + kk * 2048, kQBoxBytes, 1024);
+              ptx::mma_ts(tmem + kColDV, tmem + a_col, bd, id_acc, (s > 0 || kk > 0) ? 1u : 0u);
+            }
           }
+          __syncwarp();
+          if (s + 1 < n && !issue_dp(i + 1)) { ok = false; break; }
+          // this side is done with Q_i / dO_i once S^T_i, dP^T_i and dV's product are
+          if (ptx::elect_one()) ptx::mma_commit(&sm.qdo_empty[qs]);
+          __syncwarp();
         }
-        __syncwarp();
-        if (s + 1 < n && !issue_dp(i + 1)) { ok = false; break; }
-        // dK += dS^T_i Q_i: A = dS^T (key rows, query contiguous), B = Q_i MN-major
-        if (!W.warp(&sm.ds_full[st], (i >> 1) & 1)) { ok = false; break; }
-        ptx::tc_fence_after();
-        const uint32_t ds_addr = ptx::smem_u32(sm.ds[st]);
-        if (ptx::elect_one()) {
+      } else {
+        for (int s = 0; ok && s < n; ++s) {
+          const uint32_t i = gi + s;
+          const int st = i & 1, qs = i % kStages;
+          // dK += dS^T_i Q_i: A = dS^T (key rows, query contiguous), B = Q_i MN-major
+          if (!W.warp(&sm.qdo_full[qs], (i / kStages) & 1)) { ok = false; break; }
+          if (!W.warp(&sm.ds_full[st], (i >> 1) & 1)) { ok = false; break; }
+          if (s == 0 && !W.warp(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t q_addr = ptx::smem_u32(sm.q[qs]), ds_addr = ptx::smem_u32(sm.ds[st]);
+          if (ptx::elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ad = ptx::sdesc_sw128(ds_addr + kk * 32, 16, 1024);
-            const uint64_t bd = ptx::sdesc_sw128(q_addr + kk * 2048, kQBoxBytes, 1024);
-            ptx::mma_ss(tmem + kColDK, ad, bd, id_acc, (s > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = ptx::sdesc_sw128(ds_addr + kk * 32, 16, 1024);
+              const uint64_t bd = ptx::sdesc_sw128(q_addr + kk * 2048, kQBoxBytes, 1024);
+              ptx::mma_ss(tmem + kColDK, ad, bd, id_acc, (s > 0 || kk > 0) ? 1u : 0u);
+            }
           }
-        }
-        __syncwarp();
-        // dQ_i^T = K^T dS^T_i: A = K^T (head dim contiguous: MN-major), B = dS^T as
-        // (query, key) with query contiguous: MN-major
-        if (i > 0 && !W.warp(&sm.dq_free, (i - 1) & 1)) { ok = false; break; }
-        ptx::tc_fence_after();
-        if (ptx::elect_one()) {
+          __syncwarp();
+          // dQ_i^T = K^T dS^T_i: A = K^T (head dim contiguous: MN-major), B = dS^T as
+          // (query, key) with query contiguous: MN-major
+          if (i > 0 && !W.warp(&sm.dq_free, (i - 1) & 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+          if (ptx::elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t ad = ptx::sdesc_sw128(k_addr + kk * 2048, kHalfTileBytes, 1024);
-            const uint64_t bd = ptx::sdesc_sw128(ds_addr + kk * 2048, kDsBytes, 1024);
-            ptx::mma_ss(tmem + kColDQ, ad, bd, id_dq, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t ad = ptx::sdesc_sw128(k_addr + kk * 2048, kHalfTileBytes, 1024);
+              const uint64_t bd = ptx::sdesc_sw128(ds_addr + kk * 2048, kDsBytes, 1024);
+              ptx::mma_ss(tmem + kColDQ, ad, bd, id_dq, kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(&sm.dq_full);
+            ptx::mma_commit(&sm.qdo_empty[qs]);
+            ptx::mma_commit(&sm.ds_free[st]);
           }
-          ptx::mma_commit(&sm.dq_full);
-          ptx::mma_commit(&sm.qdo_empty[qs]);
-          ptx::mma_commit(&sm.ds_free[st]);
+          __syncwarp();
         }
-        __syncwarp();
       }
       if (!ok) break;
       if (n == 0 && !W.warp(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
@@ -402,54 +438,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
     }
     (void)ok;
     __syncwarp();
-    if (ptx::elect_one()) ptx::mma_commit(&sm.drain);
+    if (ptx::elect_one()) ptx::mma_commit(&sm.drain[side]);
     __syncwarp();
-    if (lane == 0) W.drain(&sm.drain, 0);
+    if (lane == 0) W.drain(&sm.drain[side], 0);
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
     // ================================================================ compute warps
     const int qr = warp & 3, ch = warp >> 2;  // TMEM lane quarter, query-column half
-    const int t = qr * 32 + lane;              // key row (S^T, dP^T) / head-dim column (dQ^T)
+    const int t = qr * 32 + lane;              // key row of S^T / dP^T
     const uint32_t lane_base = (uint32_t)(qr * 32) << 16;
     const float c = p.scale_log2;
     const int key_half = t >= 64 ? 1 : 0;
-    const bool issuer = threadIdx.x == 0;      // issues the dQ reduce-adds
     uint32_t n_units = 0, i = 0;
-    bool ok = true;
-    // the previous step's dQ^T is read and reduced one step late
-    bool dq_pending = false;
-    int pend_h = 0, pend_q0 = 0, pend_b = 0;
-    long long pend_tok0 = 0;
-
-    // dQ^T of step j: tensor memory -> staging [query][head dim] -> TMA reduce-add
-    auto flush_dq = [&](uint32_t j, bool mine_ok) -> bool {
-      if (!group_all(mine_ok && W.warp(&sm.dq_full, j & 1))) return false;
-      ptx::tc_fence_after();
-      uint32_t vr[32];
-      ptx::tmem_ld32(tmem + lane_base + kColDQ + 32 * ch, vr);
-      ptx::tmem_ld_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&sm.dq_free);
-      if (issuer) ptx::bulk_wait_group_read<0>();  // the staging tile has been read
-      group_sync();
-#pragma unroll
-      for (int cc = 0; cc < 32; ++cc) sm.dq[(32 * ch + cc) * kHeadDim + t] = __uint_as_float(vr[cc]);
-      ptx::fence_proxy_async_smem();
-      group_sync();
-      if (issuer) {
-        // rows past the sequence end carry exact zeros (their P is 0); the map
-        // clips rows past the tensor end
-        if (a.acc_rows_inner) ptx::tma_reduce_add_4d(&a.tacc, sm.dq, 0, (int)(pend_tok0 + pend_q0), pend_h, pend_b);
-        else ptx::tma_reduce_add_4d(&a.tacc, sm.dq, 0, pend_h, (int)(pend_tok0 + pend_q0), 0);
-        ptx::bulk_commit_group();
-      }
-      return true;
-    };
-
     for (;;) {
       const int slot = n_units & 1;
-      if (!group_all(W.warp(&sm.unit_full[slot], (n_units >> 1) & 1))) { ok = false; break; }
+      if (!group_all(W.warp(&sm.unit_full[slot], (n_units >> 1) & 1))) break;
       Unit un;
       const bool valid = read_unit(sm, slot, un);
       __syncwarp();
@@ -460,10 +463,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       BwdSteps steps;
       steps.init(p, si.len, un.tile);
       int hh, qb, bits, n = 0;
+      // A warp whose wait gave up skips the rest of the unit's steps but still
+      // reaches the unit's group-wide agreement below, like every other warp.
+      bool alive = true;
       while (steps.next(hh, qb, bits)) {
         const int st = i & 1, qs = i % kStages;
         const int q0 = qb * kQB;
-        bool mine = W.warp(&sm.qdo_full[qs], (i / kStages) & 1) && W.warp(&sm.st_full[st], (i >> 1) & 1);
+        bool mine = alive && W.warp(&sm.qdo_full[qs], (i / kStages) & 1) && W.warp(&sm.st_full[st], (i >> 1) & 1);
         float pv[32];
         if (mine) {
           // P^T = exp2(S^T * scale * log2 e - LSE * log2 e) for 32 query columns
@@ -511,7 +517,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
           if (mine) {
             // dS^T = P^T o (dP^T - D), bf16, 128-byte swizzled row t of the dS^T tile
             uint8_t* dsrow = sm.ds[st] + t * 128;
-#pragma unroll
             const float2* nd2 = reinterpret_cast<const float2*>(&sm.ndlt[qs][32 * ch]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -537,24 +542,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
             if (lane == 0) ptx::mbar_arrive(&sm.ds_full[st]);
           }
         }
-        // the previous step's dQ (also agrees on this step's outcome group-wide)
-        if (dq_pending) {
-          if (!flush_dq(i - 1, mine)) { ok = false; break; }
-        } else if (!group_all(mine)) {
-          ok = false;
-          break;
-        }
-        dq_pending = true;
-        pend_h = g * p.group + hh;
-        pend_q0 = q0;
-        pend_b = si.b;
-        pend_tok0 = si.tok0;
+        alive = mine;
+        (void)hh;
         ++i;
         ++n;
       }
-      if (!ok) break;
       // unit epilogue: warps 0-3 write dK (x scale), warps 4-7 dV
-      if (!group_all(W.warp(&sm.acc_done, n_units & 1))) { ok = false; break; }
+      if (!group_all(alive && W.warp(&sm.acc_done, n_units & 1))) break;
       ptx::tc_fence_after();
       if (ch == 0) store_kv_rows(tmem + lane_base + kColDK, n > 0, p.scale, t, p, si, g, k0, p.dk);
       else store_kv_rows(tmem + lane_base + kColDV, n > 0, 1.f, t, p, si, g, k0, p.dv);
@@ -563,7 +557,60 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       if (lane == 0) ptx::mbar_arrive(&sm.acc_free);
       ++n_units;
     }
-    if (ok && dq_pending) flush_dq(i - 1, true);
+  } else if (warp >= 10 && warp < 14) {
+    // ================================================================ dQ writers
+    const int qr = warp & 3;
+    const int d = qr * 32 + lane;  // head-dim column of dQ = TMEM lane of dQ^T
+    const uint32_t lane_base = (uint32_t)(qr * 32) << 16;
+    const bool issuer = warp == 10 && lane == 0;  // issues the reduce-adds
+    uint32_t n_units = 0, i = 0;
+    bool ok = true;
+    for (;;) {
+      const int slot = n_units & 1;
+      if (!dq_all(W.warp(&sm.unit_full[slot], (n_units >> 1) & 1))) { ok = false; break; }
+      Unit un;
+      const bool valid = read_unit(sm, slot, un);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sm.unit_empty[slot]);
+      if (!valid) break;
+      const SeqInfo si = seq_info(p, un.seq);
+      BwdSteps steps;
+      steps.init(p, si.len, un.tile);
+      int hh, qb, bits;
+      while (steps.next(hh, qb, bits)) {
+        // named barriers below: the four warps agree on the wait first
+        if (!dq_all(W.warp(&sm.dq_full, i & 1))) { ok = false; break; }
+        ptx::tc_fence_after();
+        uint32_t v0[32], v1[32];
+        ptx::tmem_ld32(tmem + lane_base + kColDQ, v0);
+        ptx::tmem_ld32(tmem + lane_base + kColDQ + 32, v1);
+        ptx::tmem_ld_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.dq_free);
+        if (issuer) ptx::bulk_wait_group_read<0>();  // the previous tile has left the staging buffer
+        dq_sync();
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc) sm.dq[cc * kHeadDim + d] = __uint_as_float(v0[cc]);
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc) sm.dq[(32 + cc) * kHeadDim + d] = __uint_as_float(v1[cc]);
+        ptx::fence_proxy_async_smem();
+        dq_sync();
+        if (issuer) {
+          // rows past the sequence end carry exact zeros (their P is 0); the map
+          // clips rows past the tensor end
+          const int h = un.head * p.group + hh, q0 = qb * kQB;
+          if (a.acc_rows_inner) ptx::tma_reduce_add_4d(&a.tacc, sm.dq, 0, (int)(si.tok0 + q0), h, si.b);
+          else ptx::tma_reduce_add_4d(&a.tacc, sm.dq, 0, h, (int)(si.tok0 + q0), 0);
+          ptx::bulk_commit_group();
+        }
+        (void)bits;
+        ++i;
+      }
+      if (!ok) break;
+      ++n_units;
+    }
+    (void)ok;
     if (issuer) ptx::bulk_wait_group<0>();
   }
 
