@@ -67,6 +67,7 @@ struct Smem {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
   uint64_t s_full[2], p_full[2], o_final[2], o_free[2];
+  uint64_t turn[2];  // turn[q]: issuer q has issued its products for a key tile
   uint64_t drain[2];
   int unit_slot[2][4];  // seq, head, 256-row tile, valid
   uint32_t tmem_base;
@@ -155,6 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       ptx::mbar_init(&sm.k_empty[s], 2);  // one commit per MMA warp
       ptx::mbar_init(&sm.v_empty[s], 2);
     }
+    ptx::mbar_init(&sm.turn[0], 1);
+    ptx::mbar_init(&sm.turn[1], 1);
     ptx::mbar_init(&sm.drain[0], 1);
     ptx::mbar_init(&sm.drain[1], 1);
     sm.abort.flag = 0;
@@ -283,6 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     // Both issuers walk every key tile of the unit and commit once per K / V
     // stage (the empty barriers count two), so the ring stays in step even for
     // tiles where one query tile has no visible keys.
+    // Per key tile the two issuers take turns (tile 0's products, then tile
+    // 1's, ...): left free-running, both warpgroups drift into the same phase,
+    // their products interleave and each waits for both; taking turns keeps one
+    // warpgroup's exponentials under the other's products.
     // The whole warp runs the control flow; elect.sync on the full, converged
     // warp picks the same lane every time, so each commit covers every product
     // that lane issued before it.
@@ -292,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     const uint32_t q_addr = ptx::smem_u32(sm.q[q]);
     const uint32_t t_s = tmem + q * 128, t_o = tmem + 256 + q * 128;
     uint32_t n_units_seen = 0, n_q = 0, n_p = 0, n_o = 0, n_k = 0, n_v = 0;
+    uint32_t n_turn = 0;  // key tiles walked so far (all units)
     bool ok = true;
     for (;;) {
       const int slot = n_units_seen & 1;
@@ -357,12 +365,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         const uint32_t nst = n_k % kStages;
         if (!W.warp(&sm.v_full[cur_stage], (n_v / kStages) & 1)) { ok = false; break; }
         ++n_v;
+        // K of the next tile is waited for before P_q: it is normally there long
+        // before P_q, so the wait stays off the softmax -> products -> softmax chain.
+        if (nhave) {
+          if (!W.warp(&sm.k_full[nst], (n_k / kStages) & 1)) { ok = false; break; }
+          ++n_k;
+        }
         if ((cur_bits >> (4 * q)) & 0xF) {
           // O_q += P_q V.  Before the unit's first product, the previous unit's
           // epilogue must have read O_q.
           if (!W.warp(&sm.p_full[q], n_p & 1)) { ok = false; break; }
           ++n_p;
           if (pv_issued == 0 && !W.warp(&sm.o_free[q], (n_o & 1) ^ 1)) { ok = false; break; }
+        }
+        // this tile's turn: issuer 0 after issuer 1's previous tile, issuer 1
+        // after issuer 0's same tile
+        if (q == 0 ? (n_turn > 0 && !W.warp(&sm.turn[1], (n_turn - 1) & 1)) : !W.warp(&sm.turn[0], n_turn & 1)) {
+          ok = false;
+          break;
+        }
+        if ((cur_bits >> (4 * q)) & 0xF) {
           ptx::tc_fence_after();
           const uint32_t v_addr = ptx::smem_u32(sm.v[cur_stage]);
           const uint32_t acc0 = pv_issued > 0 ? 1u : 0u;
@@ -380,12 +402,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
           if (last) ++n_o;
         }
         // S_q of the next tile: the S_q buffer held P_q, consumed by the product above
-        if (nhave) {
-          if (!W.warp(&sm.k_full[nst], (n_k / kStages) & 1)) { ok = false; break; }
-          ++n_k;
+        if (nhave && ((nbits >> (4 * q)) & 0xF)) {
           ptx::tc_fence_after();
-          if (((nbits >> (4 * q)) & 0xF) && !issue_s(ptx::smem_u32(sm.k[nst]))) { ok = false; break; }
+          if (!issue_s(ptx::smem_u32(sm.k[nst]))) { ok = false; break; }
         }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.turn[q]);  // hand the turn to the other issuer
+        ++n_turn;
         if (ptx::elect_one()) {
           ptx::mma_commit(&sm.v_empty[cur_stage]);       // V of this tile: this warp's P V product issued
           if (nhave) ptx::mma_commit(&sm.k_empty[nst]);  // K of the next tile: this warp's S product issued
