@@ -169,8 +169,12 @@ def attn_fwd(q, k, v, *, causal=False, block_mask: BlockMask | None = None, scal
 
 
 def attn_bwd(q, k, v, o, do, lse, *, causal=False, block_mask: BlockMask | None = None, scale=None,
-             seqlens: SeqLens | None = None, seqlen: int | None = None, stream=None, workspace=None):
-    """dQ, dK, dV of the attention forward.  Returns (dq, dk, dv)."""
+             seqlens: SeqLens | None = None, seqlen: int | None = None, stream=None, workspace=None,
+             deterministic=False):
+    """dQ, dK, dV of the attention forward.  Returns (dq, dk, dv).
+
+    deterministic: bit-identical results from run to run (attn_bwd_deterministic:
+    dQ from a query-stationary pass; bf16, head_dim 128 only)."""
     lib = _lib.load()
     q, k, v, o, do = (t.contiguous() for t in (q, k, v, o, do))
     lse = lse.contiguous()
@@ -183,9 +187,10 @@ def attn_bwd(q, k, v, o, do, lse, *, causal=False, block_mask: BlockMask | None 
     dk = torch.empty_like(k)
     dv = torch.empty_like(v)
     ws = _workspace(lib.attn_bwd_workspace_size(ctypes.byref(p)), q.device, workspace)
-    check(lib.attn_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
-                       _ptr(dk), _ptr(dv), _ptr(ws), ctypes.c_size_t(0 if ws is None else ws.numel()),
-                       _stream_handle(stream)), "attn_bwd")
+    name = "attn_bwd_deterministic" if deterministic else "attn_bwd"
+    check(getattr(lib, name)(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                             _ptr(dk), _ptr(dv), _ptr(ws), ctypes.c_size_t(0 if ws is None else ws.numel()),
+                             _stream_handle(stream)), name)
     return dq, dk, dv
 
 

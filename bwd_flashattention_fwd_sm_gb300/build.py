@@ -22,7 +22,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgbattn.so")
 
-SOURCES = ["api.cu", "sched.cu", "bwd_aux.cu", "simt_attn.cu", "tma_host.cu", "tc_fwd.cu", "tc_bwd.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "sched.cu", "bwd_aux.cu", "simt_attn.cu", "tma_host.cu", "tc_fwd.cu", "tc_bwd.cu", "tc_dq.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", CSRC, "-I", INCLUDE]

@@ -187,6 +187,10 @@ struct Layout {
   int tile_rows;       // rows per work unit (query rows fwd, key rows bwd)
   long long n_units;
   size_t counter, units, sched, csc_ptr, csc_idx, dq_acc, delta, total;
+  // backward on the tensor cores: the query-stationary dQ pass's work list
+  // (forward-style units of 256 query rows), used by the deterministic mode
+  long long q_units;
+  size_t q_counter, q_list, q_sched;
 };
 
 KParams base_kparams(const attn_params_t* p, const Problem& pr) {
@@ -249,6 +253,15 @@ Layout layout_for(const attn_params_t* p, const Problem& pr, bool backward) {
     off = align_up(off + sizeof(float) * rows * (size_t)p->head_dim, 256);
     L.delta = off;
     off = align_up(off + sizeof(float) * rows, 256);
+    if (use_tensor_cores(p, true)) {
+      L.q_units = count_units(k, p->cu_seqlens_host, false, 256);
+      L.q_counter = off;
+      off = align_up(off + sizeof(int), 256);
+      L.q_list = off;
+      off = align_up(off + sizeof(Unit) * (size_t)L.q_units, 256);
+      L.q_sched = off;
+      off = align_up(off + sizeof(int) * align_up((size_t)pr.n_seqs + 1, 4) + sizeof(Unit) * (size_t)L.q_units, 256);
+    }
   }
   L.total = off;
   return L;
@@ -337,12 +350,23 @@ attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, con
   return ATTN_OK;
 }
 
-attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, const void* v,
-                       const void* o, const void* dout, const float* lse, void* dq, void* dk, void* dv,
-                       void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The backward pass.  deterministic: dK and dV from the dK/dV-stationary pass
+// without its dQ product, then dQ from the query-stationary pass (fixed sum
+// order, no accumulator); otherwise dQ is added into the float32 accumulator
+// by L2 reductions and converted at the end.
+attn_status_t bwd_impl(const attn_params_t* p, const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                       size_t workspace_bytes, void* stream, bool deterministic) {
   Problem pr;
   attn_status_t s = validate_params(p, &pr);
   if (s != ATTN_OK) return s;
+  if (deterministic && !use_tensor_cores(p, true))
+    return fail(ATTN_ERR_UNSUPPORTED,
+                "the deterministic backward runs on the tensor-core path only (bf16, head_dim 128)");
   if (pr.empty) return ATTN_OK;
   if ((s = check_ptr(q, "q")) || (s = check_ptr(k, "k")) || (s = check_ptr(v, "v")) ||
       (s = check_ptr(o, "o")) || (s = check_ptr(dout, "dout")) || (s = check_ptr(lse, "lse")) ||
@@ -369,7 +393,7 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, con
   kp.dk = dk;
   kp.dv = dv;
   kp.status = status;
-  kp.dq_accum = reinterpret_cast<float*>(ws + L.dq_acc);
+  kp.dq_accum = deterministic ? nullptr : reinterpret_cast<float*>(ws + L.dq_acc);
   kp.delta = reinterpret_cast<float*>(ws + L.delta);
   kp.units = reinterpret_cast<const Unit*>(ws + L.units);
   kp.n_units = (int)L.n_units;
@@ -385,18 +409,46 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, con
   e = launch_build_worklist(kp, true, L.tile_rows, reinterpret_cast<Unit*>(ws + L.units), (int)L.n_units,
                             reinterpret_cast<int*>(ws + L.sched), st);
   if (e != cudaSuccess) return cuda_fail(e, "work-list launch");
+  KParams kq = kp;  // the dQ pass: forward-style work list
+  if (deterministic) {
+    kq.units = reinterpret_cast<const Unit*>(ws + L.q_list);
+    kq.n_units = (int)L.q_units;
+    kq.unit_counter = reinterpret_cast<int*>(ws + L.q_counter);
+    e = launch_build_worklist(kq, false, 256, reinterpret_cast<Unit*>(ws + L.q_list), (int)L.q_units,
+                              reinterpret_cast<int*>(ws + L.q_sched), st);
+    if (e != cudaSuccess) return cuda_fail(e, "work-list launch");
+  }
   e = launch_bwd_preprocess(kp, bf16, st);
   if (e != cudaSuccess) return cuda_fail(e, "preprocess launch");
   if (g_timing_events[1][0] && (e = cudaEventRecord(g_timing_events[1][0], st)) != cudaSuccess)
     return cuda_fail(e, "timing event");
-  if (use_tensor_cores(p, true)) e = launch_tc_bwd(kp, sms, st);
+  if (use_tensor_cores(p, true)) e = launch_tc_bwd(kp, sms, st, !deterministic);
   else e = launch_simt_bwd(kp, bf16, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  if (deterministic && (e = launch_tc_dq(kq, sms, st)) != cudaSuccess) return cuda_fail(e, "dQ pass launch");
   if (g_timing_events[1][1] && (e = cudaEventRecord(g_timing_events[1][1], st)) != cudaSuccess)
     return cuda_fail(e, "timing event");
-  e = launch_dq_convert(kp, bf16, st);
-  if (e != cudaSuccess) return cuda_fail(e, "dQ conversion launch");
+  if (!deterministic) {
+    e = launch_dq_convert(kp, bf16, st);
+    if (e != cudaSuccess) return cuda_fail(e, "dQ conversion launch");
+  }
   return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, const void* v,
+                       const void* o, const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(p, q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, stream, false);
+}
+
+attn_status_t attn_bwd_deterministic(const attn_params_t* p, const void* q, const void* k, const void* v,
+                                     const void* o, const void* dout, const float* lse, void* dq, void* dk,
+                                     void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(p, q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, stream, true);
 }
 
 attn_status_t attn_get_status(void* stream) {

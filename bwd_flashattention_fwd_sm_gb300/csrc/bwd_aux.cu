@@ -98,10 +98,12 @@ __global__ void __launch_bounds__(256) k_bwd_preprocess(KParams p, long long n_r
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (lane == 0) p.delta[x.lse] = s;
-    float z[N];
+    if (p.dq_accum) {  // no accumulator in the deterministic (query-stationary dQ) mode
+      float z[N];
 #pragma unroll
-    for (int i = 0; i < N; ++i) z[i] = 0.f;
-    store_vec<float, N>(p.dq_accum + x.acc + lane * N, z);
+      for (int i = 0; i < N; ++i) z[i] = 0.f;
+      store_vec<float, N>(p.dq_accum + x.acc + lane * N, z);
+    }
   }
 }
 

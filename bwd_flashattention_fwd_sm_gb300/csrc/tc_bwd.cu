@@ -43,6 +43,8 @@
 // memory and returns.
 #include <cuda.h>
 
+#include <cstring>
+
 #include "tc_common.cuh"
 #include "tc_kernels.h"
 #include "tma_host.h"
@@ -172,6 +174,8 @@ __device__ __forceinline__ void store_kv_rows(uint32_t taddr_row, bool have, flo
   }
 }
 
+// kDq false: dK and dV only (dQ comes from the query-stationary pass).
+template <bool kDq>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -410,16 +414,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
           __syncwarp();
           // dQ_i^T = K^T dS^T_i: A = K^T (head dim contiguous: MN-major), B = dS^T as
           // (query, key) with query contiguous: MN-major
-          if (i > 0 && !W.warp(&sm.dq_free, (i - 1) & 1)) { ok = false; break; }
+          if (kDq && i > 0 && !W.warp(&sm.dq_free, (i - 1) & 1)) { ok = false; break; }
           ptx::tc_fence_after();
           if (ptx::elect_one()) {
+            if constexpr (kDq) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t ad = ptx::sdesc_sw128(k_addr + kk * 2048, kHalfTileBytes, 1024);
-              const uint64_t bd = ptx::sdesc_sw128(ds_addr + kk * 2048, kDsBytes, 1024);
-              ptx::mma_ss(tmem + kColDQ, ad, bd, id_dq, kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t ad = ptx::sdesc_sw128(k_addr + kk * 2048, kHalfTileBytes, 1024);
+                const uint64_t bd = ptx::sdesc_sw128(ds_addr + kk * 2048, kDsBytes, 1024);
+                ptx::mma_ss(tmem + kColDQ, ad, bd, id_dq, kk > 0 ? 1u : 0u);
+              }
+              ptx::mma_commit(&sm.dq_full);
             }
-            ptx::mma_commit(&sm.dq_full);
             ptx::mma_commit(&sm.qdo_empty[qs]);
             ptx::mma_commit(&sm.ds_free[st]);
           }
@@ -577,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       BwdSteps steps;
       steps.init(p, si.len, un.tile);
       int hh, qb, bits;
-      while (steps.next(hh, qb, bits)) {
+      while (kDq && steps.next(hh, qb, bits)) {
         // named barriers below: the four warps agree on the wait first
         if (!dq_all(W.warp(&sm.dq_full, i & 1))) { ok = false; break; }
         ptx::tc_fence_after();
@@ -626,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
 
 bool tc_bwd_available() { return true; }
 
-cudaError_t launch_tc_bwd(const KParams& p, int sms, cudaStream_t st) {
+cudaError_t launch_tc_bwd(const KParams& p, int sms, cudaStream_t st, bool with_dq) {
   if (p.n_units == 0) return cudaSuccess;
   BwdArgs a;
   TileMap mq, mk, mv, mdo, macc;
@@ -635,7 +641,8 @@ cudaError_t launch_tc_bwd(const KParams& p, int sms, cudaStream_t st) {
   if ((e = make_tile_map(&mdo, p.dout, p, false, kQB)) != cudaSuccess) return e;
   if ((e = make_tile_map(&mk, p.k, p, true)) != cudaSuccess) return e;
   if ((e = make_tile_map(&mv, p.v, p, true)) != cudaSuccess) return e;
-  if ((e = make_acc_map(&macc, p.dq_accum, p, kQB)) != cudaSuccess) return e;
+  if (with_dq && (e = make_acc_map(&macc, p.dq_accum, p, kQB)) != cudaSuccess) return e;
+  if (!with_dq) std::memset(&macc, 0, sizeof(macc));
   a.tq = mq.map;
   a.tdo = mdo.map;
   a.tk = mk.map;
@@ -646,10 +653,11 @@ cudaError_t launch_tc_bwd(const KParams& p, int sms, cudaStream_t st) {
   a.acc_rows_inner = macc.rows_inner;
   a.p = p;
   const size_t smem = sizeof(Smem) + 1024;
-  e = cudaFuncSetAttribute(k_tc_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kernel = with_dq ? k_tc_bwd<true> : k_tc_bwd<false>;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = p.n_units < sms ? p.n_units : sms;
-  k_tc_bwd<<<grid, kThreads, smem, st>>>(a);
+  kernel<<<grid, kThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -10,9 +10,14 @@ bool tc_fwd_available();
 bool tc_bwd_available();
 
 // bf16, head_dim 128.  Persistent kernels: one CTA per SM takes units from
-// p.unit_counter over the cost-ordered work list p.units (forward: 256 query
-// rows per unit; backward: 128 keys per unit).
+// p.unit_counter over the cost-ordered work list p.units (forward and dQ pass:
+// 256 query rows per unit; backward: 128 keys per unit).
 cudaError_t launch_tc_fwd(const KParams& p, int sms, cudaStream_t st);
-cudaError_t launch_tc_bwd(const KParams& p, int sms, cudaStream_t st);
+// with_dq: also add dQ into p.dq_accum (L2 reductions, order not fixed);
+// otherwise dK and dV only.
+cudaError_t launch_tc_bwd(const KParams& p, int sms, cudaStream_t st, bool with_dq);
+// Query-stationary dQ (fixed summation order) straight to p.dq as bf16; needs
+// p.delta from the preprocess and the forward's work list.
+cudaError_t launch_tc_dq(const KParams& p, int sms, cudaStream_t st);
 
 }  // namespace gbattn

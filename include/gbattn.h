@@ -144,12 +144,31 @@ attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, con
  * two gradients gather along the key direction and the third is accumulated by
  * many blocks into the same place).  dk and dv are sums over the query heads of
  * each KV head's group.  dq, dk, dv: outputs with the q / kv layouts; workspace
- * as for attn_fwd with attn_bwd_workspace_size bytes.  dQ is accumulated with
- * float32 atomics, so its last bits may differ from run to run.
+ * as for attn_fwd with attn_bwd_workspace_size bytes.  dQ is accumulated in
+ * float32 by L2 reductions whose order is not fixed, so its last bits may
+ * differ from run to run (see attn_bwd_deterministic).
  */
 attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, const void* v,
                        const void* o, const void* dout, const float* lse, void* dq, void* dk,
                        void* dv, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Deterministic backward: the same outputs as attn_bwd, bit-identical from run
+ * to run.  The pages point at both causes and the cure: the dQ sum's order
+ * varies with the order in which blocks add into it (zwxr.cn CANN article,
+ * section 6.1), and the backward can walk the blocks in the other loop order
+ * (smzdm contest article, section 03).  Here dK and dV come from the
+ * dK/dV-stationary pass without its dQ product, and dQ from a second,
+ * query-stationary pass that recomputes S and dP per query tile and sums over
+ * key tiles in ascending order (three products per tile instead of one, so
+ * the backward does 7 products instead of 5).  Arguments, layouts and the
+ * workspace (attn_bwd_workspace_size bytes) are those of attn_bwd.  Only the
+ * tensor-core path (bf16, head_dim 128) has it: other types return
+ * ATTN_ERR_UNSUPPORTED before queuing anything.
+ */
+attn_status_t attn_bwd_deterministic(const attn_params_t* p, const void* q, const void* k, const void* v,
+                                     const void* o, const void* dout, const float* lse, void* dq, void* dk,
+                                     void* dv, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Backward pass that allocates nothing.  The pages have no counterpart to this

@@ -56,8 +56,10 @@ def compare(name, got, ref, dtype):
     return max_abs, rel
 
 
-def gpu_run(wl: W.Workload, inputs: dict, passes="fwd+bwd"):
-    """Run the CUDA path on `inputs` (CPU tensors); returns CPU float64 numpy results."""
+def gpu_run(wl: W.Workload, inputs: dict, passes="fwd+bwd", deterministic=False):
+    """Run the CUDA path on `inputs` (CPU tensors); returns CPU float64 numpy results.
+
+    deterministic: the backward through attn_bwd_deterministic."""
     dev = torch.device("cuda")
     q, k, v, do = (inputs[n].to(dev) for n in ("q", "k", "v", "do"))
     kw = {"scale": wl.scale}
@@ -71,7 +73,7 @@ def gpu_run(wl: W.Workload, inputs: dict, passes="fwd+bwd"):
     o, lse = attn_fwd(q, k, v, **kw)
     out = {"o": o, "lse": lse}
     if "bwd" in passes:
-        dq, dk, dv = attn_bwd(q, k, v, o, do, lse, **kw)
+        dq, dk, dv = attn_bwd(q, k, v, o, do, lse, deterministic=deterministic, **kw)
         out.update(dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
     assert get_status() == 0, "device status word set"

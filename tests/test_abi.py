@@ -189,3 +189,16 @@ def test_fp32_head_dim_64_accepted(lib):
     p.q_stride_b, p.q_stride_h, p.q_stride_s = 4 * 256 * 64, 256 * 64, 64
     p.kv_stride_b, p.kv_stride_h, p.kv_stride_s = 2 * 256 * 64, 256 * 64, 64
     assert fwd(lib, p) == _lib.ATTN_ERR_CUDA
+
+
+def test_deterministic_backward_dispatch(lib):
+    """attn_bwd_deterministic: float32 I/O is refused before anything is queued;
+    a valid bf16 call without a GPU fails with the CUDA error like attn_bwd."""
+    p = params(D=64, dtype=_lib.ATTN_F32)
+    p.q_stride_b, p.q_stride_h, p.q_stride_s = 4 * 256 * 64, 256 * 64, 64
+    p.kv_stride_b, p.kv_stride_h, p.kv_stride_s = 2 * 256 * 64, 256 * 64, 64
+    det = lambda q: lib.attn_bwd_deterministic(ctypes.byref(q), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                               FAKE, FAKE, 1 << 40, None)
+    assert det(p) == _lib.ATTN_ERR_UNSUPPORTED
+    assert b"deterministic" in lib.attn_last_error()
+    assert det(params()) == _lib.ATTN_ERR_CUDA
