@@ -174,7 +174,7 @@ def attn_bwd(q, k, v, o, do, lse, *, causal=False, block_mask: BlockMask | None 
     """dQ, dK, dV of the attention forward.  Returns (dq, dk, dv).
 
     deterministic: bit-identical results from run to run (attn_bwd_deterministic:
-    dQ from a query-stationary pass; bf16, head_dim 128 only)."""
+    dQ from a query-stationary pass; bf16 only)."""
     lib = _lib.load()
     q, k, v, o, do = (t.contiguous() for t in (q, k, v, o, do))
     lse = lse.contiguous()

@@ -80,10 +80,10 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 // Which kernel family serves these parameters: the tensor-core kernels for bf16
-// with head_dim 128, the float32-arithmetic kernels for float32 I/O.
+// with head_dim 64 or 128, the float32-arithmetic kernels for float32 I/O.
 bool use_tensor_cores(const attn_params_t* p, bool backward) {
   const bool avail = backward ? tc_bwd_available() : tc_fwd_available();
-  return avail && p->dtype == ATTN_BF16 && p->head_dim == 128;
+  return avail && p->dtype == ATTN_BF16 && (p->head_dim == 128 || p->head_dim == 64);
 }
 
 struct Problem {
@@ -107,8 +107,6 @@ attn_status_t validate_params(const attn_params_t* p, Problem* pr) {
     return fail(ATTN_ERR_INVALID_ARG, "heads_q=%d is not a multiple of heads_kv=%d", p->heads_q, p->heads_kv);
   if (p->head_dim != 64 && p->head_dim != 128)
     return fail(ATTN_ERR_UNSUPPORTED, "head_dim=%d: only 64 and 128 are implemented", p->head_dim);
-  if (p->dtype == ATTN_BF16 && p->head_dim != 128)
-    return fail(ATTN_ERR_UNSUPPORTED, "bf16 with head_dim=%d: only head_dim 128 is implemented", p->head_dim);
   if (!std::isfinite(p->scale)) return fail(ATTN_ERR_INVALID_ARG, "scale is not finite");
   if (p->seqlen < 0) return fail(ATTN_ERR_INVALID_ARG, "seqlen=%d is negative", p->seqlen);
   if (p->seqlen > (1 << 30)) return fail(ATTN_ERR_UNSUPPORTED, "seqlen=%d exceeds 2^30", p->seqlen);
@@ -366,7 +364,7 @@ attn_status_t bwd_impl(const attn_params_t* p, const void* q, const void* k, con
   if (s != ATTN_OK) return s;
   if (deterministic && !use_tensor_cores(p, true))
     return fail(ATTN_ERR_UNSUPPORTED,
-                "the deterministic backward runs on the tensor-core path only (bf16, head_dim 128)");
+                "the deterministic backward runs on the tensor-core path only (bf16, head_dim 64 or 128)");
   if (pr.empty) return ATTN_OK;
   if ((s = check_ptr(q, "q")) || (s = check_ptr(k, "k")) || (s = check_ptr(v, "v")) ||
       (s = check_ptr(o, "o")) || (s = check_ptr(dout, "dout")) || (s = check_ptr(lse, "lse")) ||

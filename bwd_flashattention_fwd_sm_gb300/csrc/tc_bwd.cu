@@ -144,14 +144,15 @@ __device__ __forceinline__ bool dq_all(bool pred) {
 }
 __device__ __forceinline__ void dq_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
-// One warp writes its 32 key rows of a 128-column accumulator (x scale, bf16)
+// One warp writes its 32 key rows of a D-column accumulator (x scale, bf16)
 // straight from tensor memory to global memory rows k0 + row < len of head g.
+template <int D>
 __device__ __forceinline__ void store_kv_rows(uint32_t taddr_row, bool have, float scale, int row,
                                               const KParams& p, const SeqInfo& si, int g, int k0, void* out) {
   const bool ok = k0 + row < si.len;
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + (ok ? kv_off(p, si, g, k0 + row) : 0);
 #pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
+  for (int cc = 0; cc < D / 32; ++cc) {
     uint32_t v[32];
     if (have) {
       ptx::tmem_ld32(taddr_row + cc * 32, v);
@@ -175,7 +176,10 @@ __device__ __forceinline__ void store_kv_rows(uint32_t taddr_row, bool have, flo
 }
 
 // kDq false: dK and dV only (dQ comes from the query-stationary pass).
-template <bool kDq>
+// D: head dim, 64 or 128 (shared memory is laid out for 128 either way).  With
+// D = 64 the dQ^T product still runs with M = 128: the upper half of the K tile
+// buffer holds zeros, so head-dim rows 64-127 of dQ^T are zero and unused.
+template <bool kDq, int D>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -213,6 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
     ptx::tmem_alloc(&sm.tmem_base, kTmemCols);
     ptx::tmem_relinquish();
   }
+  if constexpr (D == 64) {  // zero upper half of the K buffer (the A operand of dQ^T reads it)
+    for (int i = threadIdx.x; i < (int)(kHalfTileBytes / 16); i += blockDim.x)
+      reinterpret_cast<uint4*>(sm.k + kHalfTileBytes)[i] = make_uint4(0u, 0u, 0u, 0u);
+    ptx::fence_proxy_async_smem();
+  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -248,9 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       // K and V of the unit, once the previous unit's products are done with them
       if (!W.warp(&sm.kv_empty, (n_units & 1) ^ 1)) break;
       if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(&sm.kv_full, 2 * kTileBytes);
-        tma_tile(sm.k, &a.tk, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b, kHalfTileBytes);
-        tma_tile(sm.v, &a.tv, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b, kHalfTileBytes);
+        ptx::mbar_arrive_expect_tx(&sm.kv_full, 2 * tile_bytes<D>());
+        tma_tile(sm.k, &a.tk, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b, kHalfTileBytes, D / 64);
+        tma_tile(sm.v, &a.tv, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b, kHalfTileBytes, D / 64);
       }
       kv_loaded = true;
       last_kv_phase = n_units & 1;
@@ -265,9 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
         if (!W.warp(&sm.qdo_empty[st], ph ^ 1)) { ok = false; break; }
         const int h = g * p.group + hh, q0 = qb * kQB;
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&sm.qdo_full[st], 2 * kQTileBytes);
-          tma_tile(sm.q[st], &a.tq, a.q_rows_inner, &sm.qdo_full[st], map_row(si, q0), h, si.b, kQBoxBytes);
-          tma_tile(sm.dO[st], &a.tdo, a.q_rows_inner, &sm.qdo_full[st], map_row(si, q0), h, si.b, kQBoxBytes);
+          ptx::mbar_arrive_expect_tx(&sm.qdo_full[st], 2 * kQBoxBytes * (D / 64));
+          tma_tile(sm.q[st], &a.tq, a.q_rows_inner, &sm.qdo_full[st], map_row(si, q0), h, si.b, kQBoxBytes, D / 64);
+          tma_tile(sm.dO[st], &a.tdo, a.q_rows_inner, &sm.qdo_full[st], map_row(si, q0), h, si.b, kQBoxBytes,
+                   D / 64);
         }
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
@@ -305,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
     // unit's accumulators) count one commit from each.
     const int side = warp == 9 ? 0 : 1;  // 0: S^T, dP^T, dV   1: dK, dQ^T
     constexpr uint32_t id_st = ptx::idesc_bf16(128, 64, false, false);   // S^T, dP^T
-    constexpr uint32_t id_acc = ptx::idesc_bf16(128, 128, false, true);  // dV, dK
+    constexpr uint32_t id_acc = ptx::idesc_bf16(128, D, false, true);    // dV, dK
     constexpr uint32_t id_dq = ptx::idesc_bf16(128, 64, true, true);     // dQ^T
     const uint32_t k_addr = ptx::smem_u32(sm.k), v_addr = ptx::smem_u32(sm.v);
     uint32_t n_units = 0, gi = 0;  // gi: global step counter (all units)
@@ -318,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       const uint32_t q_addr = ptx::smem_u32(sm.q[qs]);
       if (ptx::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ad = ptx::sdesc_sw128(k_addr + (kk >> 2) * kHalfTileBytes + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = ptx::sdesc_sw128(q_addr + (kk >> 2) * kQBoxBytes + (kk & 3) * 32, 16, 1024);
           ptx::mma_ss(tmem + kColS + st * 64, ad, bd, id_st, kk > 0 ? 1u : 0u);
@@ -335,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       const uint32_t do_addr = ptx::smem_u32(sm.dO[qs]);
       if (ptx::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ad = ptx::sdesc_sw128(v_addr + (kk >> 2) * kHalfTileBytes + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = ptx::sdesc_sw128(do_addr + (kk >> 2) * kQBoxBytes + (kk & 3) * 32, 16, 1024);
           ptx::mma_ss(tmem + kColDP, ad, bd, id_st, kk > 0 ? 1u : 0u);
@@ -556,8 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       // unit epilogue: warps 0-3 write dK (x scale), warps 4-7 dV
       if (!group_all(alive && W.warp(&sm.acc_done, n_units & 1))) break;
       ptx::tc_fence_after();
-      if (ch == 0) store_kv_rows(tmem + lane_base + kColDK, n > 0, p.scale, t, p, si, g, k0, p.dk);
-      else store_kv_rows(tmem + lane_base + kColDV, n > 0, 1.f, t, p, si, g, k0, p.dv);
+      if (ch == 0) store_kv_rows<D>(tmem + lane_base + kColDK, n > 0, p.scale, t, p, si, g, k0, p.dk);
+      else store_kv_rows<D>(tmem + lane_base + kColDV, n > 0, 1.f, t, p, si, g, k0, p.dv);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&sm.acc_free);
@@ -596,10 +606,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
         if (lane == 0) ptx::mbar_arrive(&sm.dq_free);
         if (issuer) ptx::bulk_wait_group_read<0>();  // the previous tile has left the staging buffer
         dq_sync();
+        if (D == 128 || qr * 32 < D) {  // head-dim rows past D hold zeros (see above)
 #pragma unroll
-        for (int cc = 0; cc < 32; ++cc) sm.dq[cc * kHeadDim + d] = __uint_as_float(v0[cc]);
+          for (int cc = 0; cc < 32; ++cc) sm.dq[cc * D + d] = __uint_as_float(v0[cc]);
 #pragma unroll
-        for (int cc = 0; cc < 32; ++cc) sm.dq[(32 + cc) * kHeadDim + d] = __uint_as_float(v1[cc]);
+          for (int cc = 0; cc < 32; ++cc) sm.dq[(32 + cc) * D + d] = __uint_as_float(v1[cc]);
+        }
         ptx::fence_proxy_async_smem();
         dq_sync();
         if (issuer) {
@@ -653,7 +665,8 @@ cudaError_t launch_tc_bwd(const KParams& p, int sms, cudaStream_t st, bool with_
   a.acc_rows_inner = macc.rows_inner;
   a.p = p;
   const size_t smem = sizeof(Smem) + 1024;
-  auto kernel = with_dq ? k_tc_bwd<true> : k_tc_bwd<false>;
+  auto kernel = p.head_dim == 64 ? (with_dq ? k_tc_bwd<true, 64> : k_tc_bwd<false, 64>)
+                                 : (with_dq ? k_tc_bwd<true, 128> : k_tc_bwd<false, 128>);
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = p.n_units < sms ? p.n_units : sms;

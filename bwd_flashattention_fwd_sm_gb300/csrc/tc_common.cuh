@@ -11,13 +11,18 @@ constexpr int kTile = 128;                       // rows of a Q tile / keys of a
 constexpr int kHeadDim = 128;
 constexpr uint32_t kTileBytes = kTile * kHeadDim * 2;  // bf16 128 x 128 = 32 KiB
 constexpr uint32_t kHalfTileBytes = kTileBytes / 2;    // one 128 x 64 box (128-byte rows)
+// bf16 bytes of a 128-row tile of head dim D (64: one box, 128: two boxes)
+template <int D>
+constexpr uint32_t tile_bytes() { return (uint32_t)kTile * D * 2; }
 
-// Loads rows [row, row + rows) x all 128 columns of one head as two 64-column
-// boxes (each rows x 128 bytes, 128-byte swizzled) at dst and dst + box_bytes.
+// Loads rows [row, row + rows) x all nbox * 64 columns of one head as nbox
+// 64-column boxes (each rows x 128 bytes, 128-byte swizzled) at dst,
+// dst + box_bytes, ...
 __device__ __forceinline__ void tma_tile(void* dst, const CUtensorMap* map, int rows_inner, uint64_t* bar,
-                                         int row, int head, int b, uint32_t box_bytes) {
+                                         int row, int head, int b, uint32_t box_bytes, int nbox = 2) {
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
+    if (c >= nbox) break;
     void* d = static_cast<char*>(dst) + c * box_bytes;
     if (rows_inner) ptx::tma_load_4d(d, map, bar, c * 64, row, head, b);
     else ptx::tma_load_4d(d, map, bar, c * 64, head, row, b);

@@ -101,7 +101,8 @@ __device__ __forceinline__ int count_active(const KParams& p, int len, int q0_un
   return n;
 }
 
-template <bool kSparse>
+// D: head dim, 64 or 128 (shared memory is laid out for 128 either way).
+template <bool kSparse, int D>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ DqArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -172,9 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
         if (q0 >= si.len || count_active<kSparse>(p, si.len, q0u, q) == 0) continue;
         if (!W.warp(&sm.qd_empty, (n_qd & 1) ^ 1)) { ok = false; break; }
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&sm.qd_full, 2 * kTileBytes);
-          tma_tile(sm.q, &a.tq, a.q_rows_inner, &sm.qd_full, map_row(si, q0), h, si.b, kHalfTileBytes);
-          tma_tile(sm.dO, &a.tdo, a.q_rows_inner, &sm.qd_full, map_row(si, q0), h, si.b, kHalfTileBytes);
+          ptx::mbar_arrive_expect_tx(&sm.qd_full, 2 * tile_bytes<D>());
+          tma_tile(sm.q, &a.tq, a.q_rows_inner, &sm.qd_full, map_row(si, q0), h, si.b, kHalfTileBytes, D / 64);
+          tma_tile(sm.dO, &a.tdo, a.q_rows_inner, &sm.qd_full, map_row(si, q0), h, si.b, kHalfTileBytes, D / 64);
         }
         last_qd_phase = (int)(n_qd & 1);
         ++n_qd;
@@ -187,12 +188,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
           const uint32_t ph = (n_kv / kStages) & 1;
           if (!W.warp(&sm.k_empty[st], ph ^ 1) || !W.warp(&sm.v_empty[st], ph ^ 1)) { ok = false; break; }
           if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+            ptx::mbar_arrive_expect_tx(&sm.k_full[st], tile_bytes<D>());
             tma_tile(sm.k[st], &a.tk, a.kv_rows_inner, &sm.k_full[st], map_row(si, kt * kTile), g, si.b,
-                     kHalfTileBytes);
-            ptx::mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+                     kHalfTileBytes, D / 64);
+            ptx::mbar_arrive_expect_tx(&sm.v_full[st], tile_bytes<D>());
             tma_tile(sm.v[st], &a.tv, a.kv_rows_inner, &sm.v_full[st], map_row(si, kt * kTile), g, si.b,
-                     kHalfTileBytes);
+                     kHalfTileBytes, D / 64);
           }
           last_kv_phase[st] = (int)ph;
           ++n_kv;
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
     // warp picks the same lane every time, so each commit covers every product
     // that lane issued before it.
     constexpr uint32_t idesc_ss = ptx::idesc_bf16(128, 128, false, false);  // S, dP
-    constexpr uint32_t idesc_dq = ptx::idesc_bf16(128, 128, false, true);   // dQ: B = K MN-major
+    constexpr uint32_t idesc_dq = ptx::idesc_bf16(128, D, false, true);     // dQ: B = K MN-major
     const uint32_t q_addr = ptx::smem_u32(sm.q), do_addr = ptx::smem_u32(sm.dO);
     uint32_t n_units = 0, n_qd = 0, n_kv = 0, n_sdp = 0, n_ds = 0, n_tiles = 0;
     bool ok = true;
@@ -277,13 +278,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
           const uint32_t k_addr = ptx::smem_u32(sm.k[st]), v_addr = ptx::smem_u32(sm.v[st]);
           if (ptx::elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+            for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
               ptx::mma_ss(tmem + kColS, ptx::sdesc_sw128(q_addr + off, 16, 1024),
                           ptx::sdesc_sw128(k_addr + off, 16, 1024), idesc_ss, kk > 0 ? 1u : 0u);
             }
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+            for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
               ptx::mma_ss(tmem + kColDP, ptx::sdesc_sw128(do_addr + off, 16, 1024),
                           ptx::sdesc_sw128(v_addr + off, 16, 1024), idesc_ss, kk > 0 ? 1u : 0u);
@@ -343,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
         if (n_act == 0) {  // no visible key: dQ rows are zero
           if (row_ok) {
 #pragma unroll
-            for (int w = 0; w < 16; ++w) *reinterpret_cast<uint4*>(drow + w * 8) = make_uint4(0u, 0u, 0u, 0u);
+            for (int w = 0; w < D / 8; ++w) *reinterpret_cast<uint4*>(drow + w * 8) = make_uint4(0u, 0u, 0u, 0u);
           }
           continue;
         }
@@ -415,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
         ++n_tiles;
         ptx::tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t v[32];
           ptx::tmem_ld32(tmem + lane_base + kColDQ + cc * 32, v);
           ptx::tmem_ld_wait();
@@ -468,7 +469,8 @@ cudaError_t launch_tc_dq(const KParams& p, int sms, cudaStream_t st) {
   a.p = p;
   const size_t smem = sizeof(Smem) + 1024;
   const int grid = p.n_units < sms ? p.n_units : sms;
-  auto kernel = p.mask == kMaskBlock ? k_tc_dq<true> : k_tc_dq<false>;
+  auto kernel = p.head_dim == 64 ? (p.mask == kMaskBlock ? k_tc_dq<true, 64> : k_tc_dq<false, 64>)
+                                 : (p.mask == kMaskBlock ? k_tc_dq<true, 128> : k_tc_dq<false, 128>);
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kernel<<<grid, kThreads, smem, st>>>(a);

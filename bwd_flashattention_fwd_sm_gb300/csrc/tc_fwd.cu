@@ -131,7 +131,8 @@ __device__ __forceinline__ float write_p(const uint32_t (&sr)[128], float c, flo
   return (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
 }
 
-template <bool kSparse>
+// D: head dim, 64 or 128 (shared memory is laid out for 128 either way).
+template <bool kSparse, int D>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -216,9 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         const uint32_t c = n_q_loads[q];
         if (!W.warp(&sm.q_empty[q], ((c & 1) ^ 1))) { ok = false; break; }
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&sm.q_full[q], kTileBytes);
+          ptx::mbar_arrive_expect_tx(&sm.q_full[q], tile_bytes<D>());
           tma_tile(sm.q[q], &a.tq, a.q_rows_inner, &sm.q_full[q], map_row(si, q0 + q * kTile), h, si.b,
-                   kHalfTileBytes);
+                   kHalfTileBytes, D / 64);
         }
         last_q_phase[q] = c & 1;
         ++n_q_loads[q];
@@ -232,9 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         const uint32_t ph = (n_k / kStages) & 1;
         if (!W.warp(&sm.k_empty[st], ph ^ 1)) return false;
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
+          ptx::mbar_arrive_expect_tx(&sm.k_full[st], tile_bytes<D>());
           tma_tile(sm.k[st], &a.tk, a.kv_rows_inner, &sm.k_full[st], map_row(si, kt_ * kTile), g, si.b,
-                   kHalfTileBytes);
+                   kHalfTileBytes, D / 64);
         }
         last_k_phase[st] = (int)ph;
         ++n_k;
@@ -245,9 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         const uint32_t ph = (n_v / kStages) & 1;
         if (!W.warp(&sm.v_empty[st], ph ^ 1)) return false;
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
+          ptx::mbar_arrive_expect_tx(&sm.v_full[st], tile_bytes<D>());
           tma_tile(sm.v[st], &a.tv, a.kv_rows_inner, &sm.v_full[st], map_row(si, kt_ * kTile), g, si.b,
-                   kHalfTileBytes);
+                   kHalfTileBytes, D / 64);
         }
         last_v_phase[st] = (int)ph;
         ++n_v;
@@ -295,9 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     // that lane issued before it.
     const int q = warp - 9;
     constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, false, false);
-    constexpr uint32_t idesc_pv = ptx::idesc_bf16(128, 128, false, true);
+    constexpr uint32_t idesc_pv = ptx::idesc_bf16(128, D, false, true);
     const uint32_t q_addr = ptx::smem_u32(sm.q[q]);
-    const uint32_t t_s = tmem + q * 128, t_o = tmem + 256 + q * 128;
+    const uint32_t t_s = tmem + q * 128, t_o = tmem + 256 + q * D;
     uint32_t n_units_seen = 0, n_q = 0, n_p = 0, n_o = 0, n_k = 0, n_v = 0;
     uint32_t n_turn = 0;  // key tiles walked so far (all units)
     bool ok = true;
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         const bool last = ++s_issued == n_act;
         if (ptx::elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
+          for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
             ptx::mma_ss(t_s, ptx::sdesc_sw128(q_addr + off, 16, 1024), ptx::sdesc_sw128(k_addr + off, 16, 1024),
                         idesc_s, kk > 0 ? 1u : 0u);
@@ -433,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     const int wq = warp & 3;          // warp within the group = TMEM lane quarter
     const int r = wq * 32 + lane;     // row in the query tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    const uint32_t col_s = q * 128, col_o = 256 + q * 128;
+    const uint32_t col_s = q * 128, col_o = 256 + q * D;
     const bool elem_causal = p.mask == kMaskCausal || (p.mask == kMaskBlock && p.causal_in_block);
     const float c = p.scale_log2;
     const int row_half = r >= 64 ? 2 : 0;
@@ -516,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         // waits for p_full, so rescaling O_q now (after P is written) is in time.
         if (n_done > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t orr[32];
             ptx::tmem_ld32(tmem + lane_base + col_o + cc * 32, orr);
             ptx::tmem_ld_wait();
@@ -544,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       const bool row_ok = qi < si.len;
       __nv_bfloat16* orow = O + (row_ok ? q_off(p, si, h, qi) : 0);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t orr[32];
         if (n_done > 0) {
           ptx::tmem_ld32(tmem + lane_base + col_o + cc * 32, orr);
@@ -605,7 +606,8 @@ cudaError_t launch_tc_fwd(const KParams& p, int sms, cudaStream_t st) {
   a.p = p;
   const size_t smem = sizeof(Smem) + 1024;
   const int grid = p.n_units < sms ? p.n_units : sms;
-  auto kernel = p.mask == kMaskBlock ? k_tc_fwd<true> : k_tc_fwd<false>;
+  auto kernel = p.head_dim == 64 ? (p.mask == kMaskBlock ? k_tc_fwd<true, 64> : k_tc_fwd<false, 64>)
+                                 : (p.mask == kMaskBlock ? k_tc_fwd<true, 128> : k_tc_fwd<false, 128>);
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kernel<<<grid, kThreads, smem, st>>>(a);

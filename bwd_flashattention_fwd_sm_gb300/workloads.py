@@ -67,6 +67,9 @@ WORKLOADS = {
     "p2_dense_s2048": Workload("p2_dense_s2048", 1, 8, 8, 2048, 128, "bf16", "none", seed=7),
     # half of the headline batch: the same kernels at a size a profiler replays quickly
     "h1_dense_s8192": Workload("h1_dense_s8192", 1, 16, 16, 8192, 128, "bf16", "none", seed=6),
+    # head dim 64 at the headline length (bf16 on the tensor cores)
+    "h2_dense_s8192_d64": Workload("h2_dense_s8192_d64", 2, 16, 16, 8192, 64, "bf16", "none", seed=8),
+    "h2_causal_s8192_d64": Workload("h2_causal_s8192_d64", 2, 16, 16, 8192, 64, "bf16", "causal", seed=8),
 }
 
 

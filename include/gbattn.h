@@ -43,7 +43,7 @@
  *                   *_stride_s (between tokens) and *_stride_h; *_stride_b ignored.
  *                   lse: contiguous float32 [heads_q, T].
  *
- * Constraints.  head_dim 128 for ATTN_BF16 and 64 or 128 for ATTN_F32;
+ * Constraints.  head_dim 64 or 128 (both types);
  * heads_q % heads_kv == 0; every tensor pointer 16-byte aligned; strides
  * multiples of 8 elements (16 bytes) for bf16 and 4 elements for float32.
  *
@@ -163,7 +163,7 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, con
  * key tiles in ascending order (three products per tile instead of one, so
  * the backward does 7 products instead of 5).  Arguments, layouts and the
  * workspace (attn_bwd_workspace_size bytes) are those of attn_bwd.  Only the
- * tensor-core path (bf16, head_dim 128) has it: other types return
+ * tensor-core path (bf16, head_dim 64 or 128) has it: float32 returns
  * ATTN_ERR_UNSUPPORTED before queuing anything.
  */
 attn_status_t attn_bwd_deterministic(const attn_params_t* p, const void* q, const void* k, const void* v,

@@ -73,7 +73,6 @@ def test_valid_call_without_gpu_fails_with_cuda_error(lib):
     (lambda p: setattr(p, "heads_kv", 3), _lib.ATTN_ERR_INVALID_ARG),
     (lambda p: setattr(p, "heads_q", 0), _lib.ATTN_ERR_INVALID_ARG),
     (lambda p: setattr(p, "head_dim", 96), _lib.ATTN_ERR_UNSUPPORTED),
-    (lambda p: setattr(p, "head_dim", 64), _lib.ATTN_ERR_UNSUPPORTED),  # bf16 needs D = 128
     (lambda p: setattr(p, "dtype", 7), _lib.ATTN_ERR_INVALID_ARG),
     (lambda p: setattr(p, "mask", 9), _lib.ATTN_ERR_INVALID_ARG),
     (lambda p: setattr(p, "q_stride_s", 100), _lib.ATTN_ERR_INVALID_ARG),  # not a multiple of 8
@@ -202,3 +201,12 @@ def test_deterministic_backward_dispatch(lib):
     assert det(p) == _lib.ATTN_ERR_UNSUPPORTED
     assert b"deterministic" in lib.attn_last_error()
     assert det(params()) == _lib.ATTN_ERR_CUDA
+
+
+def test_bf16_head_dim_64_accepted(lib):
+    """bf16 with head_dim 64 runs on the tensor-core kernels: a valid call fails only for want of a GPU."""
+    p = params(D=64)
+    p.q_stride_b, p.q_stride_h, p.q_stride_s = 4 * 256 * 64, 256 * 64, 64
+    p.kv_stride_b, p.kv_stride_h, p.kv_stride_s = 2 * 256 * 64, 256 * 64, 64
+    assert fwd(lib, p) == _lib.ATTN_ERR_CUDA
+    assert bwd(lib, p) == _lib.ATTN_ERR_CUDA

@@ -20,11 +20,12 @@ from test_gpu_parity import SMALL_SHAPES, _slice_heads, small, tiles_csr
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("mask", ["none", "causal", "block"])
 @pytest.mark.parametrize("shape", SMALL_SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_small_shapes_deterministic(shape, mask):
+def test_small_shapes_deterministic(shape, mask, D):
     B, Hq, Hkv, S = shape
-    wl = small(f"det_{mask}", B, Hq, Hkv, S, 128, "bf16", mask, seed=200 + S)
+    wl = small(f"det_{mask}", B, Hq, Hkv, S, D, "bf16", mask, seed=200 + S)
     inp = W.make_inputs(wl.with_(mask="none"))
     if mask == "block":
         inp["block_mask"] = tiles_csr(S, seed=S + 1)

@@ -39,7 +39,7 @@ SMALL_SHAPES = [(1, 2, 2, 1), (1, 2, 1, 17), (2, 2, 2, 64), (1, 4, 1, 127), (1, 
                 (2, 4, 4, 129), (1, 8, 2, 300)]
 
 
-@pytest.mark.parametrize("dtype,D", [("f32", 64), ("f32", 128), ("bf16", 128)])
+@pytest.mark.parametrize("dtype,D", [("f32", 64), ("f32", 128), ("bf16", 64), ("bf16", 128)])
 @pytest.mark.parametrize("mask", ["none", "causal", "block"])
 @pytest.mark.parametrize("shape", SMALL_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_small_shapes(shape, mask, dtype, D):
@@ -53,7 +53,7 @@ def test_small_shapes(shape, mask, dtype, D):
     check_all(wl, got, ref)
 
 
-@pytest.mark.parametrize("dtype,D", [("f32", 64), ("bf16", 128)])
+@pytest.mark.parametrize("dtype,D", [("f32", 64), ("bf16", 64), ("bf16", 128)])
 def test_block_mask_with_empty_row_block(dtype, D):
     """A query block with no listed tile: O = 0, LSE = -inf, no gradient from it."""
     wl = small("empty_row", 1, 2, 2, 256, D, dtype, "block", seed=5)
@@ -66,7 +66,7 @@ def test_block_mask_with_empty_row_block(dtype, D):
     check_all(wl, got, ref)
 
 
-@pytest.mark.parametrize("dtype,D", [("f32", 64), ("bf16", 128)])
+@pytest.mark.parametrize("dtype,D", [("f32", 64), ("bf16", 64), ("bf16", 128)])
 def test_block_mask_without_causal_in_block(dtype, D):
     wl = small("sparse_full", 1, 4, 2, 200, D, dtype, "block", seed=6)
     inp = W.make_inputs(wl.with_(mask="none"))
@@ -74,7 +74,7 @@ def test_block_mask_without_causal_in_block(dtype, D):
     check_all(wl, gpu_run(wl, inp), oracle_run(wl, inp))
 
 
-@pytest.mark.parametrize("dtype,D", [("f32", 128), ("bf16", 128)])
+@pytest.mark.parametrize("dtype,D", [("f32", 128), ("bf16", 64), ("bf16", 128)])
 @pytest.mark.parametrize("causal", [False, True])
 def test_varlen_small(causal, dtype, D):
     lens = [5, 0, 128, 1, 200, 64, 129]
@@ -164,7 +164,7 @@ def test_c5_varlen_sampled_sequences():
     check_all(wl, sub, ref)
 
 
-@pytest.mark.parametrize("name", ["h0_dense_s8192", "h0_causal_s8192"])
+@pytest.mark.parametrize("name", ["h0_dense_s8192", "h0_causal_s8192", "h2_causal_s8192_d64"])
 def test_h0_s8192_sampled_head(name):
     """The S=8192, D=128 headline shape (B=2, H=16): full run, one seeded head checked."""
     wl = W.WORKLOADS[name]
