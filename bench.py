@@ -392,6 +392,85 @@ def run_reference(args, wl):
     return line
 
 
+LN_ROWS, LN_COLS = 16384, 4096  # 2 x 8192 tokens of a 4096-wide residual stream, bf16
+
+
+def run_ln(args):
+    """Fused residual add + LayerNorm, bf16 [16384, 4096]: HBM GB/s of one call.
+
+    Each call reads x and the residual and writes y and h (8 bytes per element;
+    gamma and beta, 32 KB, stay in L2).  The four tensors (512 MiB) exceed L2, so
+    no flush is needed between calls."""
+    import torch
+
+    from bwd_flashattention_fwd_sm_gb300 import layernorm_residual
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator().manual_seed(21)
+    x = (torch.randn(LN_ROWS, LN_COLS, generator=g) * 2 + 0.5).to(torch.bfloat16).to(dev)
+    r = torch.randn(LN_ROWS, LN_COLS, generator=g).to(torch.bfloat16).to(dev)
+    gm = (torch.randn(LN_COLS, generator=g) * 0.5 + 1).to(dev)
+    bt = (torch.randn(LN_COLS, generator=g) * 0.1).to(dev)
+    for _ in range(args.warmup):
+        layernorm_residual(x, r, gm, bt)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(gpu_identity(torch))
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record()
+        layernorm_residual(x, r, gm, bt)
+        b.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    bytes_per_call = 8.0 * LN_ROWS * LN_COLS
+    gbs = bytes_per_call * args.steps / (sum(ms) * 1e-3) / 1e9
+    # end to end: host tensors in pinned memory, copied in and out every call
+    xh, rh = x.cpu().pin_memory(), r.cpu().pin_memory()
+    yh, hh = torch.empty_like(xh).pin_memory(), torch.empty_like(xh).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 5))
+    e0.record()
+    for _ in range(e2e_steps):
+        y, h = layernorm_residual(xh.to(dev, non_blocking=True), rh.to(dev, non_blocking=True), gm, bt)
+        yh.copy_(y, non_blocking=True)
+        hh.copy_(h, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e = bytes_per_call * e2e_steps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    peaks, src = load_peaks()
+    peak = peak_value(peaks, "hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"]
+    line = {
+        "metric": "fused residual add + LayerNorm HBM throughput", "value": round(gbs, 1), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sum(ms) / len(ms), 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: x ~ N(0.5, 2), residual ~ N(0, 1), gamma ~ N(1, 0.5), beta ~ N(0, 0.1), fixed seed",
+        "config": {"workload": f"ln_residual_{LN_ROWS}x{LN_COLS}_bf16", "rows": LN_ROWS, "cols": LN_COLS,
+                   "l2": "inputs and outputs (512 MiB) larger than L2; no flush"},
+        "roofline": {"kernel": "k_ln_residual", "bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(gbs / peak, 4), "traffic": None,
+                     "peak_source": f"{src} HBM copy bandwidth"},
+        "e2e": {"value": round(e2e, 1), "unit": "GB/s", "h2d_bytes_per_step": 4 * LN_ROWS * LN_COLS,
+                "d2h_bytes_per_step": 4 * LN_ROWS * LN_COLS, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        import oracle.ln as oln
+        rows = 256
+        t0 = time.time()
+        oln.ln_residual(x[:rows].double().cpu().numpy(), r[:rows].double().cpu().numpy(), gm.double().cpu().numpy(),
+                        bt.double().cpu().numpy())
+        sec = time.time() - t0
+        line["cpu_baseline"] = {"value": round(8.0 * rows * LN_COLS / sec / 1e9, 4), "unit": "GB/s", "cores": 1,
+                                "kind": "oracle", "sample": f"{rows} rows of the workload, float64 numpy",
+                                "seconds": round(sec, 3)}
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -400,9 +479,15 @@ def main():
     ap.add_argument("--workload", default="h0_dense_s8192")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ln", action="store_true",
+                    help="measure the fused residual add + LayerNorm instead of attention")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.ln:
+        if int(os.environ.get("RANK", "0")) == 0 and args.impl == "ours":
+            print(json.dumps(run_ln(args)), flush=True)
+        return 0
 
     from bwd_flashattention_fwd_sm_gb300 import workloads as W
     wl = W.WORKLOADS[args.workload]

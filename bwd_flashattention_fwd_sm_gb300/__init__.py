@@ -1,9 +1,10 @@
 """gbattn: fused multi-head attention forward and backward for GB300 (sm_103a).
 
 The computation lives in libgbattn.so (hand-written CUDA, C ABI in
-include/gbattn.h); this package is its thin PyTorch binding.
+include/gbattn.h and include/gbln.h); this package is its thin PyTorch binding.
 """
 
 from .attention import BlockMask, SeqLens, attn_bwd, attn_fwd, get_status, make_params
+from .layernorm import layernorm_residual
 
-__all__ = ["attn_fwd", "attn_bwd", "BlockMask", "SeqLens", "get_status", "make_params"]
+__all__ = ["attn_fwd", "attn_bwd", "BlockMask", "SeqLens", "get_status", "make_params", "layernorm_residual"]

@@ -71,7 +71,21 @@ class ParamsC(ctypes.Structure):
     ]
 
 
-# Every symbol include/gbattn.h declares, with its ctypes signature.
+class LnParamsC(ctypes.Structure):
+    """ln_params_t of include/gbln.h."""
+    _fields_ = [
+        ("rows", ctypes.c_int64),
+        ("cols", ctypes.c_int64),
+        ("x_stride", ctypes.c_int64),
+        ("r_stride", ctypes.c_int64),
+        ("y_stride", ctypes.c_int64),
+        ("h_stride", ctypes.c_int64),
+        ("eps", ctypes.c_float),
+        ("dtype", ctypes.c_int32),
+    ]
+
+
+# Every symbol include/gbattn.h and include/gbln.h declare, with its ctypes signature.
 _VP = ctypes.c_void_p
 _PP = ctypes.POINTER(ParamsC)
 SIGNATURES = {
@@ -87,6 +101,7 @@ SIGNATURES = {
     "attn_last_error": (ctypes.c_char_p, []),
     "attn_set_timing_events": (ctypes.c_int, [ctypes.c_int, _VP, _VP]),
     "attn_version": (ctypes.c_char_p, []),
+    "ln_residual_fwd": (ctypes.c_int, [ctypes.POINTER(LnParamsC), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
 }
 
 _lock = threading.Lock()

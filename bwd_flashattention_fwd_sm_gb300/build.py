@@ -23,7 +23,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgbattn.so")
 
 SOURCES = ["api.cu", "sched.cu", "bwd_aux.cu", "simt_attn.cu", "tma_host.cu", "tc_fwd.cu", "tc_bwd.cu", "tc_dq.cu",
-           "noalloc.cu"]
+           "noalloc.cu", "ln.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", CSRC, "-I", INCLUDE]
@@ -47,8 +47,11 @@ def _stamp(extra) -> str:
             h.update(name.encode())
             with open(os.path.join(CSRC, name), "rb") as f:
                 h.update(f.read())
-    with open(os.path.join(INCLUDE, "gbattn.h"), "rb") as f:
-        h.update(f.read())
+    for name in sorted(os.listdir(INCLUDE)):
+        if name.endswith(".h"):
+            h.update(name.encode())
+            with open(os.path.join(INCLUDE, name), "rb") as f:
+                h.update(f.read())
     h.update(" ".join(ARCH + FLAGS + extra).encode())
     return h.hexdigest()
 

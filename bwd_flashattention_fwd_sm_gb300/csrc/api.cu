@@ -288,6 +288,12 @@ attn_status_t cuda_fail(cudaError_t e, const char* what) {
 namespace gbattn {
 // Lets other translation units of the library report an argument error.
 void set_last_error_text(const char* text) { g_last_error = text; }
+// The device status word, SM count and wait limit, for kernels in other
+// translation units of the library.
+attn_status_t device_status(int** status, int* sms, unsigned long long* wait_ns) {
+  *wait_ns = wait_limit_ns();
+  return device_state(status, sms);
+}
 }  // namespace gbattn
 
 extern "C" {

@@ -1,5 +1,5 @@
 """The C ABI without a GPU: the library builds, loads and exports every symbol
-include/gbattn.h declares, and host-side validation rejects bad calls before
+include/gbattn.h and include/gbln.h declare, and host-side validation rejects bad calls before
 any device work.  Valid calls on a machine with no GPU must fail with
 ATTN_ERR_CUDA: there is no CPU path behind the ABI."""
 
@@ -13,15 +13,18 @@ import pytest
 from bwd_flashattention_fwd_sm_gb300 import _lib
 from bwd_flashattention_fwd_sm_gb300._lib import ParamsC, BlockMaskC
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gbattn.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADERS = [os.path.join(INCLUDE, n) for n in sorted(os.listdir(INCLUDE)) if n.endswith(".h")]
 
 FAKE = 1 << 20  # an aligned non-NULL address; never dereferenced by host validation
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(attn_[a-z_]+)\s*\(", text)))
+    names = set()
+    for path in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+        names |= set(re.findall(r"\b((?:attn|ln)_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def params(B=2, Hq=4, Hkv=2, S=256, D=128, dtype=_lib.ATTN_BF16, mask=_lib.ATTN_MASK_CAUSAL):
