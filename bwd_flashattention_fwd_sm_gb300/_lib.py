@@ -101,6 +101,7 @@ SIGNATURES = {
     "attn_last_error": (ctypes.c_char_p, []),
     "attn_set_timing_events": (ctypes.c_int, [ctypes.c_int, _VP, _VP]),
     "attn_version": (ctypes.c_char_p, []),
+    "attn_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_uint, _VP]),
     "ln_residual_fwd": (ctypes.c_int, [ctypes.POINTER(LnParamsC), _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
 }
 

@@ -498,4 +498,16 @@ attn_status_t attn_set_timing_events(int which, void* start, void* stop) {
 
 const char* attn_version(void) { return "gbattn 0.1.0 sm_103a"; }
 
+attn_status_t attn_selftest_bounded_wait(unsigned int limit_us, void* stream) {
+  if (limit_us == 0 || limit_us > 1000000u)
+    return fail(ATTN_ERR_INVALID_ARG, "limit_us=%u: must be in [1, 1000000]", limit_us);
+  int* status = nullptr;
+  int sms = 0;
+  attn_status_t s = device_state(&status, &sms);
+  if (s != ATTN_OK) return s;
+  cudaError_t e = launch_wait_probe(status, (unsigned long long)limit_us * 1000ull, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wait probe launch");
+  return ATTN_OK;
+}
+
 }  // extern "C"

@@ -12,6 +12,7 @@
 // Both are pure streaming kernels: one warp per row, 128-bit or 64-bit loads per
 // lane, a grid sized in multiples of the SM count.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace gbattn {
 
@@ -172,6 +173,28 @@ cudaError_t launch_dq_convert(const KParams& p, bool bf16, cudaStream_t st) {
     if (p.head_dim == 128) k_dq_convert<float, 128><<<grid, 256, 0, st>>>(p, rows);
     else k_dq_convert<float, 64><<<grid, 256, 0, st>>>(p, rows);
   }
+  return cudaGetLastError();
+}
+
+namespace {
+
+__global__ void k_wait_probe(int* status, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ ptx::Abort abort;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&bar, 1);  // one arrival completes it; none comes
+    abort.flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  ptx::mbar_wait(&bar, 0, &abort, status, limit_ns);
+  __syncwarp();
+}
+
+}  // namespace
+
+cudaError_t launch_wait_probe(int* status, unsigned long long limit_ns, cudaStream_t st) {
+  k_wait_probe<<<1, 32, 0, st>>>(status, limit_ns);
   return cudaGetLastError();
 }
 

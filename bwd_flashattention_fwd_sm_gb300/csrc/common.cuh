@@ -150,6 +150,10 @@ cudaError_t launch_csr_to_csc(const KParams& p, int* csc_ptr, int* csc_idx, cuda
 // Backward preprocess (D_i and zeroed dQ accumulator) and dQ conversion.
 cudaError_t launch_bwd_preprocess(const KParams& p, bool bf16, cudaStream_t st);
 cudaError_t launch_dq_convert(const KParams& p, bool bf16, cudaStream_t st);
+// One warp waits, through the kernels' bounded mbarrier wait, on a barrier that
+// nothing completes: after limit_ns it records kStatusTimeout in *status and
+// returns (a check of the device-side timeout path).
+cudaError_t launch_wait_probe(int* status, unsigned long long limit_ns, cudaStream_t st);
 
 // float32-arithmetic SIMT kernels (any dtype, D in {64, 128}).
 cudaError_t launch_simt_fwd(const KParams& p, bool bf16, cudaStream_t st);

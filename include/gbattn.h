@@ -218,6 +218,20 @@ attn_status_t attn_set_timing_events(int which, void* start, void* stop);
 /* Library version, e.g. "gbattn 0.1.0 sm_103a". */
 const char* attn_version(void);
 
+/*
+ * Self-test of the device-side timeout path (the pages have no counterpart:
+ * it checks this library's own failure handling).  Queues one small kernel in
+ * which a warp waits, through the same bounded mbarrier wait every
+ * tensor-core kernel uses, on a barrier that nothing completes.  After
+ * limit_us microseconds (1 .. 1000000) the wait gives up, records
+ * ATTN_ERR_DEVICE_TIMEOUT in the device status word and the kernel returns:
+ * nothing faults, traps or hangs, and the context stays usable.  The next
+ * attn_get_status() on the stream returns ATTN_ERR_DEVICE_TIMEOUT (and clears
+ * it).  Returns ATTN_OK once queued, ATTN_ERR_INVALID_ARG for a limit out of
+ * range.
+ */
+attn_status_t attn_selftest_bounded_wait(unsigned int limit_us, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -213,3 +213,10 @@ def test_bf16_head_dim_64_accepted(lib):
     p.kv_stride_b, p.kv_stride_h, p.kv_stride_s = 2 * 256 * 64, 256 * 64, 64
     assert fwd(lib, p) == _lib.ATTN_ERR_CUDA
     assert bwd(lib, p) == _lib.ATTN_ERR_CUDA
+
+
+def test_selftest_bounded_wait_limit_validated(lib):
+    """The timeout self-test refuses a limit outside [1 us, 1 s] before touching a device."""
+    assert lib.attn_selftest_bounded_wait(0, None) == _lib.ATTN_ERR_INVALID_ARG
+    assert lib.attn_selftest_bounded_wait(2_000_000, None) == _lib.ATTN_ERR_INVALID_ARG
+    assert lib.attn_selftest_bounded_wait(1000, None) == _lib.ATTN_ERR_CUDA  # valid, but no GPU here
