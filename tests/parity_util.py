@@ -11,6 +11,11 @@ Tolerances (written here, used by every GPU test):
                 values; a bf16 output of magnitude >= 4 cannot hold it by itself
                 (its spacing is 2^-5 and above), so each element also gets one
                 bf16 unit in the last place of its own magnitude (2^-7 |x| bounds it).
+                dK and dV of a KV head are sums over its group of G query heads,
+                each head adding its own bf16 rounding of dS and P, so their
+                absolute error grows like sqrt(G): the 2e-2 term is read at the
+                largest group of the configurations (G = 4, the causal GQA one)
+                and scaled by sqrt(G / 4) above it.
 """
 
 from __future__ import annotations
@@ -28,7 +33,7 @@ TOL_BF16_REL = 1e-2
 TOL_BF16_ULP = 2.0 ** -7
 
 
-def compare(name, got, ref, dtype):
+def compare(name, got, ref, dtype, abs_scale=1.0):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, f"{name}: shape {got.shape} vs {ref.shape}"
@@ -48,7 +53,7 @@ def compare(name, got, ref, dtype):
     elif name.startswith("lse"):
         assert max_abs <= TOL_BF16_ABS, f"{name}: max-abs {max_abs:.3e} > {TOL_BF16_ABS}"
     else:
-        bound = TOL_BF16_ABS + TOL_BF16_ULP * np.abs(r)
+        bound = TOL_BF16_ABS * abs_scale + TOL_BF16_ULP * np.abs(r)
         worst = int(np.argmax(err - bound))
         assert np.all(err <= bound), (f"{name}: |err| {err[worst]:.3e} > {bound[worst]:.3e} at value "
                                       f"{r[worst]:.4f} (max-abs {max_abs:.3e})")
@@ -104,7 +109,9 @@ def oracle_run(wl, inputs, passes="fwd+bwd", cu=None):
 
 def check_all(wl, got, ref, names=("o", "lse", "dq", "dk", "dv")):
     report = {}
+    group = wl.heads_q // wl.heads_kv
     for n in names:
         if n in ref:
-            report[n] = compare(f"{n}[{wl.name}]", got[n], ref[n], wl.dtype)
+            scale = max(1.0, (group / 4.0) ** 0.5) if n in ("dk", "dv") else 1.0
+            report[n] = compare(f"{n}[{wl.name}]", got[n], ref[n], wl.dtype, abs_scale=scale)
     return report

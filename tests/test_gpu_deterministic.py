@@ -42,16 +42,17 @@ def test_block_mask_empty_row_block_deterministic():
     check_all(wl, got, oracle_run(wl, inp))
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_varlen_deterministic(causal):
+def test_varlen_deterministic(causal, D):
     lens = [5, 0, 128, 1, 300, 64, 129, 257]
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
-    wl = W.Workload("det_varlen", 1, 4, 2, max(lens), 128, "bf16", "causal" if causal else "none",
+    wl = W.Workload("det_varlen", 1, 4, 2, max(lens), D, "bf16", "causal" if causal else "none",
                     varlen=True, n_seqs=len(lens), seed=19)
     T = int(cu[-1])
     g = torch.Generator().manual_seed(19)
     inp = {n: torch.randn(s, generator=g).to(torch.bfloat16) for n, s in
-           (("q", (T, 4, 128)), ("k", (T, 2, 128)), ("v", (T, 2, 128)), ("do", (T, 4, 128)))}
+           (("q", (T, 4, D)), ("k", (T, 2, D)), ("v", (T, 2, D)), ("do", (T, 4, D)))}
     inp["cu_seqlens"] = cu
     check_all(wl, gpu_run(wl, inp, deterministic=True), oracle_run(wl, inp, cu=cu))
 

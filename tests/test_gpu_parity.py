@@ -36,7 +36,7 @@ def tiles_csr(S, seed, density=0.5, empty_row=None, causal_in_block=1):
 
 
 SMALL_SHAPES = [(1, 2, 2, 1), (1, 2, 1, 17), (2, 2, 2, 64), (1, 4, 1, 127), (1, 2, 2, 128),
-                (2, 4, 4, 129), (1, 8, 2, 300)]
+                (2, 4, 4, 129), (1, 8, 2, 300), (1, 16, 1, 257)]
 
 
 @pytest.mark.parametrize("dtype,D", [("f32", 64), ("f32", 128), ("bf16", 64), ("bf16", 128)])
@@ -183,3 +183,12 @@ def test_empty_batch():
     o, lse = attn_fwd(q, q, q)
     dq, dk, dv = attn_bwd(q, q, q, o, q, lse)
     assert o.shape == q.shape and lse.shape == (0, 2, 64) and dq.shape == q.shape
+
+
+def test_longest_sequence_sampled_head():
+    """S = 32768 (four times the headline length), causal, D = 64, one head: the
+    whole problem on the GPU against the oracle's full result (LSE spans the
+    largest row sums, the last query tile sees 256 key tiles)."""
+    wl = W.Workload("long_s32768", 1, 1, 1, 32768, 64, "bf16", "causal", seed=13)
+    inp = W.make_inputs(wl)
+    check_all(wl, gpu_run(wl, inp), oracle_run(wl, inp))
