@@ -190,9 +190,11 @@ def run_ours(args, wl, rank, world, dist):
     step_ev = [(ev(), ev()) for _ in range(args.steps)]
     fwd_ev = [(ev(), ev()) for _ in range(args.steps)]
     bwd_ev = [(ev(), ev()) for _ in range(args.steps)]
+    pre_ev = [(ev(), ev()) for _ in range(args.steps)]
+    cvt_ev = [(ev(), ev()) for _ in range(args.steps)]
     # torch creates the CUDA event behind an Event on its first record: record
     # each once so that the library's timing hook receives real handles.
-    for pair in fwd_ev + bwd_ev:
+    for pair in fwd_ev + bwd_ev + pre_ev + cvt_ev:
         for e in pair:
             e.record(stream)
     torch.cuda.synchronize()
@@ -207,11 +209,13 @@ def run_ours(args, wl, rank, world, dist):
         flush.fill_(i & 0xFF)
         lib.attn_set_timing_events(0, ctypes.c_void_p(fwd_ev[i][0].cuda_event), ctypes.c_void_p(fwd_ev[i][1].cuda_event))
         lib.attn_set_timing_events(1, ctypes.c_void_p(bwd_ev[i][0].cuda_event), ctypes.c_void_p(bwd_ev[i][1].cuda_event))
+        lib.attn_set_timing_events(2, ctypes.c_void_p(pre_ev[i][0].cuda_event), ctypes.c_void_p(pre_ev[i][1].cuda_event))
+        lib.attn_set_timing_events(3, ctypes.c_void_p(cvt_ev[i][0].cuda_event), ctypes.c_void_p(cvt_ev[i][1].cuda_event))
         step_ev[i][0].record(stream)
         step()
         step_ev[i][1].record(stream)
-    lib.attn_set_timing_events(0, None, None)
-    lib.attn_set_timing_events(1, None, None)
+    for which in range(4):
+        lib.attn_set_timing_events(which, None, None)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -223,6 +227,8 @@ def run_ours(args, wl, rank, world, dist):
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     fwd_ms = [a.elapsed_time(b) for a, b in fwd_ev]
     bwd_ms = [a.elapsed_time(b) for a, b in bwd_ev]
+    pre_ms = [a.elapsed_time(b) for a, b in pre_ev]
+    cvt_ms = [a.elapsed_time(b) for a, b in cvt_ev]
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
     ms_per_step = total_ms / args.steps
     step_flops = fwd_flops + bwd_flops
@@ -300,6 +306,17 @@ def run_ours(args, wl, rank, world, dist):
         except Exception:
             traffic = None
     launches_per_step = 2 + 4 + (1 if wl.mask == "block" else 0)
+    # the backward's two HBM-bound kernels, against the HBM copy bandwidth
+    hbm = peak_value(peaks, "hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"]
+    rows = (int(inp["cu_seqlens"][-1]) if wl.varlen else wl.batch * wl.seqlen) * wl.heads_q
+    esz = 2 if wl.dtype == "bf16" else 4
+    aux = {}
+    for name, times, per_row in (("bwd_preprocess", pre_ms, 2 * wl.head_dim * esz + 4 + 4 * wl.head_dim),
+                                 ("dq_convert", cvt_ms, 4 * wl.head_dim + wl.head_dim * esz)):
+        t = sum(times) / len(times)
+        gbs = rows * per_row / (t * 1e-3) / 1e9
+        aux[name] = {"ms": round(t, 4), "bytes": rows * per_row, "gbs": round(gbs, 1),
+                     "frac_of_hbm": round(gbs / hbm, 4), "bound": "hbm"}
 
     line = {
         "metric": "attention fwd+bwd TFLOPS (bf16, D=128, S=8192) and % of GB300 BF16 tensor peak",
@@ -332,6 +349,7 @@ def run_ours(args, wl, rank, world, dist):
             "peak_source": f"{peak_src} bf16 dense" + (" (MEASURED_PEAKS.json)" if peak_src == "measured" else
                                                         " (no MEASURED_PEAKS.json: 1.9 PFLOP/s burst)"),
         },
+        "aux": aux,
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "copies": "pinned host buffers; H2D and D2H on their own streams, double-buffered, "

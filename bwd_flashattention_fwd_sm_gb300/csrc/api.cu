@@ -23,7 +23,9 @@ using namespace gbattn;
 namespace {
 
 thread_local std::string g_last_error;
-thread_local cudaEvent_t g_timing_events[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};
+// [which][start/stop]: 0 forward main kernel, 1 backward main kernel(s), 2 backward
+// preprocess, 3 dQ conversion
+thread_local cudaEvent_t g_timing_events[4][2] = {};
 
 __device__ int g_status_word;  // one per device; set by kernels, cleared by attn_get_status
 
@@ -133,6 +135,10 @@ attn_status_t validate_params(const attn_params_t* p, Problem* pr) {
   }
   pr->empty = pr->total_tokens == 0;
   if (pr->empty) return ATTN_OK;  // nothing is read or written
+  // query rows over all heads are indexed in 32 bits on the device
+  if (pr->total_tokens * (long long)p->heads_q >= (1ll << 31))
+    return fail(ATTN_ERR_UNSUPPORTED, "%lld query rows over all heads: at most 2^31 - 1 are supported",
+                pr->total_tokens * (long long)p->heads_q);
 
   const int align = p->dtype == ATTN_BF16 ? 8 : 4;
   const long long strides[6] = {p->q_stride_b, p->q_stride_h, p->q_stride_s,
@@ -422,8 +428,12 @@ attn_status_t bwd_impl(const attn_params_t* p, const void* q, const void* k, con
                               reinterpret_cast<int*>(ws + L.q_sched), st);
     if (e != cudaSuccess) return cuda_fail(e, "work-list launch");
   }
+  if (g_timing_events[2][0] && (e = cudaEventRecord(g_timing_events[2][0], st)) != cudaSuccess)
+    return cuda_fail(e, "timing event");
   e = launch_bwd_preprocess(kp, bf16, st);
   if (e != cudaSuccess) return cuda_fail(e, "preprocess launch");
+  if (g_timing_events[2][1] && (e = cudaEventRecord(g_timing_events[2][1], st)) != cudaSuccess)
+    return cuda_fail(e, "timing event");
   if (g_timing_events[1][0] && (e = cudaEventRecord(g_timing_events[1][0], st)) != cudaSuccess)
     return cuda_fail(e, "timing event");
   if (use_tensor_cores(p, true)) e = launch_tc_bwd(kp, sms, st, !deterministic);
@@ -433,8 +443,12 @@ attn_status_t bwd_impl(const attn_params_t* p, const void* q, const void* k, con
   if (g_timing_events[1][1] && (e = cudaEventRecord(g_timing_events[1][1], st)) != cudaSuccess)
     return cuda_fail(e, "timing event");
   if (!deterministic) {
+    if (g_timing_events[3][0] && (e = cudaEventRecord(g_timing_events[3][0], st)) != cudaSuccess)
+      return cuda_fail(e, "timing event");
     e = launch_dq_convert(kp, bf16, st);
     if (e != cudaSuccess) return cuda_fail(e, "dQ conversion launch");
+    if (g_timing_events[3][1] && (e = cudaEventRecord(g_timing_events[3][1], st)) != cudaSuccess)
+      return cuda_fail(e, "timing event");
   }
   return ATTN_OK;
 }
@@ -490,7 +504,7 @@ const char* attn_status_string(attn_status_t s) {
 const char* attn_last_error(void) { return g_last_error.c_str(); }
 
 attn_status_t attn_set_timing_events(int which, void* start, void* stop) {
-  if (which != 0 && which != 1) return fail(ATTN_ERR_INVALID_ARG, "timing hook %d is not 0 or 1", which);
+  if (which < 0 || which > 3) return fail(ATTN_ERR_INVALID_ARG, "timing hook %d is not 0, 1, 2 or 3", which);
   g_timing_events[which][0] = static_cast<cudaEvent_t>(start);
   g_timing_events[which][1] = static_cast<cudaEvent_t>(stop);
   return ATTN_OK;

@@ -9,8 +9,9 @@
 //    the gradient whose accumulation runs against the key-block loop, so every key
 //    tile adds into it (same section: "many cores accumulate into the same place").
 //
-// Both are pure streaming kernels: one warp per row, 128-bit or 64-bit loads per
-// lane, a grid sized in multiples of the SM count.
+// Both are pure streaming kernels: a warp takes a batch of rows at a time
+// (16-byte loads and stores per lane, all loads issued before use), a grid
+// sized in multiples of the SM count.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -59,20 +60,22 @@ struct RowRef {
 };
 
 // Flat row r (over all positions of all sequences and all query heads) to offsets.
+// The divisions run in 32 bits (rows, heads and lengths all fit; the host caps
+// problems well below 2^31 rows).
 __device__ __forceinline__ RowRef row_ref(const KParams& p, long long r) {
   RowRef x;
-  const int H = p.heads_q;
+  const unsigned H = (unsigned)p.heads_q, ur = (unsigned)r;
   if (p.varlen) {
-    const long long tok = r / H;
-    const int h = (int)(r - tok * H);
-    x.q = tok * p.q_ss + (long long)h * p.q_sh;
+    const unsigned tok = ur / H;
+    const int h = (int)(ur - tok * H);
+    x.q = (long long)tok * p.q_ss + (long long)h * p.q_sh;
     x.lse = (long long)h * p.total_tokens + tok;
-    x.acc = (tok * H + h) * (long long)p.head_dim;
+    x.acc = r * (long long)p.head_dim;
   } else {
-    const long long S = p.seqlen;
-    const long long bh = r / S;
-    const long long pos = r - bh * S;
-    const int b = (int)(bh / H), h = (int)(bh % H);
+    const unsigned S = (unsigned)p.seqlen;
+    const unsigned bh = ur / S;
+    const long long pos = (long long)(ur - bh * S);
+    const int b = (int)(bh / H), h = (int)(bh - (bh / H) * H);
     x.q = (long long)b * p.q_sb + (long long)h * p.q_sh + pos * p.q_ss;
     x.lse = r;
     x.acc = r * (long long)p.head_dim;
@@ -80,55 +83,107 @@ __device__ __forceinline__ RowRef row_ref(const KParams& p, long long r) {
   return x;
 }
 
+// Rows a warp is given at least (grid sizing); each kernel takes its own batch
+// per iteration, all loads issued before use, so HBM sees tens of KB in flight
+// per SM.
+constexpr int kRows = 4;
+
+// Preprocess with 16-byte loads: L = D / E lanes cover one row (E elements of
+// 16 bytes each), so one load instruction covers 32 / L rows; a warp takes
+// kPreRows rows per iteration, all loads issued before use.
+constexpr int kPreRows = 8;
+
 template <class T, int D>
 __global__ void __launch_bounds__(256) k_bwd_preprocess(KParams p, long long n_rows) {
-  constexpr int N = D / 32;
+  constexpr int E = 16 / (int)sizeof(T);   // elements per 16-byte load
+  constexpr int L = D / E;                 // lanes per row
+  constexpr int RP = 32 / L;               // rows per load instruction
+  constexpr int NL = kPreRows / RP;        // load instructions per tensor per iteration
+  static_assert(L <= 32 && 32 % L == 0 && kPreRows % RP == 0, "row geometry");
   const int lane = threadIdx.x & 31;
+  const int sub = lane % L, part = lane / L;
   const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   const T* o = static_cast<const T*>(p.o);
   const T* dO = static_cast<const T*>(p.dout);
-  for (long long r = warp0; r < n_rows; r += nwarps) {
-    const RowRef x = row_ref(p, r);
-    float a[N], b[N];
-    load_vec<T, N>(o + x.q + lane * N, a);
-    load_vec<T, N>(dO + x.q + lane * N, b);
-    float s = 0.f;
+  for (long long r0 = warp0 * kPreRows; r0 < n_rows; r0 += nwarps * kPreRows) {
+    float a[NL][E], b[NL][E];
+    RowRef x[NL];
 #pragma unroll
-    for (int i = 0; i < N; ++i) s = fmaf(a[i], b[i], s);
+    for (int j = 0; j < NL; ++j) {
+      const long long r = r0 + j * RP + part;
+      if (r < n_rows) {
+        x[j] = row_ref(p, r);
+        load_vec<T, E>(o + x[j].q + sub * E, a[j]);
+        load_vec<T, E>(dO + x[j].q + sub * E, b[j]);
+      } else {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) p.delta[x.lse] = s;
+        for (int i = 0; i < E; ++i) a[j][i] = b[j][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NL; ++j) {
+      const long long r = r0 + j * RP + part;
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < E; ++i) s = fmaf(a[j][i], b[j][i], s);
+#pragma unroll
+      for (int off = L / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (sub == 0 && r < n_rows) p.delta[x[j].lse] = s;
+    }
     if (p.dq_accum) {  // no accumulator in the deterministic (query-stationary dQ) mode
-      float z[N];
+      // zero the rows' float32 accumulator: D / 4 lanes of 16 bytes per row
+      constexpr int LZ = D / 4, RZ = 32 / LZ;
+      const int subz = lane % LZ, partz = lane / LZ;
 #pragma unroll
-      for (int i = 0; i < N; ++i) z[i] = 0.f;
-      store_vec<float, N>(p.dq_accum + x.acc + lane * N, z);
+      for (int j = 0; j < kPreRows / RZ; ++j) {
+        const long long r = r0 + j * RZ + partz;
+        // the accumulator is contiguous over flat rows: row r starts at r * D
+        if (r < n_rows) *reinterpret_cast<float4*>(p.dq_accum + r * D + subz * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   }
 }
 
+// dQ conversion with 16-byte stores: a lane converts E = 16 / sizeof(T)
+// consecutive elements (E float32 read as E / 4 16-byte loads), L = D / E
+// lanes per row; a warp takes kCvtRows rows per iteration.
+constexpr int kCvtRows = 8;
+
 template <class T, int D>
 __global__ void __launch_bounds__(256) k_dq_convert(KParams p, long long n_rows) {
-  constexpr int N = D / 32;
+  constexpr int E = 16 / (int)sizeof(T);
+  constexpr int L = D / E, RP = 32 / L, NL = kCvtRows / RP;
+  static_assert(L <= 32 && 32 % L == 0 && kCvtRows % RP == 0 && E % 4 == 0, "row geometry");
   const int lane = threadIdx.x & 31;
+  const int sub = lane % L, part = lane / L;
   const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
   T* dq = static_cast<T*>(p.dq);
-  for (long long r = warp0; r < n_rows; r += nwarps) {
-    const RowRef x = row_ref(p, r);
-    float a[N];
-    const float4* src = reinterpret_cast<const float4*>(p.dq_accum + x.acc + lane * N);
-    if constexpr (N == 4) {
-      float4 f = __ldcs(src);
-      a[0] = f.x; a[1] = f.y; a[2] = f.z; a[3] = f.w;
-    } else {
-      float2 f = __ldcs(reinterpret_cast<const float2*>(src));
-      a[0] = f.x; a[1] = f.y;
+  for (long long r0 = warp0 * kCvtRows; r0 < n_rows; r0 += nwarps * kCvtRows) {
+    float a[NL][E];
+    RowRef x[NL];
+#pragma unroll
+    for (int j = 0; j < NL; ++j) {
+      const long long r = r0 + j * RP + part;
+      if (r < n_rows) {
+        x[j] = row_ref(p, r);
+        const float4* src = reinterpret_cast<const float4*>(p.dq_accum + x[j].acc + sub * E);
+#pragma unroll
+        for (int v = 0; v < E / 4; ++v) {
+          const float4 f = __ldcs(src + v);
+          a[j][4 * v] = f.x; a[j][4 * v + 1] = f.y; a[j][4 * v + 2] = f.z; a[j][4 * v + 3] = f.w;
+        }
+      }
     }
 #pragma unroll
-    for (int i = 0; i < N; ++i) a[i] *= p.scale;
-    store_vec<T, N>(dq + x.q + lane * N, a);
+    for (int j = 0; j < NL; ++j) {
+      const long long r = r0 + j * RP + part;
+      if (r >= n_rows) continue;
+#pragma unroll
+      for (int i = 0; i < E; ++i) a[j][i] *= p.scale;
+      store_vec<T, E>(dq + x[j].q + sub * E, a[j]);
+    }
   }
 }
 
@@ -141,7 +196,7 @@ int grid_for(long long rows) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  long long want = (rows + 7) / 8;  // 8 warps per block
+  long long want = (rows + 8 * kRows - 1) / (8 * kRows);  // 8 warps per block, kRows (or more) rows per warp
   long long cap = (long long)sms * 8;
   return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }

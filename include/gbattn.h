@@ -208,10 +208,11 @@ const char* attn_last_error(void);
 /*
  * Measurement hook.  While set, every attn_fwd (which = 0) or attn_bwd (which = 1)
  * made by the calling thread records the CUDA event `start` on its stream just
- * before launching its main attention kernel and `stop` just after it, so a
- * caller can time that kernel alone.  `start` and `stop` are cudaEvent_t handles
- * owned by the caller; NULL clears the hook.  Returns ATTN_ERR_INVALID_ARG for an
- * unknown `which`.
+ * before launching its main attention kernel(s) and `stop` just after, so a
+ * caller can time them alone; which = 2 and 3 bracket the backward's
+ * preprocess (D and the accumulator zero-fill) and its dQ conversion.  `start`
+ * and `stop` are cudaEvent_t handles owned by the caller; NULL clears the hook.
+ * Returns ATTN_ERR_INVALID_ARG for an unknown `which`.
  */
 attn_status_t attn_set_timing_events(int which, void* start, void* stop);
 

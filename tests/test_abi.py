@@ -220,3 +220,10 @@ def test_selftest_bounded_wait_limit_validated(lib):
     assert lib.attn_selftest_bounded_wait(0, None) == _lib.ATTN_ERR_INVALID_ARG
     assert lib.attn_selftest_bounded_wait(2_000_000, None) == _lib.ATTN_ERR_INVALID_ARG
     assert lib.attn_selftest_bounded_wait(1000, None) == _lib.ATTN_ERR_CUDA  # valid, but no GPU here
+
+
+def test_row_count_limit(lib):
+    """Query rows over all heads are indexed in 32 bits on the device: more are refused."""
+    p = params(B=1 << 12, Hq=1 << 10, Hkv=1 << 10, S=1 << 10)
+    assert fwd(lib, p) == _lib.ATTN_ERR_UNSUPPORTED
+    assert b"2^31" in lib.attn_last_error()
