@@ -278,7 +278,7 @@ def run_ours(args, wl, rank, world, dist):
     e2e_run(max(1, min(args.warmup, 2)))
     torch.cuda.synchronize()
     keep.clear()
-    e2e_steps = max(1, min(args.steps, 5))
+    e2e_steps = max(1, min(args.steps, 10))
     if dist is not None:
         dist.barrier()
     t0 = time.perf_counter()
@@ -475,7 +475,7 @@ def run_ln(args):
     xh, rh = x.cpu().pin_memory(), r.cpu().pin_memory()
     yh, hh = torch.empty_like(xh).pin_memory(), torch.empty_like(xh).pin_memory()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(1, min(args.steps, 5))
+    e2e_steps = max(1, min(args.steps, 10))
     e0.record()
     for _ in range(e2e_steps):
         y, h = layernorm_residual(xh.to(dev, non_blocking=True), rh.to(dev, non_blocking=True), gm, bt)
