@@ -514,6 +514,139 @@ def run_ln(args):
     return line
 
 
+def run_fp8(args, wl):
+    """FP8 (e4m3) forward: one step = per-tile quantisation of Q, K, V plus the
+    FP8 forward kernel, over the workload's batch (fixed length).  `value` counts
+    the forward's algorithmic FLOPs (4 D per unmasked pair per head) over the
+    whole step; the roofline covers the forward kernel alone, against the
+    measured bf16 dense peak times the nominal FP8 / bf16 ratio (4.5 / 2.25)."""
+    import ctypes
+
+    import torch
+
+    from bwd_flashattention_fwd_sm_gb300 import BlockMask, attn_fwd_fp8, get_status, quantize_fp8
+    from bwd_flashattention_fwd_sm_gb300 import _lib
+    from bwd_flashattention_fwd_sm_gb300 import workloads as W
+
+    if wl.varlen or wl.head_dim != 128 or wl.dtype != "bf16":
+        raise SystemExit("--fp8 takes fixed-length bf16 workloads with head_dim 128")
+    lib = _lib.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = W.make_inputs(wl)
+    bm = inp.get("block_mask")
+    fwd_flops, _, pairs = flops_of(wl, bm)
+    kw = {"scale": wl.scale, "causal": wl.mask == "causal"}
+    if bm is not None:
+        kw["block_mask"] = BlockMask.from_csr(bm, device=dev)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    f = quantize_fp8(q, k, v)
+    o, lse = attn_fwd_fp8(f, **kw)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        quantize_fp8(q, k, v, out=f)
+        return attn_fwd_fp8(f, workspace=ws, out=o, **kw)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    step_ev = [(ev(), ev()) for _ in range(args.steps)]
+    fwd_ev = [(ev(), ev()) for _ in range(args.steps)]
+    for pair in fwd_ev:
+        for e in pair:
+            e.record(stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(gpu_identity(torch))
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        lib.attn_set_timing_events(0, ctypes.c_void_p(fwd_ev[i][0].cuda_event), ctypes.c_void_p(fwd_ev[i][1].cuda_event))
+        step_ev[i][0].record(stream)
+        step()
+        step_ev[i][1].record(stream)
+    lib.attn_set_timing_events(0, None, None)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if get_status() != 0:
+        raise RuntimeError("device status word set during the benchmark")
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    fwd_ms = [a.elapsed_time(b) for a, b in fwd_ev]
+    ms_per_step = sum(step_ms) / len(step_ms)
+    fwd_avg = sum(fwd_ms) / len(fwd_ms)
+    value = fwd_flops / (ms_per_step * 1e-3) / 1e12
+    achieved = fwd_flops / (fwd_avg * 1e-3) / 1e12
+    quant_ms = ms_per_step - fwd_avg  # the rest of the step: quantisation and the work-list build
+    elems = (wl.heads_q + 2 * wl.heads_kv) * wl.batch * wl.seqlen * wl.head_dim
+    quant_bytes = 3 * elems  # 2 bytes read and 1 written per element
+
+    # end to end: bf16 inputs from pinned host memory, O and LSE back, every step
+    host_in = [t.cpu().pin_memory() for t in (q, k, v)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    ho, hl = torch.empty(o.shape, dtype=o.dtype, pin_memory=True), torch.empty(lse.shape, dtype=lse.dtype,
+                                                                                pin_memory=True)
+    e2e_steps = max(1, min(args.steps, 10))
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        dq_, dk_, dv_ = (h.to(dev, non_blocking=True) for h in host_in)
+        quantize_fp8(dq_, dk_, dv_, out=f)
+        o2, l2 = attn_fwd_fp8(f, workspace=ws, **kw)
+        ho.copy_(o2, non_blocking=True)
+        hl.copy_(l2, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e = fwd_flops * e2e_steps / (e0.elapsed_time(e1) * 1e-3) / 1e12
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    peaks, src = load_peaks()
+    bf16_peak = peak_value(peaks, "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
+    peak = 2.0 * bf16_peak
+    hbm = peak_value(peaks, "hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"]
+    qgbs = quant_bytes / (quant_ms * 1e-3) / 1e9
+    line = {
+        "metric": "attention forward TFLOPS with e4m3 operands (D=128, S=8192) and % of GB300 FP8 tensor peak",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3",
+        "data": "synthetic: Q,K,V iid N(0,1) from a fixed seed, rounded to bf16, quantised per 128-row tile",
+        "config": {"workload": wl.name + "_fp8", "batch": wl.batch, "heads_q": wl.heads_q, "heads_kv": wl.heads_kv,
+                   "seq_len": wl.seqlen, "head_dim": wl.head_dim, "mask": wl.mask,
+                   "step": "attn_quantize_fp8 + attn_fwd_fp8",
+                   "l2": "512 MiB L2 flush written between timed steps (outside the step events)",
+                   "fwd_flops": fwd_flops},
+        "fwd_ms": round(fwd_avg, 4), "fwd_tflops": round(achieved, 2),
+        "roofline": {"kernel": "FP8 forward (k_tc_fwd, e4m3 operands)", "bound": "tensor",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": f"{src} bf16 dense x 2 (nominal FP8 / bf16 ratio 4.5 / 2.25 PFLOP/s)"},
+        "aux": {"quantize": {"ms": round(quant_ms, 4), "bytes": quant_bytes, "gbs": round(qgbs, 1),
+                             "frac_of_hbm": round(qgbs / hbm, 4), "bound": "hbm",
+                             "note": "step time minus the forward kernel's events (includes the work-list build)"}},
+        "e2e": {"value": round(e2e, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        from oracle import fp8 as ofp8
+        t0 = time.perf_counter()
+        sl = (slice(0, 1), slice(0, 1))
+        deq = [ofp8.dequantize(*ofp8.quantize_tiles(inp[n][sl].float().numpy())) for n in ("q", "k", "v")]
+        oracle.attn_fwd(*deq, scale=wl.scale, causal=wl.mask == "causal", block_mask=bm)
+        sec = time.perf_counter() - t0
+        per_head = fwd_flops / wl.heads_q / wl.batch
+        line["cpu_baseline"] = {"value": per_head / sec / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count() or 1,
+                                "kind": "oracle",
+                                "sample": f"1 head of {wl.name} at full length: quantise + float64 forward",
+                                "seconds": round(sec, 2)}
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -524,6 +657,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ln", action="store_true",
                     help="measure the fused residual add + LayerNorm instead of attention")
+    ap.add_argument("--fp8", action="store_true",
+                    help="measure the FP8 (e4m3) forward (quantisation + forward) on --workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -534,6 +669,10 @@ def main():
 
     from bwd_flashattention_fwd_sm_gb300 import workloads as W
     wl = W.WORKLOADS[args.workload]
+    if args.fp8:
+        if int(os.environ.get("RANK", "0")) == 0 and args.impl == "ours":
+            print(json.dumps(run_fp8(args, wl)), flush=True)
+        return 0
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

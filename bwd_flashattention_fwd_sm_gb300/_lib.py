@@ -96,6 +96,8 @@ SIGNATURES = {
     "attn_bwd_deterministic": (ctypes.c_int,
                                [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
     "attn_bwd_noalloc": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "attn_quantize_fp8": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "attn_fwd_fp8": (ctypes.c_int, [_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
     "attn_get_status": (ctypes.c_int, [_VP]),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_last_error": (ctypes.c_char_p, []),

@@ -194,6 +194,64 @@ def attn_bwd(q, k, v, o, do, lse, *, causal=False, block_mask: BlockMask | None 
     return dq, dk, dv
 
 
+class Fp8Operands:
+    """Per-tile e4m3 codes and scales of Q, K, V (attn_quantize_fp8's outputs).
+
+    q8 [B, Hq, S, 128] and k8 [B, Hkv, S, 128] uint8; v8t [B, Hkv, 128, ld] uint8
+    (V's codes transposed, ld = S rounded up to 16); q_scale [B, Hq, n_tiles],
+    k_scale and v_scale [B, Hkv, n_tiles] float32 with n_tiles = ceil(S / 128).
+    """
+
+    def __init__(self, q8, k8, v8t, q_scale, k_scale, v_scale):
+        self.q8, self.k8, self.v8t = q8, k8, v8t
+        self.q_scale, self.k_scale, self.v_scale = q_scale, k_scale, v_scale
+
+    @classmethod
+    def empty(cls, batch, heads_q, heads_kv, seqlen, device):
+        ld = (seqlen + 15) // 16 * 16
+        nt = (seqlen + 127) // 128
+        u8, f32 = torch.uint8, torch.float32
+        return cls(torch.empty((batch, heads_q, seqlen, 128), dtype=u8, device=device),
+                   torch.empty((batch, heads_kv, seqlen, 128), dtype=u8, device=device),
+                   torch.empty((batch, heads_kv, 128, ld), dtype=u8, device=device),
+                   torch.empty((batch, heads_q, nt), dtype=f32, device=device),
+                   torch.empty((batch, heads_kv, nt), dtype=f32, device=device),
+                   torch.empty((batch, heads_kv, nt), dtype=f32, device=device))
+
+
+def quantize_fp8(q, k, v, *, stream=None, out: Fp8Operands | None = None) -> Fp8Operands:
+    """Per-tile e4m3 quantisation of bf16 q [B, Hq, S, 128], k, v [B, Hkv, S, 128]."""
+    lib = _lib.load()
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    if v.shape != k.shape or v.dtype != k.dtype:
+        raise ValueError("v must match k in shape and dtype")
+    p = make_params(q, k)
+    f = out if out is not None else Fp8Operands.empty(q.shape[0], q.shape[1], k.shape[1], q.shape[2], q.device)
+    check(lib.attn_quantize_fp8(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(f.q8), _ptr(f.k8), _ptr(f.v8t),
+                                _ptr(f.q_scale), _ptr(f.k_scale), _ptr(f.v_scale), _stream_handle(stream)),
+          "attn_quantize_fp8")
+    return f
+
+
+def attn_fwd_fp8(f: Fp8Operands, *, causal=False, block_mask: BlockMask | None = None, scale=None, stream=None,
+                 workspace=None, out=None):
+    """O (bf16), LSE of attention on the dequantised FP8 operands.  Returns (o, lse)."""
+    lib = _lib.load()
+    B, Hq, S, D = f.q8.shape
+    o = out if out is not None else torch.empty((B, Hq, S, D), dtype=torch.bfloat16, device=f.q8.device)
+    # the parameter block: q strides describe the bf16 O; K and V are the codes' fixed layouts
+    p = make_params(o, o, causal=causal, block_mask=block_mask, scale=scale)
+    Hkv = f.k8.shape[1]
+    p.heads_kv = Hkv
+    p.kv_stride_b, p.kv_stride_h, p.kv_stride_s = Hkv * S * D, S * D, D
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=f.q8.device)
+    ws = _workspace(lib.attn_fwd_workspace_size(ctypes.byref(p)), f.q8.device, workspace)
+    check(lib.attn_fwd_fp8(ctypes.byref(p), _ptr(f.q8), _ptr(f.k8), _ptr(f.v8t), _ptr(f.q_scale), _ptr(f.k_scale),
+                           _ptr(f.v_scale), _ptr(o), _ptr(lse), _ptr(ws),
+                           ctypes.c_size_t(0 if ws is None else ws.numel()), _stream_handle(stream)), "attn_fwd_fp8")
+    return o, lse
+
+
 def get_status(stream=None) -> int:
     """Wait for the stream; return and clear the device status word."""
     return _lib.load().attn_get_status(_stream_handle(stream))

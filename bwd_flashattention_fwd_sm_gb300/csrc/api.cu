@@ -16,6 +16,7 @@
 
 #include "../../include/gbattn.h"
 #include "common.cuh"
+#include "fp8.h"
 #include "tc_kernels.h"
 
 using namespace gbattn;
@@ -289,6 +290,29 @@ attn_status_t cuda_fail(cudaError_t e, const char* what) {
   return fail(ATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Row length in bytes of the transposed V codes: S rounded up to 16.
+int fp8_vt_ld(int seqlen) { return (seqlen + 15) / 16 * 16; }
+
+attn_status_t check_scale_ptr(const float* ptr, const char* name) {
+  if (!ptr) return fail(ATTN_ERR_INVALID_ARG, "%s is NULL", name);
+  if (reinterpret_cast<uintptr_t>(ptr) & 3u) return fail(ATTN_ERR_INVALID_ARG, "%s is not 4-byte aligned", name);
+  return ATTN_OK;
+}
+
+// The FP8 forward's extra constraints on top of validate_params.
+attn_status_t validate_fp8_params(const attn_params_t* p, Problem* pr) {
+  attn_status_t s = validate_params(p, pr);
+  if (s != ATTN_OK) return s;
+  if (p->dtype != ATTN_BF16)
+    return fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward takes bf16 inputs and writes a bf16 O (dtype must be ATTN_BF16)");
+  if (p->head_dim != 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "head_dim=%d: the FP8 forward has head_dim 128 only", p->head_dim);
+  if (p->cu_seqlens)
+    return fail(ATTN_ERR_UNSUPPORTED, "the FP8 forward takes fixed-length batches only (cu_seqlens must be NULL)");
+  if (!tc_fwd_available()) return fail(ATTN_ERR_UNSUPPORTED, "this build has no tensor-core forward");
+  return ATTN_OK;
+}
+
 }  // namespace
 
 namespace gbattn {
@@ -355,6 +379,77 @@ attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, con
   if (use_tensor_cores(p, false)) e = launch_tc_fwd(kp, sms, st);
   else e = launch_simt_fwd(kp, p->dtype == ATTN_BF16, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  if (g_timing_events[0][1] && (e = cudaEventRecord(g_timing_events[0][1], st)) != cudaSuccess)
+    return cuda_fail(e, "timing event");
+  return ATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// FP8 (e4m3) forward
+// ---------------------------------------------------------------------------
+
+attn_status_t attn_quantize_fp8(const attn_params_t* p, const void* q, const void* k, const void* v, void* q8,
+                                void* k8, void* v8t, float* q_scale, float* k_scale, float* v_scale, void* stream) {
+  Problem pr;
+  attn_status_t s = validate_fp8_params(p, &pr);
+  if (s != ATTN_OK) return s;
+  if (pr.empty) return ATTN_OK;
+  if ((s = check_ptr(q, "q")) || (s = check_ptr(k, "k")) || (s = check_ptr(v, "v")) || (s = check_ptr(q8, "q8")) ||
+      (s = check_ptr(k8, "k8")) || (s = check_ptr(v8t, "v8t")) || (s = check_scale_ptr(q_scale, "q_scale")) ||
+      (s = check_scale_ptr(k_scale, "k_scale")) || (s = check_scale_ptr(v_scale, "v_scale")))
+    return s;
+  Fp8QuantJob jobs[3];
+  jobs[0] = {static_cast<const __nv_bfloat16*>(q), p->q_stride_b, p->q_stride_h, p->q_stride_s,
+             static_cast<uint8_t*>(q8), q_scale, p->heads_q, 0};
+  jobs[1] = {static_cast<const __nv_bfloat16*>(k), p->kv_stride_b, p->kv_stride_h, p->kv_stride_s,
+             static_cast<uint8_t*>(k8), k_scale, p->heads_kv, 0};
+  jobs[2] = {static_cast<const __nv_bfloat16*>(v), p->kv_stride_b, p->kv_stride_h, p->kv_stride_s,
+             static_cast<uint8_t*>(v8t), v_scale, p->heads_kv, 1};
+  cudaError_t e = launch_quant_fp8(jobs, p->batch, p->seqlen, fp8_vt_ld(p->seqlen), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantisation launch");
+  return ATTN_OK;
+}
+
+attn_status_t attn_fwd_fp8(const attn_params_t* p, const void* q8, const void* k8, const void* v8t,
+                           const float* q_scale, const float* k_scale, const float* v_scale, void* o, float* lse,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+  Problem pr;
+  attn_status_t s = validate_fp8_params(p, &pr);
+  if (s != ATTN_OK) return s;
+  if (pr.empty) return ATTN_OK;
+  if ((s = check_ptr(q8, "q8")) || (s = check_ptr(k8, "k8")) || (s = check_ptr(v8t, "v8t")) ||
+      (s = check_scale_ptr(q_scale, "q_scale")) || (s = check_scale_ptr(k_scale, "k_scale")) ||
+      (s = check_scale_ptr(v_scale, "v_scale")) || (s = check_ptr(o, "o")) || (s = check_ptr(lse, "lse")))
+    return s;
+  const Layout L = layout_for(p, pr, false);
+  if ((s = check_workspace(workspace, workspace_bytes, L.total))) return s;
+  int* status = nullptr;
+  int sms = 0;
+  if ((s = device_state(&status, &sms))) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+
+  KParams kp = base_kparams(p, pr);
+  kp.o = o;
+  kp.lse = lse;
+  kp.status = status;
+  kp.units = reinterpret_cast<const Unit*>(ws + L.units);
+  kp.n_units = (int)L.n_units;
+  kp.unit_counter = reinterpret_cast<int*>(ws + L.counter);
+  cudaError_t e = launch_build_worklist(kp, false, L.tile_rows, reinterpret_cast<Unit*>(ws + L.units),
+                                        (int)L.n_units, reinterpret_cast<int*>(ws + L.sched), st);
+  if (e != cudaSuccess) return cuda_fail(e, "work-list launch");
+  Fp8Operands f;
+  f.q8 = static_cast<const uint8_t*>(q8);
+  f.k8 = static_cast<const uint8_t*>(k8);
+  f.v8t = static_cast<const uint8_t*>(v8t);
+  f.qs = q_scale;
+  f.ks = k_scale;
+  f.vs = v_scale;
+  f.ld_t = fp8_vt_ld(p->seqlen);
+  if (g_timing_events[0][0] && (e = cudaEventRecord(g_timing_events[0][0], st)) != cudaSuccess)
+    return cuda_fail(e, "timing event");
+  if ((e = launch_tc_fwd_fp8(kp, sms, st, f)) != cudaSuccess) return cuda_fail(e, "FP8 forward launch");
   if (g_timing_events[0][1] && (e = cudaEventRecord(g_timing_events[0][1], st)) != cudaSuccess)
     return cuda_fail(e, "timing event");
   return ATTN_OK;

@@ -36,6 +36,7 @@
 // drains its copies and tensor-core work, frees tensor memory and returns.
 #include <cuda.h>
 
+#include "fp8.h"
 #include "tc_common.cuh"
 #include "tc_kernels.h"
 #include "tma_host.h"
@@ -57,6 +58,11 @@ struct FwdArgs {
   CUtensorMap tq, tk, tv;
   int q_rows_inner, kv_rows_inner;
   KParams p;
+  // FP8 operands: per-tile scales [batch, heads, n_tiles] of Q, K, V
+  const float* qs;
+  const float* ks;
+  const float* vs;
+  int n_tiles;
 };
 
 struct Smem {
@@ -131,14 +137,56 @@ __device__ __forceinline__ float write_p(const uint32_t (&sr)[128], float c, flo
   return (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
 }
 
+// The FP8 form of write_p: P-hat = exp2(s * c - mu) rounded to e4m3 (mu also
+// carries the V tile's scale ratio, so P-hat stays below 2^8 < 448), four keys
+// per 32-bit column (key 4i + b in byte b), stored 8 columns = 32 keys at a time.
+// Returns the row sum of the float32 P-hat values.
+template <bool kMask>
+__device__ __forceinline__ float write_p8(const uint32_t (&sr)[128], float c, float mu, int thr, bool lo_ok,
+                                          bool hi_ok, uint32_t taddr) {
+  const float2 c2 = make_float2(c, c), nmu2 = make_float2(-mu, -mu);
+  float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t pk[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int k = cc * 32 + 4 * i;
+      const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2, nmu2);
+      const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3])), c2, nmu2);
+      float2 p0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
+      float2 p1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
+      if constexpr (kMask) {
+        const bool half_ok = k < 64 ? lo_ok : hi_ok;  // the four keys share a 64-key half
+        if (!(k < thr && half_ok)) p0.x = 0.f;
+        if (!(k + 1 < thr && half_ok)) p0.y = 0.f;
+        if (!(k + 2 < thr && half_ok)) p1.x = 0.f;
+        if (!(k + 3 < thr && half_ok)) p1.y = 0.f;
+      }
+      rs2[0] = __fadd2_rn(rs2[0], p0);
+      rs2[1] = __fadd2_rn(rs2[1], p1);
+      pk[i] = ptx::pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
+    }
+    ptx::tmem_st8(taddr + cc * 8, pk);
+  }
+  return (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
+}
+
 // D: head dim, 64 or 128 (shared memory is laid out for 128 either way).
-template <bool kSparse, int D>
+// kFp8: e4m3 operands (D = 128): Q and K tiles of 128 rows x 128 bytes, V
+// transposed (128 head-dim rows x 128 keys), both products kind::f8f6f4 with
+// K = 32 per instruction; P rounded to e4m3 into tensor memory; per-tile scales
+// folded into the softmax constant (Q and K) and into P (V, relative to the
+// head's largest V scale, which multiplies O in the epilogue).
+template <bool kSparse, int D, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const KParams& p = a.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Waiter W{sm, p};
+  static_assert(!kFp8 || D == 128, "the FP8 forward has head dim 128");
+  constexpr uint32_t kLoadBytes = kFp8 ? (uint32_t)kTile * 128 : tile_bytes<D>();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -217,9 +265,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         const uint32_t c = n_q_loads[q];
         if (!W.warp(&sm.q_empty[q], ((c & 1) ^ 1))) { ok = false; break; }
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&sm.q_full[q], tile_bytes<D>());
-          tma_tile(sm.q[q], &a.tq, a.q_rows_inner, &sm.q_full[q], map_row(si, q0 + q * kTile), h, si.b,
-                   kHalfTileBytes, D / 64);
+          ptx::mbar_arrive_expect_tx(&sm.q_full[q], kLoadBytes);
+          if constexpr (kFp8)
+            ptx::tma_load_4d(sm.q[q], &a.tq, &sm.q_full[q], 0, q0 + q * kTile, h, si.b);
+          else
+            tma_tile(sm.q[q], &a.tq, a.q_rows_inner, &sm.q_full[q], map_row(si, q0 + q * kTile), h, si.b,
+                     kHalfTileBytes, D / 64);
         }
         last_q_phase[q] = c & 1;
         ++n_q_loads[q];
@@ -233,9 +284,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         const uint32_t ph = (n_k / kStages) & 1;
         if (!W.warp(&sm.k_empty[st], ph ^ 1)) return false;
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&sm.k_full[st], tile_bytes<D>());
-          tma_tile(sm.k[st], &a.tk, a.kv_rows_inner, &sm.k_full[st], map_row(si, kt_ * kTile), g, si.b,
-                   kHalfTileBytes, D / 64);
+          ptx::mbar_arrive_expect_tx(&sm.k_full[st], kLoadBytes);
+          if constexpr (kFp8)
+            ptx::tma_load_4d(sm.k[st], &a.tk, &sm.k_full[st], 0, kt_ * kTile, g, si.b);
+          else
+            tma_tile(sm.k[st], &a.tk, a.kv_rows_inner, &sm.k_full[st], map_row(si, kt_ * kTile), g, si.b,
+                     kHalfTileBytes, D / 64);
         }
         last_k_phase[st] = (int)ph;
         ++n_k;
@@ -246,9 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         const uint32_t ph = (n_v / kStages) & 1;
         if (!W.warp(&sm.v_empty[st], ph ^ 1)) return false;
         if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&sm.v_full[st], tile_bytes<D>());
-          tma_tile(sm.v[st], &a.tv, a.kv_rows_inner, &sm.v_full[st], map_row(si, kt_ * kTile), g, si.b,
-                   kHalfTileBytes, D / 64);
+          ptx::mbar_arrive_expect_tx(&sm.v_full[st], kLoadBytes);
+          if constexpr (kFp8)  // V transposed: keys along x, head dim along y
+            ptx::tma_load_4d(sm.v[st], &a.tv, &sm.v_full[st], kt_ * kTile, 0, g, si.b);
+          else
+            tma_tile(sm.v[st], &a.tv, a.kv_rows_inner, &sm.v_full[st], map_row(si, kt_ * kTile), g, si.b,
+                     kHalfTileBytes, D / 64);
         }
         last_v_phase[st] = (int)ph;
         ++n_v;
@@ -295,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     // warp picks the same lane every time, so each commit covers every product
     // that lane issued before it.
     const int q = warp - 9;
-    constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, false, false);
-    constexpr uint32_t idesc_pv = ptx::idesc_bf16(128, D, false, true);
+    constexpr uint32_t idesc_s = kFp8 ? ptx::idesc_e4m3(128, 128) : ptx::idesc_bf16(128, 128, false, false);
+    constexpr uint32_t idesc_pv = kFp8 ? ptx::idesc_e4m3(128, D) : ptx::idesc_bf16(128, D, false, true);
     const uint32_t q_addr = ptx::smem_u32(sm.q[q]);
     const uint32_t t_s = tmem + q * 128, t_o = tmem + 256 + q * D;
     uint32_t n_units_seen = 0, n_q = 0, n_p = 0, n_o = 0, n_k = 0, n_v = 0;
@@ -331,11 +388,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         }
         const bool last = ++s_issued == n_act;
         if (ptx::elect_one()) {
+          if constexpr (kFp8) {
+            // one 128-byte row per position: four K-steps of 32 bytes
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
-            ptx::mma_ss(t_s, ptx::sdesc_sw128(q_addr + off, 16, 1024), ptx::sdesc_sw128(k_addr + off, 16, 1024),
-                        idesc_s, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::mma_ss_f8(t_s, ptx::sdesc_sw128(q_addr + kk * 32, 16, 1024),
+                             ptx::sdesc_sw128(k_addr + kk * 32, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
+              ptx::mma_ss(t_s, ptx::sdesc_sw128(q_addr + off, 16, 1024), ptx::sdesc_sw128(k_addr + off, 16, 1024),
+                          idesc_s, kk > 0 ? 1u : 0u);
+            }
           }
           ptx::mma_commit(&sm.s_full[q]);
           if (last) ptx::mma_commit(&sm.q_empty[q]);
@@ -391,11 +456,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
           const uint32_t acc0 = pv_issued > 0 ? 1u : 0u;
           const bool last = ++pv_issued == n_act;
           if (ptx::elect_one()) {
+            if constexpr (kFp8) {
+              // B = V^T as (N = head dim, K = keys), keys contiguous: K-major;
+              // A = P, 32 keys per 8 tensor-memory columns
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              // B = V as (N = head dim, K = keys), head dim contiguous: MN-major.
-              const uint64_t bdesc = ptx::sdesc_sw128(v_addr + kk * 2048, kHalfTileBytes, 1024);
-              ptx::mma_ts(t_o, t_s + kk * 8, bdesc, idesc_pv, kk > 0 ? 1u : acc0);
+              for (int kk = 0; kk < 4; ++kk)
+                ptx::mma_ts_f8(t_o, t_s + kk * 8, ptx::sdesc_sw128(v_addr + kk * 32, 16, 1024), idesc_pv,
+                               kk > 0 ? 1u : acc0);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                // B = V as (N = head dim, K = keys), head dim contiguous: MN-major.
+                const uint64_t bdesc = ptx::sdesc_sw128(v_addr + kk * 2048, kHalfTileBytes, 1024);
+                ptx::mma_ts(t_o, t_s + kk * 8, bdesc, idesc_pv, kk > 0 ? 1u : acc0);
+              }
             }
             if (last) ptx::mma_commit(&sm.o_final[q]);
           }
@@ -455,6 +529,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       const int q0 = un.tile * 2 * kTile + q * kTile;  // this tile's first row
       const int qi = q0 + r;
       float m_used = -INFINITY, l = 0.f;
+      // FP8: this Q tile's scale and the KV head's largest V tile scale
+      float sq = 1.f, sv_ref = 1.f;
+      const float *ks_row = nullptr, *vs_row = nullptr;
+      if constexpr (kFp8) {
+        const long long kv_base = ((long long)si.b * p.heads_kv + h / p.group) * a.n_tiles;
+        ks_row = a.ks + kv_base;
+        vs_row = a.vs + kv_base;
+        sq = q0 < si.len ? a.qs[((long long)si.b * p.heads_q + h) * a.n_tiles + q0 / kTile] : 0.f;
+        float mx = 0.f;
+        for (int t2 = lane; t2 < a.n_tiles; t2 += 32) mx = fmaxf(mx, vs_row[t2]);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        sv_ref = mx;
+      }
       int n_done = 0;
       KvTileList2<kSparse> t;
       t.init(p, si.len, un.tile * 2 * kTile);
@@ -462,6 +550,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       while (t.next(kt, bits8)) {
         const int bits = (bits8 >> (4 * q)) & 0xF;
         if (!bits) continue;
+        float sk = 1.f, sv = 1.f;
+        if constexpr (kFp8) {  // read before the wait so that the loads overlap it
+          sk = ks_row[kt];
+          sv = vs_row[kt];
+        }
         if (!W.warp(&sm.s_full[q], n_s & 1)) { ok = false; break; }
         ++n_s;
         ptx::tc_fence_after();
@@ -485,7 +578,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
 #pragma unroll
           for (int k = 0; k < 128; ++k) sr[k] ^= 0x80000000u;
         }
-        const float ca = fabsf(c);
+        const float ca = kFp8 ? fabsf(c) * sq * sk : fabsf(c);
+        // FP8: P-hat = P r with r = sv / sv_ref in (0, 1], as 2^lr in the exponent
+        // (lr >= -64: a tile with r below 2^-64 holds only zero codes or values
+        // under 2^-55 of the head's largest); the row sum takes P-hat / r.
+        float lr = 0.f, inv_r = 1.f;
+        if constexpr (kFp8) {
+          const float rr = sv_ref > 0.f ? sv / sv_ref : 1.f;
+          lr = rr > 0.f ? fmaxf(fast_log2(rr), -64.f) : -64.f;
+          inv_r = fast_exp2(-lr);
+        }
         float e8[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) e8[u] = -INFINITY;
@@ -510,8 +612,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         }
         const float mu = m_used == -INFINITY ? 0.f : m_used;
         // P = exp2(s' |c| - m) as bf16 pairs, written over S_q 8 columns at a time
-        const float rs = need_mask ? write_p<true>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s)
-                                   : write_p<false>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s);
+        float rs;
+        if constexpr (kFp8)
+          rs = (need_mask ? write_p8<true>(sr, ca, mu - lr, thr, lo_ok, hi_ok, tmem + lane_base + col_s)
+                          : write_p8<false>(sr, ca, mu - lr, thr, lo_ok, hi_ok, tmem + lane_base + col_s)) *
+               inv_r;
+        else
+          rs = need_mask ? write_p<true>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s)
+                         : write_p<false>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s);
         // S_q of this tile was issued after the previous P_q V product and its
         // completion covers that product, so O_q is stable here; the next product
         // waits for p_full, so rescaling O_q now (after P is written) is in time.
@@ -540,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         if (!W.warp(&sm.o_final[q], n_o & 1)) { ok = false; break; }
         ptx::tc_fence_after();
       }
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? (kFp8 ? sv_ref / l : 1.f / l) : 0.f;
       __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
       const bool row_ok = qi < si.len;
       __nv_bfloat16* orow = O + (row_ok ? q_off(p, si, h, qi) : 0);
@@ -606,8 +714,37 @@ cudaError_t launch_tc_fwd(const KParams& p, int sms, cudaStream_t st) {
   a.p = p;
   const size_t smem = sizeof(Smem) + 1024;
   const int grid = p.n_units < sms ? p.n_units : sms;
-  auto kernel = p.head_dim == 64 ? (p.mask == kMaskBlock ? k_tc_fwd<true, 64> : k_tc_fwd<false, 64>)
-                                 : (p.mask == kMaskBlock ? k_tc_fwd<true, 128> : k_tc_fwd<false, 128>);
+  auto kernel = p.head_dim == 64
+                    ? (p.mask == kMaskBlock ? k_tc_fwd<true, 64, false> : k_tc_fwd<false, 64, false>)
+                    : (p.mask == kMaskBlock ? k_tc_fwd<true, 128, false> : k_tc_fwd<false, 128, false>);
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_fwd_fp8(const KParams& p, int sms, cudaStream_t st, const Fp8Operands& f) {
+  if (p.n_units == 0) return cudaSuccess;
+  FwdArgs a;
+  TileMap mq, mk, mv;
+  cudaError_t e;
+  const long long S = p.seqlen;
+  // Q and K codes: 128-byte rows, one per position; V codes: one row per head dim, keys along it
+  if ((e = make_byte_map(&mq, f.q8, 128, S, p.heads_q, p.batch, 128)) != cudaSuccess) return e;
+  if ((e = make_byte_map(&mk, f.k8, 128, S, p.heads_kv, p.batch, 128)) != cudaSuccess) return e;
+  if ((e = make_byte_map(&mv, f.v8t, S, 128, p.heads_kv, p.batch, f.ld_t)) != cudaSuccess) return e;
+  a.tq = mq.map;
+  a.tk = mk.map;
+  a.tv = mv.map;
+  a.q_rows_inner = a.kv_rows_inner = 1;
+  a.p = p;
+  a.qs = f.qs;
+  a.ks = f.ks;
+  a.vs = f.vs;
+  a.n_tiles = (int)((S + kTile - 1) / kTile);
+  const size_t smem = sizeof(Smem) + 1024;
+  const int grid = p.n_units < sms ? p.n_units : sms;
+  auto kernel = p.mask == kMaskBlock ? k_tc_fwd<true, 128, true> : k_tc_fwd<false, 128, true>;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kernel<<<grid, kThreads, smem, st>>>(a);

@@ -66,6 +66,23 @@ cudaError_t make_tile_map(TileMap* out, const void* base, const KParams& p, bool
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t make_byte_map(TileMap* out, const void* base, long long x_extent, long long rows, long long heads,
+                          long long batch, long long row_bytes) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  if (x_extent < 1 || rows < 1 || heads < 1 || batch < 1 || row_bytes % 16) return cudaErrorInvalidValue;
+  out->rows_inner = 1;
+  cuuint64_t dims[4] = {(cuuint64_t)x_extent, (cuuint64_t)rows, (cuuint64_t)heads, (cuuint64_t)batch};
+  cuuint64_t strides[3] = {(cuuint64_t)row_bytes, (cuuint64_t)(row_bytes * rows),
+                           (cuuint64_t)(row_bytes * rows * heads)};
+  cuuint32_t box[4] = {128, 128, 1, 1}, estr[4] = {1, 1, 1, 1};
+  std::memset(&out->map, 0, sizeof(out->map));
+  CUresult r = enc(&out->map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t make_acc_map(TileMap* out, float* base, const KParams& p, int box_rows) {
   EncodeFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;

@@ -22,6 +22,14 @@ struct TileMap {
 // `base`, with boxes of `box_rows` positions x 64 columns.
 cudaError_t make_tile_map(TileMap* out, const void* base, const KParams& p, bool kv, int box_rows = 128);
 
+// Map of a 4-D byte tensor (x, row, head, batch) with x contiguous, `row_bytes`
+// between rows and rows packed per head and heads per batch entry, for TMA loads
+// of 128 x 128-byte boxes with the 128-byte swizzle (the FP8 operands: x = head
+// dim for Q and K codes, x = key for the transposed V codes).  x and rows past
+// the extents read as zero.
+cudaError_t make_byte_map(TileMap* out, const void* base, long long x_extent, long long rows, long long heads,
+                          long long batch, long long row_bytes);
+
 // Map of the float32 dQ accumulator (rows laid out like a contiguous q) for
 // TMA reduce-adds of 64-row x 128-column tiles (no swizzle, 512-byte rows).
 //   fixed length: dims (d, position, head, batch); variable: (d, head, token, 1).

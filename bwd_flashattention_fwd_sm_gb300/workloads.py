@@ -165,6 +165,18 @@ def make_inputs(wl: Workload) -> dict:
     return out
 
 
+def tile_spread(x: torch.Tensor, seed: int, spread: int = 3, tile: int = 128) -> torch.Tensor:
+    """x [..., S, D] with each `tile`-row block along S multiplied by 2^U{-spread..spread}
+    (seeded), rounded back to x's dtype: inputs whose per-tile magnitudes differ, so
+    that per-tile scales differ too."""
+    g = torch.Generator().manual_seed(seed)
+    S = x.shape[-2]
+    nt = (S + tile - 1) // tile
+    e = torch.randint(-spread, spread + 1, tuple(x.shape[:-2]) + (nt,), generator=g).float()
+    f = torch.pow(2.0, e).repeat_interleave(tile, dim=-1)[..., :S, None]
+    return (x.float() * f).to(x.dtype)
+
+
 def unmasked_pairs(wl: Workload, block_mask: dict | None = None) -> int:
     """Number of allowed (query, key) pairs summed over batch entries, for ONE head.
 

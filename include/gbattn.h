@@ -171,6 +171,53 @@ attn_status_t attn_bwd_deterministic(const attn_params_t* p, const void* q, cons
                                      void* dv, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * FP8 (e4m3) forward.  Newer accelerators multiply 8-bit floats so that each
+ * transfer and each matrix instruction handles more numbers, while sums are
+ * kept in a wider format so that small terms are not lost (smzdm contest
+ * article, closing section on precision).  The pages fix no format or scaling;
+ * this library's choices:
+ *
+ * Format: E4M3 of the OCP 8-bit floating-point specification without
+ * infinities (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; largest
+ * finite value 448, smallest subnormal 2^-9).
+ *
+ * attn_quantize_fp8: for each 128-row tile (positions r0 .. r0 + 127, the last
+ * one possibly short) of each head of q, k and v (bf16, laid out and strided
+ * as for attn_fwd), amax = max |x| over the tile; scale = amax / 448 and
+ * code = e4m3(x * (448 / amax)), the division and the product rounded to
+ * float32, the conversion rounded to nearest even and saturated at +-448; an
+ * all-zero tile gets scale 0 and zero codes.  A code stands for
+ * e4m3_value(code) * scale.  Outputs (contiguous, caller-owned device memory):
+ *   q8  [batch, heads_q, seqlen, 128] bytes;  k8 [batch, heads_kv, seqlen, 128] bytes;
+ *   v8t [batch, heads_kv, 128, ld] bytes with ld = seqlen rounded up to 16: V's
+ *       codes transposed, keys along each row (positions seqlen .. ld-1 unwritten);
+ *   q_scale [batch, heads_q, n_tiles], k_scale and v_scale [batch, heads_kv, n_tiles]
+ *       float32, n_tiles = ceil(seqlen / 128).
+ * Device-memory bound: 2 bytes read and 1 written per element.
+ *
+ * attn_fwd_fp8: O and LSE of attention on the dequantised q, k, v (the
+ * definitions at the top of this file, every mask kind, GQA) with both products
+ * on e4m3 operands and float32 accumulation.  The Q and K tile scales fold into
+ * the score scale; each V tile's scale, relative to the largest V tile scale of
+ * its KV head, folds into P, which is rounded to e4m3 before the P V product
+ * (that rounding is the one approximation beyond float32 rounding: it moves
+ * each output element by at most sum_j (2^-4 P_ij + min(P_ij, 2^-10 / (l_i r_j)))
+ * |v_jd|, with l_i the row's sum of exp(s_ij - max_j s_ij) and r_j the V scale
+ * ratio).  LSE is computed from the unrounded P.  o: bf16, laid out by the q
+ * strides as for attn_fwd; lse: float32 [batch, heads_q, seqlen]; workspace:
+ * attn_fwd_workspace_size(p) bytes.
+ *
+ * Both calls: p->dtype must be ATTN_BF16, p->head_dim 128 and p->cu_seqlens NULL
+ * (else ATTN_ERR_UNSUPPORTED); byte tensors 16-byte aligned, scale arrays 4-byte
+ * aligned; inputs must be finite.  Errors and asynchrony as for attn_fwd.
+ */
+attn_status_t attn_quantize_fp8(const attn_params_t* p, const void* q, const void* k, const void* v, void* q8,
+                                void* k8, void* v8t, float* q_scale, float* k_scale, float* v_scale, void* stream);
+attn_status_t attn_fwd_fp8(const attn_params_t* p, const void* q8, const void* k8, const void* v8t,
+                           const float* q_scale, const float* k_scale, const float* v_scale, void* o, float* lse,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Backward pass that allocates nothing.  The pages have no counterpart to this
  * entry point: it exists for callers that cannot allocate device memory and so
  * cannot pass a workspace -- code running while a stream is captured into a CUDA

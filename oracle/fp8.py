@@ -127,17 +127,36 @@ def dequantize(codes, scales, tile: int = TILE):
     return vals * rep[..., None]
 
 
-def p_rounding_bound(q, k, v, v_codes, v_scales, *, scale, causal=False, block_mask=None, tile: int = TILE):
+def _allowed(q_pos, n_keys, causal, block_mask):
+    """keep(i, j) for query positions q_pos and keys 0 .. n_keys - 1."""
+    q_pos = np.asarray(q_pos)
+    j = np.arange(n_keys)
+    if block_mask is not None:
+        rp, ci = block_mask["row_ptr"], block_mask["col_idx"]
+        bs = int(block_mask.get("block_q", 64))
+        listed = np.zeros((len(rp) - 1, (n_keys + bs - 1) // bs), dtype=bool)
+        for r in range(len(rp) - 1):
+            listed[r, ci[rp[r]:rp[r + 1]]] = True
+        allowed = listed[q_pos[:, None] // bs, j[None, :] // bs]
+        if int(block_mask.get("causal_in_block", 1)):
+            allowed &= j[None, :] <= q_pos[:, None]
+        return allowed
+    if causal:
+        return j[None, :] <= q_pos[:, None]
+    return np.ones((len(q_pos), n_keys), dtype=bool)
+
+
+def p_rounding_bound(q, k, v, v_scales, *, scale, causal=False, block_mask=None, q_pos=None, tile: int = TILE):
     """Per-element bound on |O_gpu - O_ref| from rounding P to e4m3 (float64).
 
-    q [B, Hq, S, D], k, v [B, Hkv, S, D] are the dequantised values; v_codes and
-    v_scales the V tiles' codes and scales.  On the GPU, each key tile j of a KV
-    head is folded into P as r_j = s_j / s_ref (s_ref the head's largest V tile
-    scale), and p * r_j is rounded to e4m3, where p = exp(s - m_used) with a
-    running maximum m_used at most 8 binades below the final maximum.  Rounding
-    changes a value y by at most 2^-4 y (normal range) or, below 2^-6, by at
-    most min(y, 2^-10); carried to the normalised output that gives, per
-    element,
+    q [B, Hq, Sq, D] (the query rows at positions q_pos, default 0 .. Sq - 1),
+    k, v [B, Hkv, S, D] are the dequantised values and v_scales the V tiles'
+    scales.  On the GPU, each key tile j of a KV head is folded into P as
+    r_j = s_j / s_ref (s_ref the head's largest V tile scale), and p * r_j is
+    rounded to e4m3, where p = exp(s - m_used) with a running maximum m_used at
+    most 8 binades below the final maximum.  Rounding changes a value y by at
+    most 2^-4 y (normal range) or, below 2^-6, by at most min(y, 2^-10); carried
+    to the normalised output that gives, per element,
         |dO_id| <= sum_j (2^-4 P_ij + min(P_ij, 2^-10 / (l_i r_j))) |v_jd|
     with P the exact probabilities and l_i = sum_j exp(s_ij - max_j s_ij).
     Returns (terms, A) where terms is that bound and A = sum_j P_ij |v_jd|.
@@ -145,22 +164,11 @@ def p_rounding_bound(q, k, v, v_codes, v_scales, *, scale, causal=False, block_m
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
-    B, Hq, S, D = q.shape
-    Hkv = k.shape[1]
-    G = Hq // Hkv
+    B, Hq, Sq, D = q.shape
+    S = k.shape[2]
+    G = Hq // k.shape[1]
     vs = np.asarray(v_scales, dtype=np.float64)
-    allowed = np.ones((S, S), dtype=bool)
-    if block_mask is not None:
-        allowed = np.zeros((S, S), dtype=bool)
-        rp, ci = block_mask["row_ptr"], block_mask["col_idx"]
-        bs = int(block_mask.get("block_q", 64))
-        for r in range(len(rp) - 1):
-            for c in ci[rp[r]:rp[r + 1]]:
-                allowed[r * bs:(r + 1) * bs, c * bs:(c + 1) * bs] = True
-        if int(block_mask.get("causal_in_block", 1)):
-            allowed &= np.tril(np.ones((S, S), dtype=bool))
-    elif causal:
-        allowed = np.tril(np.ones((S, S), dtype=bool))
+    allowed = _allowed(np.arange(Sq) if q_pos is None else q_pos, S, causal, block_mask)
     terms = np.zeros_like(q)
     A = np.zeros_like(q)
     for b in range(B):

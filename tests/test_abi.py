@@ -23,7 +23,7 @@ def declared_functions():
     names = set()
     for path in HEADERS:
         text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
-        names |= set(re.findall(r"\b((?:attn|ln)_[a-z_]+)\s*\(", text))
+        names |= set(re.findall(r"\b((?:attn|ln)_[a-z0-9_]+)\s*\(", text))
     return sorted(names)
 
 
@@ -227,3 +227,34 @@ def test_row_count_limit(lib):
     p = params(B=1 << 12, Hq=1 << 10, Hkv=1 << 10, S=1 << 10)
     assert fwd(lib, p) == _lib.ATTN_ERR_UNSUPPORTED
     assert b"2^31" in lib.attn_last_error()
+
+
+def fp8_fwd(lib, p, scales=FAKE, ws_bytes=1 << 40):
+    return lib.attn_fwd_fp8(ctypes.byref(p), FAKE, FAKE, FAKE, scales, FAKE, FAKE, FAKE, FAKE, FAKE, ws_bytes, None)
+
+
+def fp8_quant(lib, p, scales=FAKE):
+    return lib.attn_quantize_fp8(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, scales, FAKE, FAKE, None)
+
+
+def test_fp8_validation(lib):
+    """The FP8 entry points: bf16, head_dim 128, fixed length; checked before any device work."""
+    for mask in (_lib.ATTN_MASK_NONE, _lib.ATTN_MASK_CAUSAL):
+        assert fp8_fwd(lib, params(mask=mask)) == _lib.ATTN_ERR_CUDA  # valid: fails only for want of a GPU
+        assert fp8_quant(lib, params(mask=mask)) == _lib.ATTN_ERR_CUDA
+    p = params(D=64)
+    p.q_stride_b, p.q_stride_h, p.q_stride_s = 4 * 256 * 64, 256 * 64, 64
+    p.kv_stride_b, p.kv_stride_h, p.kv_stride_s = 2 * 256 * 64, 256 * 64, 64
+    assert fp8_fwd(lib, p) == _lib.ATTN_ERR_UNSUPPORTED and b"head_dim" in lib.attn_last_error()
+    assert fp8_quant(lib, p) == _lib.ATTN_ERR_UNSUPPORTED
+    assert fp8_fwd(lib, params(dtype=_lib.ATTN_F32)) == _lib.ATTN_ERR_UNSUPPORTED
+    cu = np.array([0, 100, 256], dtype=np.int32)
+    pv = params(S=256)
+    pv.cu_seqlens = FAKE
+    pv.cu_seqlens_host = cu.ctypes.data
+    pv.n_seqs = 2
+    assert fp8_fwd(lib, pv) == _lib.ATTN_ERR_UNSUPPORTED and b"fixed-length" in lib.attn_last_error()
+    assert fp8_fwd(lib, params(), scales=FAKE + 2) == _lib.ATTN_ERR_INVALID_ARG
+    assert fp8_quant(lib, params(), scales=0) == _lib.ATTN_ERR_INVALID_ARG
+    assert fp8_fwd(lib, params(), ws_bytes=16) == _lib.ATTN_ERR_WORKSPACE
+    assert fp8_fwd(lib, params(B=0)) == _lib.ATTN_OK and fp8_quant(lib, params(S=0)) == _lib.ATTN_OK
