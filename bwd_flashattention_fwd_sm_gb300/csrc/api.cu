@@ -83,10 +83,13 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 // Which kernel family serves these parameters: the tensor-core kernels for bf16
-// with head_dim 64 or 128, the float32-arithmetic kernels for float32 I/O.
+// with head_dim 64 or 128 (and the forward at 256), the float32-arithmetic
+// kernels for float32 I/O and for the bf16 backward at head_dim 256 (its dK and
+// dV accumulators for a 128-key tile would fill all of tensor memory).
 bool use_tensor_cores(const attn_params_t* p, bool backward) {
   const bool avail = backward ? tc_bwd_available() : tc_fwd_available();
-  return avail && p->dtype == ATTN_BF16 && (p->head_dim == 128 || p->head_dim == 64);
+  return avail && p->dtype == ATTN_BF16 &&
+         (p->head_dim == 128 || p->head_dim == 64 || (!backward && p->head_dim == 256));
 }
 
 struct Problem {
@@ -108,8 +111,8 @@ attn_status_t validate_params(const attn_params_t* p, Problem* pr) {
     return fail(ATTN_ERR_INVALID_ARG, "heads_q=%d and heads_kv=%d must be positive", p->heads_q, p->heads_kv);
   if (p->heads_q % p->heads_kv)
     return fail(ATTN_ERR_INVALID_ARG, "heads_q=%d is not a multiple of heads_kv=%d", p->heads_q, p->heads_kv);
-  if (p->head_dim != 64 && p->head_dim != 128)
-    return fail(ATTN_ERR_UNSUPPORTED, "head_dim=%d: only 64 and 128 are implemented", p->head_dim);
+  if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256)
+    return fail(ATTN_ERR_UNSUPPORTED, "head_dim=%d: only 64, 128 and 256 are implemented", p->head_dim);
   if (!std::isfinite(p->scale)) return fail(ATTN_ERR_INVALID_ARG, "scale is not finite");
   if (p->seqlen < 0) return fail(ATTN_ERR_INVALID_ARG, "seqlen=%d is negative", p->seqlen);
   if (p->seqlen > (1 << 30)) return fail(ATTN_ERR_UNSUPPORTED, "seqlen=%d exceeds 2^30", p->seqlen);
@@ -235,8 +238,9 @@ Layout layout_for(const attn_params_t* p, const Problem& pr, bool backward) {
   Layout L;
   std::memset(&L, 0, sizeof(L));
   // tensor cores: forward units are 256 query rows (two 128-row tiles sharing
-  // each K/V tile), backward units 128 keys; float32 path: 64 rows
-  L.tile_rows = use_tensor_cores(p, backward) ? (backward ? 128 : 256) : 64;
+  // each K/V tile; one 128-row tile at head_dim 256), backward units 128 keys;
+  // float32 path: 64 rows
+  L.tile_rows = use_tensor_cores(p, backward) ? (backward ? 128 : (p->head_dim == 256 ? 128 : 256)) : 64;
   KParams k = base_kparams(p, pr);
   L.n_units = count_units(k, p->cu_seqlens_host, backward, L.tile_rows);
   size_t off = 0;

@@ -19,9 +19,9 @@ namespace gbattn {
 
 namespace {
 
-// Loads N contiguous elements of T starting at ptr (N * sizeof(T) in {4, 8, 16} bytes).
+// Loads N contiguous elements of T starting at ptr (N * sizeof(T) in {4, 8, 16} bytes) into out[0, N).
 template <class T, int N>
-__device__ __forceinline__ void load_vec(const T* ptr, float (&out)[N]) {
+__device__ __forceinline__ void load_vec(const T* ptr, float* out) {
   constexpr int kBytes = N * (int)sizeof(T);
   static_assert(kBytes == 4 || kBytes == 8 || kBytes == 16, "vector width");
   union {
@@ -38,7 +38,7 @@ __device__ __forceinline__ void load_vec(const T* ptr, float (&out)[N]) {
 }
 
 template <class T, int N>
-__device__ __forceinline__ void store_vec(T* ptr, const float (&in)[N]) {
+__device__ __forceinline__ void store_vec(T* ptr, const float* in) {
   constexpr int kBytes = N * (int)sizeof(T);
   union {
     uint4 u4;
@@ -88,18 +88,20 @@ __device__ __forceinline__ RowRef row_ref(const KParams& p, long long r) {
 // per SM.
 constexpr int kRows = 4;
 
-// Preprocess with 16-byte loads: L = D / E lanes cover one row (E elements of
-// 16 bytes each), so one load instruction covers 32 / L rows; a warp takes
-// kPreRows rows per iteration, all loads issued before use.
+// Preprocess with 16-byte loads: L = min(32, D / E) lanes cover one row, each
+// with NV vectors of E elements (16 bytes), so one load instruction covers
+// 32 / L rows; a warp takes kPreRows rows per iteration, all loads issued
+// before use.
 constexpr int kPreRows = 8;
 
 template <class T, int D>
 __global__ void __launch_bounds__(256) k_bwd_preprocess(KParams p, long long n_rows) {
-  constexpr int E = 16 / (int)sizeof(T);   // elements per 16-byte load
-  constexpr int L = D / E;                 // lanes per row
+  constexpr int E0 = 16 / (int)sizeof(T);  // elements per 16-byte load
+  constexpr int L = D / E0 < 32 ? D / E0 : 32;  // lanes per row
+  constexpr int E = D / L;                 // elements per lane (E / E0 loads)
   constexpr int RP = 32 / L;               // rows per load instruction
   constexpr int NL = kPreRows / RP;        // load instructions per tensor per iteration
-  static_assert(L <= 32 && 32 % L == 0 && kPreRows % RP == 0, "row geometry");
+  static_assert(L <= 32 && 32 % L == 0 && kPreRows % RP == 0 && E % E0 == 0, "row geometry");
   const int lane = threadIdx.x & 31;
   const int sub = lane % L, part = lane / L;
   const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -114,8 +116,11 @@ __global__ void __launch_bounds__(256) k_bwd_preprocess(KParams p, long long n_r
       const long long r = r0 + j * RP + part;
       if (r < n_rows) {
         x[j] = row_ref(p, r);
-        load_vec<T, E>(o + x[j].q + sub * E, a[j]);
-        load_vec<T, E>(dO + x[j].q + sub * E, b[j]);
+#pragma unroll
+        for (int v = 0; v < E / E0; ++v) {
+          load_vec<T, E0>(o + x[j].q + (sub + v * L) * E0, a[j] + v * E0);
+          load_vec<T, E0>(dO + x[j].q + (sub + v * L) * E0, b[j] + v * E0);
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < E; ++i) a[j][i] = b[j][i] = 0.f;
@@ -132,14 +137,18 @@ __global__ void __launch_bounds__(256) k_bwd_preprocess(KParams p, long long n_r
       if (sub == 0 && r < n_rows) p.delta[x[j].lse] = s;
     }
     if (p.dq_accum) {  // no accumulator in the deterministic (query-stationary dQ) mode
-      // zero the rows' float32 accumulator: D / 4 lanes of 16 bytes per row
-      constexpr int LZ = D / 4, RZ = 32 / LZ;
+      // zero the rows' float32 accumulator: LZ lanes of 16 bytes per row, NZ stores each
+      constexpr int LZ = D / 4 < 32 ? D / 4 : 32, NZ = D / 4 / LZ, RZ = 32 / LZ;
       const int subz = lane % LZ, partz = lane / LZ;
 #pragma unroll
       for (int j = 0; j < kPreRows / RZ; ++j) {
         const long long r = r0 + j * RZ + partz;
         // the accumulator is contiguous over flat rows: row r starts at r * D
-        if (r < n_rows) *reinterpret_cast<float4*>(p.dq_accum + r * D + subz * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < n_rows) {
+#pragma unroll
+          for (int z = 0; z < NZ; ++z)
+            *reinterpret_cast<float4*>(p.dq_accum + r * D + (subz + z * LZ) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
     }
   }
@@ -152,9 +161,9 @@ constexpr int kCvtRows = 8;
 
 template <class T, int D>
 __global__ void __launch_bounds__(256) k_dq_convert(KParams p, long long n_rows) {
-  constexpr int E = 16 / (int)sizeof(T);
-  constexpr int L = D / E, RP = 32 / L, NL = kCvtRows / RP;
-  static_assert(L <= 32 && 32 % L == 0 && kCvtRows % RP == 0 && E % 4 == 0, "row geometry");
+  constexpr int E0 = 16 / (int)sizeof(T);
+  constexpr int L = D / E0 < 32 ? D / E0 : 32, E = D / L, RP = 32 / L, NL = kCvtRows / RP;
+  static_assert(L <= 32 && 32 % L == 0 && kCvtRows % RP == 0 && E % E0 == 0 && E0 % 4 == 0, "row geometry");
   const int lane = threadIdx.x & 31;
   const int sub = lane % L, part = lane / L;
   const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -168,11 +177,15 @@ __global__ void __launch_bounds__(256) k_dq_convert(KParams p, long long n_rows)
       const long long r = r0 + j * RP + part;
       if (r < n_rows) {
         x[j] = row_ref(p, r);
-        const float4* src = reinterpret_cast<const float4*>(p.dq_accum + x[j].acc + sub * E);
 #pragma unroll
-        for (int v = 0; v < E / 4; ++v) {
-          const float4 f = __ldcs(src + v);
-          a[j][4 * v] = f.x; a[j][4 * v + 1] = f.y; a[j][4 * v + 2] = f.z; a[j][4 * v + 3] = f.w;
+        for (int w = 0; w < E / E0; ++w) {
+          const float4* src = reinterpret_cast<const float4*>(p.dq_accum + x[j].acc + (sub + w * L) * E0);
+#pragma unroll
+          for (int v = 0; v < E0 / 4; ++v) {
+            const float4 f = __ldcs(src + v);
+            float* d = a[j] + w * E0 + 4 * v;
+            d[0] = f.x; d[1] = f.y; d[2] = f.z; d[3] = f.w;
+          }
         }
       }
     }
@@ -182,7 +195,8 @@ __global__ void __launch_bounds__(256) k_dq_convert(KParams p, long long n_rows)
       if (r >= n_rows) continue;
 #pragma unroll
       for (int i = 0; i < E; ++i) a[j][i] *= p.scale;
-      store_vec<T, E>(dq + x[j].q + sub * E, a[j]);
+#pragma unroll
+      for (int w = 0; w < E / E0; ++w) store_vec<T, E0>(dq + x[j].q + (sub + w * L) * E0, a[j] + w * E0);
     }
   }
 }
@@ -208,10 +222,12 @@ cudaError_t launch_bwd_preprocess(const KParams& p, bool bf16, cudaStream_t st) 
   if (rows == 0) return cudaSuccess;
   const int grid = grid_for(rows);
   if (bf16) {
-    if (p.head_dim == 128) k_bwd_preprocess<__nv_bfloat16, 128><<<grid, 256, 0, st>>>(p, rows);
+    if (p.head_dim == 256) k_bwd_preprocess<__nv_bfloat16, 256><<<grid, 256, 0, st>>>(p, rows);
+    else if (p.head_dim == 128) k_bwd_preprocess<__nv_bfloat16, 128><<<grid, 256, 0, st>>>(p, rows);
     else k_bwd_preprocess<__nv_bfloat16, 64><<<grid, 256, 0, st>>>(p, rows);
   } else {
-    if (p.head_dim == 128) k_bwd_preprocess<float, 128><<<grid, 256, 0, st>>>(p, rows);
+    if (p.head_dim == 256) k_bwd_preprocess<float, 256><<<grid, 256, 0, st>>>(p, rows);
+    else if (p.head_dim == 128) k_bwd_preprocess<float, 128><<<grid, 256, 0, st>>>(p, rows);
     else k_bwd_preprocess<float, 64><<<grid, 256, 0, st>>>(p, rows);
   }
   return cudaGetLastError();
@@ -222,10 +238,12 @@ cudaError_t launch_dq_convert(const KParams& p, bool bf16, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   const int grid = grid_for(rows);
   if (bf16) {
-    if (p.head_dim == 128) k_dq_convert<__nv_bfloat16, 128><<<grid, 256, 0, st>>>(p, rows);
+    if (p.head_dim == 256) k_dq_convert<__nv_bfloat16, 256><<<grid, 256, 0, st>>>(p, rows);
+    else if (p.head_dim == 128) k_dq_convert<__nv_bfloat16, 128><<<grid, 256, 0, st>>>(p, rows);
     else k_dq_convert<__nv_bfloat16, 64><<<grid, 256, 0, st>>>(p, rows);
   } else {
-    if (p.head_dim == 128) k_dq_convert<float, 128><<<grid, 256, 0, st>>>(p, rows);
+    if (p.head_dim == 256) k_dq_convert<float, 256><<<grid, 256, 0, st>>>(p, rows);
+    else if (p.head_dim == 128) k_dq_convert<float, 128><<<grid, 256, 0, st>>>(p, rows);
     else k_dq_convert<float, 64><<<grid, 256, 0, st>>>(p, rows);
   }
   return cudaGetLastError();

@@ -155,7 +155,7 @@ cudaError_t launch_dq_convert(const KParams& p, bool bf16, cudaStream_t st);
 // returns (a check of the device-side timeout path).
 cudaError_t launch_wait_probe(int* status, unsigned long long limit_ns, cudaStream_t st);
 
-// float32-arithmetic SIMT kernels (any dtype, D in {64, 128}).
+// float32-arithmetic SIMT kernels (any dtype, D in {64, 128, 256}).
 cudaError_t launch_simt_fwd(const KParams& p, bool bf16, cudaStream_t st);
 cudaError_t launch_simt_bwd(const KParams& p, bool bf16, cudaStream_t st);
 

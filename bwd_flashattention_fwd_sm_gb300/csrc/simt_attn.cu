@@ -313,6 +313,162 @@ __global__ void __launch_bounds__(kThreads) k_simt_bwd(KParams p) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Backward at head dim 256.  The layout above would hold K, V, dK and dV rows in
+// registers (4 x 64 per thread), more than a thread has, so here K and V stay
+// in shared memory (rows padded to 260 floats so the eight key rows a warp
+// reads fall in different banks) and only dK and dV are in registers; query
+// rows are staged 32 at a time.  Thread (j = tid/4, part = tid%4) still owns key
+// row j and columns 4t + part.
+// ---------------------------------------------------------------------------
+constexpr int kQStep256 = 32;
+
+template <class T>
+__global__ void __launch_bounds__(kThreads) k_simt_bwd256(KParams p) {
+  constexpr int D = 256, NT = D / 4, KS = D + 4, SS = kRows + 1;
+  extern __shared__ float smem[];
+  float* Ks = smem;                    // [64][260]
+  float* Vs = Ks + kRows * KS;         // [64][260]
+  float* Qs = Vs + kRows * KS;         // [32][256]
+  float* dOs = Qs + kQStep256 * D;     // [32][256]
+  float* dSs = dOs + kQStep256 * D;    // [32 q][65]
+  float* lse2 = dSs + kQStep256 * SS;  // [32]
+  float* dlt = lse2 + kQStep256;       // [32]
+
+  const Unit u = p.units[blockIdx.x];
+  const SeqInfo si = seq_info(p, u.seq);
+  const int g = u.head;
+  const int k0 = u.tile * kRows;
+  if (k0 >= si.len) return;
+  const int tid = threadIdx.x, j = tid >> 2, part = tid & 3;
+  const int warp = tid >> 5, lane = tid & 31;
+  const T* Q = static_cast<const T*>(p.q);
+  const T* K = static_cast<const T*>(p.k);
+  const T* V = static_cast<const T*>(p.v);
+  const T* dO = static_cast<const T*>(p.dout);
+
+  for (int r = warp; r < kRows; r += kThreads / 32) {
+    const bool ok = k0 + r < si.len;
+    const long long off = ok ? kv_off(p, si, g, k0 + r) : 0;
+    for (int d = lane; d < D; d += 32) {
+      Ks[r * KS + d] = ok ? to_f32(K[off + d]) : 0.f;
+      Vs[r * KS + d] = ok ? to_f32(V[off + d]) : 0.f;
+    }
+  }
+  const bool kvalid = k0 + j < si.len;
+  float dk[NT], dv[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) dk[t] = dv[t] = 0.f;
+
+  const int nqb_seq = (si.len + kCols - 1) / kCols;
+  const int kblk = u.tile;
+  int qb_begin = 0, qb_count = nqb_seq, e0 = 0;
+  if (p.mask == kMaskCausal) {
+    qb_begin = kblk;
+    qb_count = nqb_seq - kblk;
+  } else if (p.mask == kMaskBlock) {
+    e0 = p.csc_ptr[kblk];
+    qb_count = p.csc_ptr[kblk + 1] - e0;
+  }
+  const bool elem_causal = p.mask == kMaskCausal || (p.mask == kMaskBlock && p.causal_in_block);
+  const float* krow = Ks + j * KS;
+  const float* vrow = Vs + j * KS;
+
+  for (int hh = 0; hh < p.group; ++hh) {
+    const int h = g * p.group + hh;
+    for (int it = 0; it < qb_count; ++it) {
+      const int qb = p.mask == kMaskBlock ? p.csc_idx[e0 + it] : qb_begin + it;
+      for (int half = 0; half < kCols / kQStep256; ++half) {
+        const int q0 = qb * kCols + half * kQStep256;
+        if (q0 >= si.len) continue;
+        __syncthreads();  // previous step done with Qs, dOs, dSs (and K, V written)
+        for (int r = warp; r < kQStep256; r += kThreads / 32) {
+          const bool ok = q0 + r < si.len;
+          const long long off = ok ? q_off(p, si, h, q0 + r) : 0;
+          for (int d = lane; d < D; d += 32) {
+            Qs[r * D + d] = ok ? to_f32(Q[off + d]) : 0.f;
+            dOs[r * D + d] = ok ? to_f32(dO[off + d]) : 0.f;
+          }
+        }
+        if (tid < kQStep256) {
+          const bool ok = q0 + tid < si.len;
+          const long long ri = ok ? row_index(p, si, h, q0 + tid) : 0;
+          const float L = ok ? p.lse[ri] : -INFINITY;
+          lse2[tid] = L * 1.4426950408889634f;
+          dlt[tid] = ok ? p.delta[ri] : 0.f;
+        }
+        __syncthreads();
+
+        for (int i = 0; i < kQStep256; ++i) {
+          const float* qi = Qs + i * D;
+          const float* doi = dOs + i * D;
+          float s = 0.f, dp = 0.f;
+#pragma unroll 16
+          for (int t = 0; t < NT; ++t) {
+            s = fmaf(qi[4 * t + part], krow[4 * t + part], s);
+            dp = fmaf(doi[4 * t + part], vrow[4 * t + part], dp);
+          }
+          s += __shfl_xor_sync(0xffffffffu, s, 1);
+          s += __shfl_xor_sync(0xffffffffu, s, 2);
+          dp += __shfl_xor_sync(0xffffffffu, dp, 1);
+          dp += __shfl_xor_sync(0xffffffffu, dp, 2);
+          const int ii = q0 + i, jj = k0 + j;
+          bool keep = kvalid && ii < si.len && lse2[i] != -INFINITY;
+          if (elem_causal) keep = keep && jj <= ii;
+          const float pij = keep ? exp2f(s * p.scale_log2 - lse2[i]) : 0.f;
+          const float ds = pij * (dp - dlt[i]);
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            dv[t] = fmaf(pij, doi[4 * t + part], dv[t]);
+            dk[t] = fmaf(ds, qi[4 * t + part], dk[t]);
+          }
+          if (part == 0) dSs[i * SS + j] = ds;
+        }
+        __syncthreads();
+
+        // dQ rows of this step: row i = tid / 8, columns 8t + sub
+        {
+          const int i = tid >> 3, sub = tid & 7;
+          if (q0 + i < si.len) {
+            float a[D / 8];
+#pragma unroll
+            for (int t = 0; t < D / 8; ++t) a[t] = 0.f;
+            for (int jj = 0; jj < kRows; ++jj) {
+              const float dsv = dSs[i * SS + jj];
+#pragma unroll
+              for (int t = 0; t < D / 8; ++t) a[t] = fmaf(dsv, Ks[jj * KS + 8 * t + sub], a[t]);
+            }
+            float* dst = p.dq_accum + dqacc_off(p, si, h, q0 + i);
+#pragma unroll
+            for (int t = 0; t < D / 8; ++t) atomicAdd(dst + 8 * t + sub, a[t]);
+          }
+        }
+      }
+    }
+  }
+
+  if (kvalid) {
+    T* dK = static_cast<T*>(p.dk);
+    T* dV = static_cast<T*>(p.dv);
+    const long long off = kv_off(p, si, g, k0 + j);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      dK[off + 4 * t + part] = from_f32<T>(dk[t] * p.scale);
+      dV[off + 4 * t + part] = from_f32<T>(dv[t]);
+    }
+  }
+}
+
+template <class T>
+cudaError_t launch_bwd256_t(const KParams& p, cudaStream_t st) {
+  constexpr size_t smem =
+      sizeof(float) * (2 * kRows * (256 + 4) + 2 * kQStep256 * 256 + kQStep256 * (kRows + 1) + 2 * kQStep256);
+  cudaError_t e = cudaFuncSetAttribute(k_simt_bwd256<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k_simt_bwd256<T><<<p.n_units, kThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
 template <class T, int D>
 cudaError_t launch_fwd_t(const KParams& p, cudaStream_t st) {
   constexpr size_t smem = sizeof(float) * (kRows * D + kCols * (D + 1) + kCols * D + 8 * 8 * kCols);
@@ -337,13 +493,17 @@ cudaError_t launch_bwd_t(const KParams& p, cudaStream_t st) {
 
 cudaError_t launch_simt_fwd(const KParams& p, bool bf16, cudaStream_t st) {
   if (p.n_units == 0) return cudaSuccess;
-  if (bf16) return p.head_dim == 128 ? launch_fwd_t<__nv_bfloat16, 128>(p, st)
-                                     : launch_fwd_t<__nv_bfloat16, 64>(p, st);
-  return p.head_dim == 128 ? launch_fwd_t<float, 128>(p, st) : launch_fwd_t<float, 64>(p, st);
+  if (bf16) return p.head_dim == 256   ? launch_fwd_t<__nv_bfloat16, 256>(p, st)
+                   : p.head_dim == 128 ? launch_fwd_t<__nv_bfloat16, 128>(p, st)
+                                       : launch_fwd_t<__nv_bfloat16, 64>(p, st);
+  return p.head_dim == 256   ? launch_fwd_t<float, 256>(p, st)
+         : p.head_dim == 128 ? launch_fwd_t<float, 128>(p, st)
+                             : launch_fwd_t<float, 64>(p, st);
 }
 
 cudaError_t launch_simt_bwd(const KParams& p, bool bf16, cudaStream_t st) {
   if (p.n_units == 0) return cudaSuccess;
+  if (p.head_dim == 256) return bf16 ? launch_bwd256_t<__nv_bfloat16>(p, st) : launch_bwd256_t<float>(p, st);
   if (bf16) return p.head_dim == 128 ? launch_bwd_t<__nv_bfloat16, 128>(p, st)
                                      : launch_bwd_t<__nv_bfloat16, 64>(p, st);
   return p.head_dim == 128 ? launch_bwd_t<float, 128>(p, st) : launch_bwd_t<float, 64>(p, st);

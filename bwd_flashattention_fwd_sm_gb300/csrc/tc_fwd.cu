@@ -45,12 +45,34 @@ namespace gbattn {
 
 namespace {
 
-constexpr int kStages = 2;
 constexpr int kThreads = 384;  // three full warpgroups
 // Register split: launched at 168 per thread (384 x 168 = 64512 registers); the
-// two softmax warpgroups raise theirs to 200, the producer/issuer warpgroup
-// lowers its to 96: 256 x 200 + 128 x 96 = 63488 <= 64512.
-constexpr uint32_t kRegsSoftmax = 200, kRegsControl = 96;
+// two softmax warpgroups raise theirs, the producer/issuer warpgroup lowers its:
+// 256 x 192 + 128 x 112 = 256 x 200 + 128 x 96 = 63488 <= 64512.  Dense and
+// causal units take 192 / 112 (at 96 the issuers' loop spills); block-sparse
+// units, whose tile lists hold more state in the softmax, 200 / 96.
+template <bool kSparse>
+struct RegSplit {
+  static constexpr uint32_t kSoftmax = 192, kControl = 112;
+};
+template <>
+struct RegSplit<true> {
+  static constexpr uint32_t kSoftmax = 200, kControl = 96;
+};
+
+// Shared-memory tile size and ring depths: bf16 tiles are 32 KiB (two Q tiles,
+// K and V rings), e4m3 tiles 16 KiB, so the FP8 rings are twice as deep in less
+// space.
+template <bool kFp8>
+struct FwdCfg {
+  static constexpr uint32_t kTileB = kTileBytes;
+  static constexpr int kKStages = 2, kVStages = 2;
+};
+template <>
+struct FwdCfg<true> {
+  static constexpr uint32_t kTileB = (uint32_t)kTile * 128;
+  static constexpr int kKStages = 4, kVStages = 4;
+};
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the row max grows by more than 2^8
 constexpr uint32_t kTmemCols = 512;
 
@@ -65,13 +87,15 @@ struct FwdArgs {
   int n_tiles;
 };
 
+template <class C>
 struct Smem {
-  uint8_t q[2][kTileBytes];
-  uint8_t k[kStages][kTileBytes];
-  uint8_t v[kStages][kTileBytes];
+  static constexpr int kKStages = C::kKStages, kVStages = C::kVStages;
+  uint8_t q[2][C::kTileB];
+  uint8_t k[kKStages][C::kTileB];
+  uint8_t v[kVStages][C::kTileB];
   uint64_t unit_full[2], unit_empty[2];
   uint64_t q_full[2], q_empty[2];
-  uint64_t k_full[kStages], v_full[kStages], k_empty[kStages], v_empty[kStages];
+  uint64_t k_full[kKStages], v_full[kVStages], k_empty[kKStages], v_empty[kVStages];
   uint64_t s_full[2], p_full[2], o_final[2], o_free[2];
   uint64_t turn[2];  // turn[q]: issuer q has issued its products for a key tile
   uint64_t drain[2];
@@ -80,10 +104,12 @@ struct Smem {
   ptx::Abort abort;
 };
 
-static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory per CTA is at most 227 KiB");
+static_assert(sizeof(Smem<FwdCfg<false>>) + 1024 <= 232448, "shared memory per CTA is at most 227 KiB");
+static_assert(sizeof(Smem<FwdCfg<true>>) + 1024 <= 232448, "shared memory per CTA is at most 227 KiB");
 
+template <class SM>
 struct Waiter {
-  Smem& sm;
+  SM& sm;
   const KParams& p;
   __device__ bool one(uint64_t* bar, uint32_t parity) {
     return ptx::mbar_wait(bar, parity, &sm.abort, p.status, p.wait_limit_ns);
@@ -100,7 +126,8 @@ struct Waiter {
 };
 
 // Reads unit slot `u` (after its full barrier); false for the end sentinel.
-__device__ __forceinline__ bool read_unit(const Smem& sm, int slot, Unit& un) {
+template <class SM>
+__device__ __forceinline__ bool read_unit(const SM& sm, int slot, Unit& un) {
   const volatile int* s = sm.unit_slot[slot];
   un.seq = s[0];
   un.head = s[1];
@@ -180,11 +207,13 @@ __device__ __forceinline__ float write_p8(const uint32_t (&sr)[128], float c, fl
 // head's largest V scale, which multiplies O in the epilogue).
 template <bool kSparse, int D, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ FwdArgs a) {
+  using SM = Smem<FwdCfg<kFp8>>;
+  constexpr int kKStages = SM::kKStages, kVStages = SM::kVStages;
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  SM& sm = *reinterpret_cast<SM*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const KParams& p = a.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  Waiter W{sm, p};
+  Waiter<SM> W{sm, p};
   static_assert(!kFp8 || D == 128, "the FP8 forward has head dim 128");
   constexpr uint32_t kLoadBytes = kFp8 ? (uint32_t)kTile * 128 : tile_bytes<D>();
 
@@ -199,10 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       ptx::mbar_init(&sm.o_final[i], 1);
       ptx::mbar_init(&sm.o_free[i], 4);
     }
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       ptx::mbar_init(&sm.k_full[s], 1);
-      ptx::mbar_init(&sm.v_full[s], 1);
       ptx::mbar_init(&sm.k_empty[s], 2);  // one commit per MMA warp
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      ptx::mbar_init(&sm.v_full[s], 1);
       ptx::mbar_init(&sm.v_empty[s], 2);
     }
     ptx::mbar_init(&sm.turn[0], 1);
@@ -220,11 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  if (warp >= 8) ptx::regs_decrease<kRegsControl>();
+  if (warp >= 8) ptx::regs_decrease<RegSplit<kSparse>::kControl>();
   if (warp == 8) {
     // ================================================================ producer
     uint32_t n_units_seen = 0, n_q_loads[2] = {0, 0}, n_k = 0, n_v = 0;
-    int last_q_phase[2] = {-1, -1}, last_k_phase[kStages] = {-1, -1}, last_v_phase[kStages] = {-1, -1};
+    int last_q_phase[2] = {-1, -1}, last_k_phase[kKStages], last_v_phase[kVStages];
+    for (int s = 0; s < kKStages; ++s) last_k_phase[s] = -1;
+    for (int s = 0; s < kVStages; ++s) last_v_phase[s] = -1;
     bool ok = true;
     for (;;) {
       const int slot = n_units_seen & 1;
@@ -280,8 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       // its tile are done, V only after the P V products, so loading K(j+1)
       // before V(j) gives it the longest lead.
       auto load_k = [&](int kt_) -> bool {
-        const int st = n_k % kStages;
-        const uint32_t ph = (n_k / kStages) & 1;
+        const int st = n_k % kKStages;
+        const uint32_t ph = (n_k / kKStages) & 1;
         if (!W.warp(&sm.k_empty[st], ph ^ 1)) return false;
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(&sm.k_full[st], kLoadBytes);
@@ -296,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         return true;
       };
       auto load_v = [&](int kt_) -> bool {
-        const int st = n_v % kStages;
-        const uint32_t ph = (n_v / kStages) & 1;
+        const int st = n_v % kVStages;
+        const uint32_t ph = (n_v / kVStages) & 1;
         if (!W.warp(&sm.v_empty[st], ph ^ 1)) return false;
         if (lane == 0) {
           ptx::mbar_arrive_expect_tx(&sm.v_full[st], kLoadBytes);
@@ -330,10 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     if (lane == 0) {
       for (int q = 0; q < 2; ++q)
         if (last_q_phase[q] >= 0) W.drain(&sm.q_full[q], (uint32_t)last_q_phase[q]);
-      for (int s = 0; s < kStages; ++s) {
+      for (int s = 0; s < kKStages; ++s)
         if (last_k_phase[s] >= 0) W.drain(&sm.k_full[s], (uint32_t)last_k_phase[s]);
+      for (int s = 0; s < kVStages; ++s)
         if (last_v_phase[s] >= 0) W.drain(&sm.v_full[s], (uint32_t)last_v_phase[s]);
-      }
     }
   } else if (warp == 9 || warp == 10) {
     // ================================================================ MMA issuers
@@ -415,8 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       uint32_t cur_stage = 0;
       int cur_bits = bits;
       if (have) {  // prologue: S of the first tile
-        cur_stage = n_k % kStages;
-        if (!W.warp(&sm.k_full[cur_stage], (n_k / kStages) & 1)) { ok = false; break; }
+        cur_stage = n_k % kKStages;
+        if (!W.warp(&sm.k_full[cur_stage], (n_k / kKStages) & 1)) { ok = false; break; }
         ++n_k;
         ptx::tc_fence_after();
         if ((bits >> (4 * q)) & 0xF) ok = issue_s(ptx::smem_u32(sm.k[cur_stage]));
@@ -428,13 +461,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       while (have) {
         int nkt, nbits = 0;
         const bool nhave = t.next(nkt, nbits);
-        const uint32_t nst = n_k % kStages;
-        if (!W.warp(&sm.v_full[cur_stage], (n_v / kStages) & 1)) { ok = false; break; }
+        const uint32_t nst = n_k % kKStages, vst = n_v % kVStages;
+        if (!W.warp(&sm.v_full[vst], (n_v / kVStages) & 1)) { ok = false; break; }
         ++n_v;
         // K of the next tile is waited for before P_q: it is normally there long
         // before P_q, so the wait stays off the softmax -> products -> softmax chain.
         if (nhave) {
-          if (!W.warp(&sm.k_full[nst], (n_k / kStages) & 1)) { ok = false; break; }
+          if (!W.warp(&sm.k_full[nst], (n_k / kKStages) & 1)) { ok = false; break; }
           ++n_k;
         }
         if ((cur_bits >> (4 * q)) & 0xF) {
@@ -452,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         }
         if ((cur_bits >> (4 * q)) & 0xF) {
           ptx::tc_fence_after();
-          const uint32_t v_addr = ptx::smem_u32(sm.v[cur_stage]);
+          const uint32_t v_addr = ptx::smem_u32(sm.v[vst]);
           const uint32_t acc0 = pv_issued > 0 ? 1u : 0u;
           const bool last = ++pv_issued == n_act;
           if (ptx::elect_one()) {
@@ -485,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         if (lane == 0) ptx::mbar_arrive(&sm.turn[q]);  // hand the turn to the other issuer
         ++n_turn;
         if (ptx::elect_one()) {
-          ptx::mma_commit(&sm.v_empty[cur_stage]);       // V of this tile: this warp's P V product issued
+          ptx::mma_commit(&sm.v_empty[vst]);             // V of this tile: this warp's P V product issued
           if (nhave) ptx::mma_commit(&sm.k_empty[nst]);  // K of the next tile: this warp's S product issued
         }
         __syncwarp();
@@ -503,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     __syncwarp();
   } else if (warp < 8) {
     // ================================================================ softmax
-    ptx::regs_increase<kRegsSoftmax>();
+    ptx::regs_increase<RegSplit<kSparse>::kSoftmax>();
     const int q = warp >> 2;          // query tile of this warpgroup
     const int wq = warp & 3;          // warp within the group = TMEM lane quarter
     const int r = wq * 32 + lane;     // row in the query tile = TMEM lane
@@ -694,12 +727,430 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
   }
 }
 
+// ===========================================================================
+// Head dim 256.  Two query tiles' O accumulators (2 x 256 columns) and S
+// buffers would need 768 tensor-memory columns, so a unit is one 128-row query
+// tile: S0 [0,128) S1 [128,256) O [256,512).  S of the CTA's k-th key tile goes
+// to buffer k % 2, so the tensor core computes S(k+1) while the softmax works on
+// S(k); P(k) is written over S(k) as bf16 and read by the P V products, and only
+// then does S(k+2) overwrite the buffer (the tensor core runs one thread's
+// products in issue order).  The products per key tile (2 x 1024 clocks) exceed
+// the softmax (about 1150), so the tensor core sets the pace.
+//
+// Shared memory: Q (128 x 256, four 64-column boxes, 64 KiB) and a ring of
+// 32 KiB chunks (128 rows x 128 columns, two boxes), each released by its own
+// eight products: per key tile K[:, 0:128), K[:, 128:256), then, one tile
+// behind, V[:, 0:128), V[:, 128:256), in the order the issuer uses them.
+//
+// Warps (256 threads): 0-3 softmax (thread r owns row r), 4 TMA producer and
+// unit fetcher, 5 tensor-core issuer, 6-7 idle.  Every wait is bounded.
+// ===========================================================================
+constexpr int kThreads256 = 256;
+constexpr int kRing256 = 5;
+constexpr uint32_t kChunk256 = 2 * kHalfTileBytes;  // 128 rows x 128 bf16 columns
+
+struct Smem256 {
+  uint8_t q[4][kHalfTileBytes];
+  uint8_t ring[kRing256][kChunk256];
+  uint64_t unit_full[2], unit_empty[2];
+  uint64_t q_full, q_empty;
+  uint64_t c_full[kRing256], c_empty[kRing256];
+  uint64_t s_full[2], p_full[2], pv_done, o_final, o_free;
+  uint64_t drain;
+  int unit_slot[2][4];
+  uint32_t tmem_base;
+  ptx::Abort abort;
+};
+static_assert(sizeof(Smem256) + 1024 <= 232448, "shared memory per CTA is at most 227 KiB");
+
+template <bool kSparse>
+__global__ void __launch_bounds__(kThreads256, 1) k_tc_fwd256(const __grid_constant__ FwdArgs a) {
+  using SM = Smem256;
+  extern __shared__ uint8_t smem_raw[];
+  SM& sm = *reinterpret_cast<SM*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const KParams& p = a.p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Waiter<SM> W{sm, p};
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&sm.unit_full[i], 1);
+      ptx::mbar_init(&sm.unit_empty[i], 5);  // 4 softmax warps + the issuer
+      ptx::mbar_init(&sm.s_full[i], 1);
+      ptx::mbar_init(&sm.p_full[i], 4);
+    }
+    ptx::mbar_init(&sm.q_full, 1);
+    ptx::mbar_init(&sm.q_empty, 1);
+    for (int s = 0; s < kRing256; ++s) {
+      ptx::mbar_init(&sm.c_full[s], 1);
+      ptx::mbar_init(&sm.c_empty[s], 1);
+    }
+    ptx::mbar_init(&sm.pv_done, 1);
+    ptx::mbar_init(&sm.o_final, 1);
+    ptx::mbar_init(&sm.o_free, 4);
+    ptx::mbar_init(&sm.drain, 1);
+    sm.abort.flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc(&sm.tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 4) {
+    // ================================================================ producer
+    uint32_t n_units_seen = 0, n_q = 0, n_c = 0;
+    int last_q_phase = -1, last_c_phase[kRing256];
+    for (int s = 0; s < kRing256; ++s) last_c_phase[s] = -1;
+    bool ok = true;
+    for (;;) {
+      const int slot = n_units_seen & 1;
+      if (!W.warp(&sm.unit_empty[slot], ((n_units_seen >> 1) & 1) ^ 1)) { ok = false; break; }
+      int idx = 0;
+      if (lane == 0) idx = atomicAdd(p.unit_counter, 1);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      const bool valid = idx < p.n_units;
+      Unit un{0, 0, 0, 0};
+      if (valid) un = p.units[idx];
+      if (lane == 0) {
+        volatile int* s = sm.unit_slot[slot];
+        s[0] = un.seq;
+        s[1] = un.head;
+        s[2] = un.tile;
+        s[3] = valid ? 1 : 0;
+        ptx::mbar_arrive(&sm.unit_full[slot]);
+      }
+      ++n_units_seen;
+      if (!valid) break;
+      const SeqInfo si = seq_info(p, un.seq);
+      const int h = un.head, g = h / p.group, q0 = un.tile * kTile;
+      bool any = false;
+      {
+        KvTileList2<kSparse> t;
+        t.init(p, si.len, q0);
+        int kt, bits;
+        while (t.next(kt, bits)) any |= (bits & 0xF) != 0;
+      }
+      if (!any) continue;
+      if (!W.warp(&sm.q_empty, (n_q & 1) ^ 1)) { ok = false; break; }
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(&sm.q_full, 4 * kHalfTileBytes);
+        for (int c = 0; c < 4; ++c) {
+          if (a.q_rows_inner) ptx::tma_load_4d(sm.q[c], &a.tq, &sm.q_full, c * 64, map_row(si, q0), h, si.b);
+          else ptx::tma_load_4d(sm.q[c], &a.tq, &sm.q_full, c * 64, h, map_row(si, q0), si.b);
+        }
+      }
+      last_q_phase = (int)(n_q & 1);
+      ++n_q;
+      // two chunks (columns 0-127, 128-255) of K or V for key tile kt_
+      auto load_pair = [&](const CUtensorMap* map, int kt_) -> bool {
+        for (int half = 0; half < 2; ++half) {
+          const int st = n_c % kRing256;
+          const uint32_t ph = (n_c / kRing256) & 1;
+          if (!W.warp(&sm.c_empty[st], ph ^ 1)) return false;
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(&sm.c_full[st], kChunk256);
+            for (int c = 0; c < 2; ++c) {
+              const int x = half * 128 + c * 64;
+              uint8_t* d = sm.ring[st] + c * kHalfTileBytes;
+              if (a.kv_rows_inner) ptx::tma_load_4d(d, map, &sm.c_full[st], x, map_row(si, kt_ * kTile), g, si.b);
+              else ptx::tma_load_4d(d, map, &sm.c_full[st], x, g, map_row(si, kt_ * kTile), si.b);
+            }
+          }
+          last_c_phase[st] = (int)ph;
+          ++n_c;
+        }
+        return true;
+      };
+      // K runs one key tile ahead of V: the issuer's order is S(0), S(1), PV(0), S(2), PV(1), ...
+      KvTileList2<kSparse> t;
+      t.init(p, si.len, q0);
+      int kt = 0, bits = 0;
+      bool have = t.next(kt, bits);
+      while (have && !(bits & 0xF)) have = t.next(kt, bits);
+      if (have && !load_pair(&a.tk, kt)) { ok = false; break; }
+      while (have) {
+        int nkt = 0, nbits = 0;
+        bool nhave = t.next(nkt, nbits);
+        while (nhave && !(nbits & 0xF)) nhave = t.next(nkt, nbits);
+        if (nhave && !load_pair(&a.tk, nkt)) { ok = false; break; }
+        if (!load_pair(&a.tv, kt)) { ok = false; break; }
+        have = nhave;
+        kt = nkt;
+      }
+      if (!ok) break;
+    }
+    (void)ok;
+    if (lane == 0) {
+      if (last_q_phase >= 0) W.drain(&sm.q_full, (uint32_t)last_q_phase);
+      for (int s = 0; s < kRing256; ++s)
+        if (last_c_phase[s] >= 0) W.drain(&sm.c_full[s], (uint32_t)last_c_phase[s]);
+    }
+  } else if (warp == 5) {
+    // ================================================================ MMA issuer
+    constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 128, false, false);
+    constexpr uint32_t idesc_pv = ptx::idesc_bf16(128, 128, false, true);
+    const uint32_t q_addr = ptx::smem_u32(sm.q[0]);
+    const uint32_t t_o = tmem + 256;
+    uint32_t n_units_seen = 0, n_q = 0, n_c = 0, n_s = 0, n_p = 0, n_o = 0;
+    bool ok = true;
+    // waits for the next ring chunk; returns its shared address (0 on a timeout)
+    auto next_chunk = [&](uint32_t& st) -> uint32_t {
+      st = n_c % kRing256;
+      if (!W.warp(&sm.c_full[st], (n_c / kRing256) & 1)) return 0;
+      ++n_c;
+      ptx::tc_fence_after();
+      return ptx::smem_u32(sm.ring[st]);
+    };
+    // S of the unit's next key tile into buffer n_s % 2: Q K^T over head-dim
+    // columns 0-127 (first chunk) and 128-255 (second chunk)
+    auto issue_s = [&](bool last_of_unit) -> bool {
+      const uint32_t t_s = tmem + (n_s & 1) * 128;
+      for (int half = 0; half < 2; ++half) {
+        uint32_t st;
+        const uint32_t k_addr = next_chunk(st);
+        if (!k_addr) return false;
+        if (ptx::elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t qo = (uint32_t)(half * 2 + (kk >> 2)) * kHalfTileBytes + (kk & 3) * 32;
+            const uint32_t ko = (uint32_t)(kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
+            ptx::mma_ss(t_s, ptx::sdesc_sw128(q_addr + qo, 16, 1024), ptx::sdesc_sw128(k_addr + ko, 16, 1024),
+                        idesc_s, (half > 0 || kk > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(&sm.c_empty[st]);
+          if (half == 1) {
+            ptx::mma_commit(&sm.s_full[n_s & 1]);
+            if (last_of_unit) ptx::mma_commit(&sm.q_empty);
+          }
+        }
+        __syncwarp();
+      }
+      ++n_s;
+      return true;
+    };
+    for (;;) {
+      const int slot = n_units_seen & 1;
+      if (!W.warp(&sm.unit_full[slot], (n_units_seen >> 1) & 1)) { ok = false; break; }
+      Unit un;
+      const bool valid = read_unit(sm, slot, un);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sm.unit_empty[slot]);
+      ++n_units_seen;
+      if (!valid) break;
+      const SeqInfo si = seq_info(p, un.seq);
+      int n_act = 0;
+      {
+        KvTileList2<kSparse> t;
+        t.init(p, si.len, un.tile * kTile);
+        int kt, bits;
+        while (t.next(kt, bits)) n_act += (bits & 0xF) != 0;
+      }
+      if (n_act == 0) continue;
+      if (!W.warp(&sm.q_full, n_q & 1)) { ok = false; break; }
+      ++n_q;
+      ptx::tc_fence_after();
+      if (!issue_s(n_act == 1)) { ok = false; break; }
+      if (n_act > 1 && !issue_s(n_act == 2)) { ok = false; break; }
+      for (int i = 0; i < n_act && ok; ++i) {
+        // O += P(i) V(i) once the softmax has written P(i); before the unit's
+        // first product, the previous unit's epilogue must have read O
+        const uint32_t b = n_p & 1;
+        if (!W.warp(&sm.p_full[b], (n_p >> 1) & 1)) { ok = false; break; }
+        ++n_p;
+        if (i == 0 && !W.warp(&sm.o_free, (n_o & 1) ^ 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t t_p = tmem + b * 128;
+        for (int half = 0; half < 2; ++half) {
+          uint32_t st;
+          const uint32_t v_addr = next_chunk(st);
+          if (!v_addr) { ok = false; break; }
+          if (ptx::elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              // B = V as (N = head dim, K = keys), head dim contiguous: MN-major
+              const uint64_t bdesc = ptx::sdesc_sw128(v_addr + kk * 2048, kHalfTileBytes, 1024);
+              ptx::mma_ts(t_o + half * 128, t_p + kk * 8, bdesc, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit(&sm.c_empty[st]);
+            if (half == 1) {
+              ptx::mma_commit(&sm.pv_done);
+              if (i == n_act - 1) ptx::mma_commit(&sm.o_final);
+            }
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (i + 2 < n_act && !issue_s(i + 3 == n_act)) { ok = false; break; }
+      }
+      if (!ok) break;
+      ++n_o;
+    }
+    (void)ok;
+    __syncwarp();
+    if (ptx::elect_one()) ptx::mma_commit(&sm.drain);
+    __syncwarp();
+    if (lane == 0) W.drain(&sm.drain, 0);
+    __syncwarp();
+  } else if (warp < 4) {
+    // ================================================================ softmax
+    const int r = warp * 32 + lane;  // row in the query tile = TMEM lane
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t col_o = 256;
+    const bool elem_causal = p.mask == kMaskCausal || (p.mask == kMaskBlock && p.causal_in_block);
+    const float c = p.scale_log2;
+    const int row_half = r >= 64 ? 2 : 0;
+    uint32_t n_units_seen = 0, n_t = 0, n_o = 0;
+    bool ok = true;
+    for (;;) {
+      const int slot = n_units_seen & 1;
+      if (!W.warp(&sm.unit_full[slot], (n_units_seen >> 1) & 1)) { ok = false; break; }
+      Unit un;
+      const bool valid = read_unit(sm, slot, un);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sm.unit_empty[slot]);
+      ++n_units_seen;
+      if (!valid) break;
+      const SeqInfo si = seq_info(p, un.seq);
+      const int h = un.head;
+      const int q0 = un.tile * kTile;
+      const int qi = q0 + r;
+      float m_used = -INFINITY, l = 0.f;
+      int n_done = 0;
+      KvTileList2<kSparse> t;
+      t.init(p, si.len, q0);
+      int kt, bits8;
+      while (t.next(kt, bits8)) {
+        const int bits = bits8 & 0xF;
+        if (!bits) continue;
+        const uint32_t b = n_t & 1, col_s = b * 128;
+        if (!W.warp(&sm.s_full[b], (n_t >> 1) & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const int k0 = kt * kTile;
+        const bool need_mask = (k0 + kTile > si.len) || (elem_causal && k0 + kTile - 1 > q0) || bits != 0xF;
+        int thr = si.len - k0;
+        if (elem_causal) thr = min(thr, qi - k0 + 1);
+        const bool lo_ok = (bits >> row_half) & 1, hi_ok = (bits >> (row_half + 1)) & 1;
+        uint32_t sr[128];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          ptx::tmem_ld32(tmem + lane_base + col_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
+        ptx::tmem_ld_wait();
+        if (c < 0.f) {
+#pragma unroll
+          for (int k = 0; k < 128; ++k) sr[k] ^= 0x80000000u;
+        }
+        const float ca = fabsf(c);
+        float e8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) e8[u] = -INFINITY;
+        if (!need_mask) {
+#pragma unroll
+          for (int k = 0; k < 128; ++k) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 128; ++k)
+            if (k < thr && (k < 64 ? lo_ok : hi_ok)) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+        }
+        const float ext = fmaxf(fmaxf(fmaxf(e8[0], e8[1]), fmaxf(e8[2], e8[3])),
+                                fmaxf(fmaxf(e8[4], e8[5]), fmaxf(e8[6], e8[7])));
+        const float mx = ext == -INFINITY ? -INFINITY : ext * ca;
+        const float m_new = fmaxf(m_used, mx);
+        const bool resc = m_new > m_used + kRescaleLog2;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = fast_exp2(m_used - m_new);
+          l *= alpha;
+          m_used = m_new;
+        }
+        const float mu = m_used == -INFINITY ? 0.f : m_used;
+        const float rs = need_mask ? write_p<true>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s)
+                                   : write_p<false>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s);
+        // Rescaling O: the previous tile's P V products may still run (S of this
+        // tile was issued before them), so wait for them first.  The products
+        // of this tile wait for p_full, so rescaling now is in time.
+        if (n_done > 0 && __any_sync(0xffffffffu, resc)) {
+          if (!W.warp(&sm.pv_done, (n_t - 1) & 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) {
+            uint32_t orr[32];
+            ptx::tmem_ld32(tmem + lane_base + col_o + cc * 32, orr);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            ptx::tmem_st32(tmem + lane_base + col_o + cc * 32, orr);
+          }
+        }
+        l += rs;
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.p_full[b]);
+        ++n_t;
+        ++n_done;
+      }
+      if (!ok) break;
+      if (q0 >= si.len) continue;
+      if (n_done > 0) {
+        if (!W.warp(&sm.o_final, n_o & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
+      const bool row_ok = qi < si.len;
+      __nv_bfloat16* orow = O + (row_ok ? q_off(p, si, h, qi) : 0);
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        uint32_t orr[32];
+        if (n_done > 0) {
+          ptx::tmem_ld32(tmem + lane_base + col_o + cc * 32, orr);
+          ptx::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orr[i] = 0u;
+        }
+        if (row_ok) {
+#pragma unroll
+          for (int w4 = 0; w4 < 4; ++w4) {
+            uint4 v4;
+            v4.x = ptx::pack_bf16x2(__uint_as_float(orr[w4 * 8 + 0]) * inv, __uint_as_float(orr[w4 * 8 + 1]) * inv);
+            v4.y = ptx::pack_bf16x2(__uint_as_float(orr[w4 * 8 + 2]) * inv, __uint_as_float(orr[w4 * 8 + 3]) * inv);
+            v4.z = ptx::pack_bf16x2(__uint_as_float(orr[w4 * 8 + 4]) * inv, __uint_as_float(orr[w4 * 8 + 5]) * inv);
+            v4.w = ptx::pack_bf16x2(__uint_as_float(orr[w4 * 8 + 6]) * inv, __uint_as_float(orr[w4 * 8 + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + cc * 32 + w4 * 8) = v4;
+          }
+        }
+      }
+      if (n_done > 0) {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.o_free);
+        ++n_o;
+      }
+      if (row_ok)
+        p.lse[row_index(p, si, h, qi)] = l > 0.f ? (m_used + fast_log2(l)) * 0.69314718055994530942f : -INFINITY;
+    }
+    (void)ok;
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 }  // namespace
 
 bool tc_fwd_available() { return true; }
 
-cudaError_t launch_tc_fwd(const KParams& p, int sms, cudaStream_t st) {
-  if (p.n_units == 0) return cudaSuccess;
+cudaError_t launch_tc_fwd256(const KParams& p, int sms, cudaStream_t st) {
   FwdArgs a;
   TileMap mq, mk, mv;
   cudaError_t e;
@@ -712,7 +1163,31 @@ cudaError_t launch_tc_fwd(const KParams& p, int sms, cudaStream_t st) {
   a.q_rows_inner = mq.rows_inner;
   a.kv_rows_inner = mk.rows_inner;
   a.p = p;
-  const size_t smem = sizeof(Smem) + 1024;
+  const size_t smem = sizeof(Smem256) + 1024;
+  const int grid = p.n_units < sms ? p.n_units : sms;
+  auto kernel = p.mask == kMaskBlock ? k_tc_fwd256<true> : k_tc_fwd256<false>;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kThreads256, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_fwd(const KParams& p, int sms, cudaStream_t st) {
+  if (p.n_units == 0) return cudaSuccess;
+  if (p.head_dim == 256) return launch_tc_fwd256(p, sms, st);
+  FwdArgs a;
+  TileMap mq, mk, mv;
+  cudaError_t e;
+  if ((e = make_tile_map(&mq, p.q, p, false)) != cudaSuccess) return e;
+  if ((e = make_tile_map(&mk, p.k, p, true)) != cudaSuccess) return e;
+  if ((e = make_tile_map(&mv, p.v, p, true)) != cudaSuccess) return e;
+  a.tq = mq.map;
+  a.tk = mk.map;
+  a.tv = mv.map;
+  a.q_rows_inner = mq.rows_inner;
+  a.kv_rows_inner = mk.rows_inner;
+  a.p = p;
+  const size_t smem = sizeof(Smem<FwdCfg<false>>) + 1024;
   const int grid = p.n_units < sms ? p.n_units : sms;
   auto kernel = p.head_dim == 64
                     ? (p.mask == kMaskBlock ? k_tc_fwd<true, 64, false> : k_tc_fwd<false, 64, false>)
@@ -742,7 +1217,7 @@ cudaError_t launch_tc_fwd_fp8(const KParams& p, int sms, cudaStream_t st, const 
   a.ks = f.ks;
   a.vs = f.vs;
   a.n_tiles = (int)((S + kTile - 1) / kTile);
-  const size_t smem = sizeof(Smem) + 1024;
+  const size_t smem = sizeof(Smem<FwdCfg<true>>) + 1024;
   const int grid = p.n_units < sms ? p.n_units : sms;
   auto kernel = p.mask == kMaskBlock ? k_tc_fwd<true, 128, true> : k_tc_fwd<false, 128, true>;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

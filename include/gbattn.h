@@ -43,7 +43,8 @@
  *                   *_stride_s (between tokens) and *_stride_h; *_stride_b ignored.
  *                   lse: contiguous float32 [heads_q, T].
  *
- * Constraints.  head_dim 64 or 128 (both types);
+ * Constraints.  head_dim 64, 128 or 256 (both types; at 256 the bf16 forward
+ * runs on the tensor cores and the backward on the float32-arithmetic kernels);
  * heads_q % heads_kv == 0; every tensor pointer 16-byte aligned; strides
  * multiples of 8 elements (16 bytes) for bf16 and 4 elements for float32.
  *
@@ -69,7 +70,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1,    /* a shape, stride, pointer or index list is invalid */
-  ATTN_ERR_UNSUPPORTED = 2,    /* valid but not implemented (e.g. bf16 with head_dim 64) */
+  ATTN_ERR_UNSUPPORTED = 2,    /* valid but not implemented (e.g. head_dim 96) */
   ATTN_ERR_WORKSPACE = 3,      /* workspace NULL, misaligned or smaller than required */
   ATTN_ERR_CUDA = 4,           /* a CUDA runtime call failed (no device, launch error) */
   ATTN_ERR_DEVICE_TIMEOUT = 5, /* device: a bounded pipeline wait gave up */
@@ -163,8 +164,8 @@ attn_status_t attn_bwd(const attn_params_t* p, const void* q, const void* k, con
  * key tiles in ascending order (three products per tile instead of one, so
  * the backward does 7 products instead of 5).  Arguments, layouts and the
  * workspace (attn_bwd_workspace_size bytes) are those of attn_bwd.  Only the
- * tensor-core path (bf16, head_dim 64 or 128) has it: float32 returns
- * ATTN_ERR_UNSUPPORTED before queuing anything.
+ * tensor-core path (bf16, head_dim 64 or 128) has it: float32 and head_dim
+ * 256 return ATTN_ERR_UNSUPPORTED before queuing anything.
  */
 attn_status_t attn_bwd_deterministic(const attn_params_t* p, const void* q, const void* k, const void* v,
                                      const void* o, const void* dout, const float* lse, void* dq, void* dk,

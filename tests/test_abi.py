@@ -258,3 +258,17 @@ def test_fp8_validation(lib):
     assert fp8_quant(lib, params(), scales=0) == _lib.ATTN_ERR_INVALID_ARG
     assert fp8_fwd(lib, params(), ws_bytes=16) == _lib.ATTN_ERR_WORKSPACE
     assert fp8_fwd(lib, params(B=0)) == _lib.ATTN_OK and fp8_quant(lib, params(S=0)) == _lib.ATTN_OK
+
+
+def test_head_dim_256_accepted(lib):
+    """head_dim 256: forward and backward accepted (both dtypes); the deterministic
+    backward, which needs the tensor-core backward, is refused."""
+    for dtype in (_lib.ATTN_BF16, _lib.ATTN_F32):
+        p = params(D=256, dtype=dtype)
+        assert fwd(lib, p) == _lib.ATTN_ERR_CUDA
+        assert bwd(lib, p) == _lib.ATTN_ERR_CUDA
+    det = lib.attn_bwd_deterministic(ctypes.byref(params(D=256)), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                     FAKE, FAKE, 1 << 40, None)
+    assert det == _lib.ATTN_ERR_UNSUPPORTED
+    p = params(D=512)
+    assert fwd(lib, p) == _lib.ATTN_ERR_UNSUPPORTED and b"256" in lib.attn_last_error()
