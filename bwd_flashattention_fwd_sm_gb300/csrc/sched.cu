@@ -128,15 +128,20 @@ __global__ void __launch_bounds__(kThreads) k_build_worklist(KParams p, int back
   for (int i = tid; i < kBuckets; i += kThreads) hist[i] = 0;
   __syncthreads();
 
-  // 2. enumerate units, compute costs, histogram
+  // 2. enumerate units, compute costs, histogram.  Units are numbered sequence
+  // by sequence, head by head, tile fastest, so that among equal costs (every
+  // unit of a dense mask) the units running at the same time share a few heads'
+  // K and V (or Q and dO) in L2 instead of touching every head at once.
   for (int u = tid; u < n_units; u += kThreads) {
-    const int pi = u / heads, h = u % heads;
-    int lo = 0, hi = n_seqs - 1;  // last n with prefix[n] <= pi
+    int lo = 0, hi = n_seqs - 1;  // last n with heads * prefix[n] <= u
     while (lo < hi) {
       int mid = (lo + hi + 1) >> 1;
-      if (prefix[mid] <= pi) lo = mid; else hi = mid - 1;
+      if ((long long)heads * prefix[mid] <= u) lo = mid; else hi = mid - 1;
     }
-    const int n = lo, t = pi - prefix[n];
+    const int n = lo;
+    const int tiles = prefix[n + 1] - prefix[n];
+    const int local = u - heads * prefix[n];
+    const int h = local / tiles, t = local % tiles;
     const int len = seq_info(p, n).len;
     Unit un;
     un.seq = n;
