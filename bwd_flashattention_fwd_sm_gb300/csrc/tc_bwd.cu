@@ -254,6 +254,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       if (!valid) break;
       const SeqInfo si = seq_info(p, un.seq);
       const int g = un.head, k0 = un.tile * kTile;
+      // The unit is known a few steps before the previous one ends: start its K
+      // and V on their way into L2, so the load below does not wait on memory.
+      if (lane == 0) {
+        tma_prefetch_tile(&a.tk, a.kv_rows_inner, map_row(si, k0), g, si.b, D / 64);
+        tma_prefetch_tile(&a.tv, a.kv_rows_inner, map_row(si, k0), g, si.b, D / 64);
+      }
       // K and V of the unit, once the previous unit's products are done with them
       if (!W.warp(&sm.kv_empty, (n_units & 1) ^ 1)) break;
       if (lane == 0) {

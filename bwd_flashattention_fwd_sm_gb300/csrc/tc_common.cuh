@@ -29,6 +29,17 @@ __device__ __forceinline__ void tma_tile(void* dst, const CUtensorMap* map, int 
   }
 }
 
+// L2 prefetch of the same tile tma_tile would load.
+__device__ __forceinline__ void tma_prefetch_tile(const CUtensorMap* map, int rows_inner, int row, int head, int b,
+                                                  int nbox = 2) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    if (c >= nbox) break;
+    if (rows_inner) ptx::tma_prefetch_4d(map, c * 64, row, head, b);
+    else ptx::tma_prefetch_4d(map, c * 64, head, row, b);
+  }
+}
+
 // Row coordinate and batch coordinate of position `pos` of a sequence in a tile map.
 __device__ __forceinline__ int map_row(const SeqInfo& s, int pos) { return (int)(s.tok0 + pos); }
 
