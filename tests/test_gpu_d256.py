@@ -9,6 +9,7 @@ Tolerances are those of every other test (parity_util).
 
 import numpy as np
 import pytest
+import torch
 
 from bwd_flashattention_fwd_sm_gb300 import workloads as W
 
@@ -59,3 +60,20 @@ def test_forward_full_size_sampled_head_d256(mask, b, h):
     ref = oracle_run(wl.with_(batch=1, heads_q=1, heads_kv=1), one, passes="fwd")
     sub = {n: got[n][b:b + 1, h:h + 1] for n in ("o", "lse")}
     check_all(wl, sub, ref, names=("o", "lse"))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_d256(causal, dtype):
+    """Packed sequences (one empty, ragged lengths) at head dim 256."""
+    lens = [5, 0, 129, 1, 300]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    wl = W.Workload("varlen_d256", 1, 4, 2, max(lens), 256, dtype, "causal" if causal else "none",
+                    varlen=True, n_seqs=len(lens), seed=64)
+    T = int(cu[-1])
+    g = torch.Generator().manual_seed(64)
+    dt = W.torch_dtype(wl)
+    inp = {n: torch.randn(s, generator=g).to(dt) for n, s in
+           (("q", (T, 4, 256)), ("k", (T, 2, 256)), ("v", (T, 2, 256)), ("do", (T, 4, 256)))}
+    inp["cu_seqlens"] = cu
+    check_all(wl, gpu_run(wl, inp), oracle_run(wl, inp, cu=cu))
