@@ -210,7 +210,10 @@ attn_status_t attn_bwd_deterministic(const attn_params_t* p, const void* q, cons
  *
  * Both calls: p->dtype must be ATTN_BF16, p->head_dim 128 and p->cu_seqlens NULL
  * (else ATTN_ERR_UNSUPPORTED); byte tensors 16-byte aligned, scale arrays 4-byte
- * aligned; inputs must be finite.  Errors and asynchrony as for attn_fwd.
+ * aligned; inputs must be finite.  p's q strides give the bf16 q (quantisation)
+ * and o (forward); its kv strides give the bf16 k and v of the quantisation and
+ * are validated by the forward like attn_fwd's (the codes' own layouts above are
+ * fixed).  Errors and asynchrony as for attn_fwd.
  */
 attn_status_t attn_quantize_fp8(const attn_params_t* p, const void* q, const void* k, const void* v, void* q8,
                                 void* k8, void* v8t, float* q_scale, float* k_scale, float* v_scale, void* stream);
