@@ -249,7 +249,8 @@ Layout layout_for(const attn_params_t* p, const Problem& pr, bool backward) {
   L.units = off;
   off = align_up(off + sizeof(Unit) * (size_t)L.n_units, 256);
   L.sched = off;
-  off = align_up(off + sizeof(int) * align_up((size_t)pr.n_seqs + 1, 4) + sizeof(Unit) * (size_t)L.n_units, 256);
+  // work-list scratch: tile prefix, sequence order and sequence starts, then the units
+  off = align_up(off + sizeof(int) * 3 * align_up((size_t)pr.n_seqs + 1, 4) + sizeof(Unit) * (size_t)L.n_units, 256);
   if (backward) {
     if (p->mask == ATTN_MASK_BLOCK) {
       L.csc_ptr = off;
@@ -269,7 +270,7 @@ Layout layout_for(const attn_params_t* p, const Problem& pr, bool backward) {
       L.q_list = off;
       off = align_up(off + sizeof(Unit) * (size_t)L.q_units, 256);
       L.q_sched = off;
-      off = align_up(off + sizeof(int) * align_up((size_t)pr.n_seqs + 1, 4) + sizeof(Unit) * (size_t)L.q_units, 256);
+      off = align_up(off + sizeof(int) * 3 * align_up((size_t)pr.n_seqs + 1, 4) + sizeof(Unit) * (size_t)L.q_units, 256);
     }
   }
   L.total = off;

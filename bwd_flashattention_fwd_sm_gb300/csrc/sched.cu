@@ -99,7 +99,33 @@ __device__ int block_exclusive_scan(int x, int* smem, int* total) {
   return r;
 }
 
-// One block.  scratch: [n_seqs + 1] tile prefix + [n_units] unsorted units (as int4).
+// Turns hist (counts per cost bucket) into the first list position of each
+// bucket, highest bucket first.  All threads of the block call it.
+__device__ void bucket_starts_desc(int* hist, int* scan_smem) {
+  const int tid = threadIdx.x;
+  const int per = kBuckets / kThreads;  // buckets per thread, thread 0 owns the highest
+  int vals[kBuckets / kThreads];
+  int s = 0;
+  for (int i = 0; i < per; ++i) {
+    vals[i] = hist[kBuckets - 1 - (tid * per + i)];
+    s += vals[i];
+  }
+  int tot;
+  int b = block_exclusive_scan(s, scan_smem, &tot);
+  for (int i = 0; i < per; ++i) {
+    hist[kBuckets - 1 - (tid * per + i)] = b;
+    b += vals[i];
+  }
+  __syncthreads();
+}
+
+// Words of int scratch before the unit array: tile prefix, sequence order and
+// sequence starts, [n_seqs + 1] each, rounded to 4.
+__host__ __device__ inline int sched_ints(int n_seqs) { return 3 * ((n_seqs + 1 + 3) & ~3); }
+
+// One block.  scratch: [n_seqs + 1] tile prefix, [n_seqs + 1] sequence order,
+// [n_seqs + 1] sequence starts (each rounded to 4 ints), then [n_units]
+// unsorted units (as int4).
 __global__ void __launch_bounds__(kThreads) k_build_worklist(KParams p, int backward, int tile_rows,
                                                            Unit* out, int n_units, int* scratch) {
   __shared__ int hist[kBuckets];
@@ -107,8 +133,11 @@ __global__ void __launch_bounds__(kThreads) k_build_worklist(KParams p, int back
   const int tid = threadIdx.x;
   const int n_seqs = p.varlen ? p.n_seqs : p.batch;
   const int heads = backward ? p.heads_kv : p.heads_q;
+  const int seq_words = (n_seqs + 1 + 3) & ~3;
   int* prefix = scratch;                                  // [n_seqs + 1]
-  Unit* tmp = reinterpret_cast<Unit*>(scratch + ((n_seqs + 1 + 3) & ~3));
+  int* seq_order = scratch + seq_words;                   // [n_seqs]
+  int* seq_start = scratch + 2 * seq_words;               // [n_seqs]
+  Unit* tmp = reinterpret_cast<Unit*>(scratch + sched_ints(n_seqs));
 
   // 1. prefix of tiles per sequence (chunked block scan)
   const int chunk = cdiv(n_seqs, kThreads);
@@ -127,6 +156,55 @@ __global__ void __launch_bounds__(kThreads) k_build_worklist(KParams p, int back
   }
   for (int i = tid; i < kBuckets; i += kThreads) hist[i] = 0;
   __syncthreads();
+
+  if (p.varlen) {
+    // Packed sequences: sequence by sequence, longest first (a sequence's cost
+    // grows with its length, for every mask a packed batch takes), each head by
+    // head and each head's tiles longest first (causal: tile 0 first backward,
+    // the last tile first forward).  Units of one sequence and head then run at
+    // the same time and share its Q and dO (or K and V) in L2; ordered by unit
+    // cost alone, the units running at once came from hundreds of different
+    // (sequence, head) pairs and shared nothing.
+    for (int n = tid; n < n_seqs; n += kThreads)
+      atomicAdd(&hist[min(prefix[n + 1] - prefix[n], kBuckets - 1)], 1);
+    __syncthreads();
+    bucket_starts_desc(hist, scan_smem);
+    for (int n = tid; n < n_seqs; n += kThreads)
+      seq_order[atomicAdd(&hist[min(prefix[n + 1] - prefix[n], kBuckets - 1)], 1)] = n;
+    __syncthreads();
+    int local2 = 0;
+    for (int i = tid * chunk; i < min(n_seqs, (tid + 1) * chunk); ++i) {
+      const int n = seq_order[i];
+      local2 += heads * (prefix[n + 1] - prefix[n]);
+    }
+    int total2;
+    int base2 = block_exclusive_scan(local2, scan_smem, &total2);
+    for (int i = tid * chunk; i < min(n_seqs, (tid + 1) * chunk); ++i) {
+      const int n = seq_order[i];
+      seq_start[n] = base2;
+      base2 += heads * (prefix[n + 1] - prefix[n]);
+    }
+    __syncthreads();
+    for (int u = tid; u < n_units; u += kThreads) {
+      int lo = 0, hi = n_seqs - 1;
+      while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if ((long long)heads * prefix[mid] <= u) lo = mid; else hi = mid - 1;
+      }
+      const int n = lo, tiles = prefix[n + 1] - prefix[n];
+      const int local = u - heads * prefix[n];
+      const int h = local / tiles, t = local % tiles;
+      const int len = seq_info(p, n).len;
+      Unit un;
+      un.seq = n;
+      un.head = h;
+      un.tile = t;
+      un.cost = (t * tile_rows < len) ? unit_cost(p, backward, tile_rows, len, t) : 0;
+      const int r = (p.mask == kMaskCausal && !backward) ? tiles - 1 - t : t;
+      out[seq_start[n] + h * tiles + r] = un;
+    }
+    return;
+  }
 
   // 2. enumerate units, compute costs, histogram.  Units are numbered sequence
   // by sequence, head by head, tile fastest, so that among equal costs (every
@@ -154,22 +232,7 @@ __global__ void __launch_bounds__(kThreads) k_build_worklist(KParams p, int back
   __syncthreads();
 
   // 3. bucket starts, highest cost first
-  {
-    const int per = kBuckets / kThreads;  // 4 buckets per thread, thread 0 owns the highest
-    int vals[kBuckets / kThreads];
-    int s = 0;
-    for (int i = 0; i < per; ++i) {
-      vals[i] = hist[kBuckets - 1 - (tid * per + i)];
-      s += vals[i];
-    }
-    int tot;
-    int b = block_exclusive_scan(s, scan_smem, &tot);
-    for (int i = 0; i < per; ++i) {
-      hist[kBuckets - 1 - (tid * per + i)] = b;
-      b += vals[i];
-    }
-  }
-  __syncthreads();
+  bucket_starts_desc(hist, scan_smem);
 
   // 4. scatter
   for (int u = tid; u < n_units; u += kThreads) {
