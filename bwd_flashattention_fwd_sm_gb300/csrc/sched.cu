@@ -18,6 +18,7 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kBuckets = 4096;  // costs are clamped into this many buckets
+constexpr int kTileGroup = 16;  // fixed-length causal backward: tiles per group, at most (see below)
 
 __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -202,6 +203,33 @@ __global__ void __launch_bounds__(kThreads) k_build_worklist(KParams p, int back
       un.cost = (t * tile_rows < len) ? unit_cost(p, backward, tile_rows, len, t) : 0;
       const int r = (p.mask == kMaskCausal && !backward) ? tiles - 1 - t : t;
       out[seq_start[n] + h * tiles + r] = un;
+    }
+    return;
+  }
+
+  if (backward && p.mask == kMaskCausal) {
+    // Fixed-length causal backward: every (batch, head) pair has the same tiles,
+    // tile t costing more the smaller t is.  Ordered by cost alone, the units
+    // running at once held about five tiles of each pair, so each pair's Q and
+    // dO were fetched about once per five units.  Groups of tg tiles in cost
+    // order, and inside a group pair by pair, keep the longest units first
+    // while a group's units of one pair share their Q and dO in L2.  tg is
+    // kTileGroup, or half a pair's tiles when that is fewer (a whole pair in
+    // one group leaves its longest unit for the end).  Measured at S = 8192 /
+    // 4096 / 2048: groups of 16 / 16 / 8 were best.  (The forward keeps the
+    // plain cost order: grouping slowed it.)
+    const int nt = n_seqs > 0 ? prefix[1] - prefix[0] : 0, n_pairs = n_seqs * heads;
+    const int tg = max(1, min(kTileGroup, nt / 2));
+    for (int u = tid; u < n_units; u += kThreads) {
+      const int pair = u / nt, t = u % nt, n = pair / heads, h = pair - n * heads;
+      const int len = seq_info(p, n).len;
+      Unit un;
+      un.seq = n;
+      un.head = h;
+      un.tile = t;
+      un.cost = (t * tile_rows < len) ? unit_cost(p, backward, tile_rows, len, t) : 0;
+      const int g = t / tg, sz = min(tg, nt - g * tg);
+      out[g * tg * n_pairs + pair * sz + (t - g * tg)] = un;
     }
     return;
   }
