@@ -207,19 +207,20 @@ __global__ void __launch_bounds__(kThreads) k_build_worklist(KParams p, int back
     return;
   }
 
-  if (backward && p.mask == kMaskCausal) {
+  if (backward && p.mask == kMaskCausal && n_seqs > 0 && prefix[1] - prefix[0] >= 2 * kTileGroup) {
     // Fixed-length causal backward: every (batch, head) pair has the same tiles,
     // tile t costing more the smaller t is.  Ordered by cost alone, the units
     // running at once held about five tiles of each pair, so each pair's Q and
     // dO were fetched about once per five units.  Groups of tg tiles in cost
     // order, and inside a group pair by pair, keep the longest units first
-    // while a group's units of one pair share their Q and dO in L2.  tg is
-    // kTileGroup, or half a pair's tiles when that is fewer (a whole pair in
-    // one group leaves its longest unit for the end).  Measured at S = 8192 /
-    // 4096 / 2048: groups of 16 / 16 / 8 were best.  (The forward keeps the
-    // plain cost order: grouping slowed it.)
-    const int nt = n_seqs > 0 ? prefix[1] - prefix[0] : 0, n_pairs = n_seqs * heads;
-    const int tg = max(1, min(kTileGroup, nt / 2));
+    // while a group's units of one pair share their Q and dO in L2.  Only pairs
+    // of at least 2 * kTileGroup tiles are grouped: with fewer (S = 2048 at
+    // 128-key tiles) there are only a few units per SM, and balancing them
+    // longest first matters more (groups of 8 there: 0.135 against 0.118 ms).
+    // Measured at S = 8192 and 4096: groups of 16 beat 8, 32 and 64.  (The
+    // forward keeps the plain cost order: grouping slowed it.)
+    const int nt = prefix[1] - prefix[0], n_pairs = n_seqs * heads;
+    const int tg = kTileGroup;
     for (int u = tid; u < n_units; u += kThreads) {
       const int pair = u / nt, t = u % nt, n = pair / heads, h = pair - n * heads;
       const int len = seq_info(p, n).len;
