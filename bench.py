@@ -368,11 +368,18 @@ def run_ours(args, wl, rank, world, dist):
 
 
 def kernel_build_id():
-    try:
-        from bwd_flashattention_fwd_sm_gb300 import build as B
-        return B._stamp([])[:16]
-    except Exception:
-        return None
+    """Hash of the kernel and header sources' contents (no paths, so it is the
+    same wherever the repository sits); profiles/traffic.json records the id of
+    the sources its counters were taken on."""
+    import hashlib
+    h = hashlib.sha256()
+    for d in (os.path.join(ROOT, "bwd_flashattention_fwd_sm_gb300", "csrc"), os.path.join(ROOT, "include")):
+        for name in sorted(os.listdir(d)):
+            if name.endswith((".cu", ".cuh", ".h")):
+                h.update(name.encode())
+                with open(os.path.join(d, name), "rb") as f:
+                    h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def cpu_baseline(wl, budget_s=20.0, rank=0):
