@@ -199,7 +199,28 @@ struct Layout {
   // (forward-style units of 256 query rows), used by the deterministic mode
   long long q_units;
   size_t q_counter, q_list, q_sched;
+  // forward with a split key range: parts per unit and the parts' partial results
+  int n_split;
+  size_t part_o, part_ml;
 };
+
+// Parts to cut each forward unit's key range into.  With fewer units than a
+// GPU has SMs, a whole unit per CTA leaves SMs idle; parts of at least
+// kSplitMinTiles key tiles each (a unit's fixed costs and the combine outweigh
+// shorter parts: at 16 key tiles, two parts of 8 were slower than one), up to
+// four parts, for a target of kSplitTarget CTAs' worth of units (a fixed
+// target, so that the workspace size needs no device query).  Dense and causal
+// fixed-length forwards on the tensor cores at head_dim 64 and 128 only.
+constexpr long long kSplitTarget = 128, kSplitMinTiles = 16;
+int forward_split(const attn_params_t* p, const Problem& pr, long long n_units) {
+  if (!use_tensor_cores(p, false) || p->head_dim == 256 || pr.varlen || p->mask == ATTN_MASK_BLOCK || n_units <= 0)
+    return 1;
+  const long long key_tiles = (p->seqlen + 127) / 128;
+  long long ns = kSplitTarget / n_units;
+  if (ns > 4) ns = 4;
+  if (ns > key_tiles / kSplitMinTiles) ns = key_tiles / kSplitMinTiles;
+  return ns > 1 ? (int)ns : 1;
+}
 
 KParams base_kparams(const attn_params_t* p, const Problem& pr) {
   KParams k;
@@ -243,6 +264,8 @@ Layout layout_for(const attn_params_t* p, const Problem& pr, bool backward) {
   L.tile_rows = use_tensor_cores(p, backward) ? (backward ? 128 : (p->head_dim == 256 ? 128 : 256)) : 64;
   KParams k = base_kparams(p, pr);
   L.n_units = count_units(k, p->cu_seqlens_host, backward, L.tile_rows);
+  L.n_split = backward ? 1 : forward_split(p, pr, L.n_units);
+  L.n_units *= L.n_split;
   size_t off = 0;
   L.counter = off;
   off = align_up(off + sizeof(int), 256);
@@ -251,6 +274,13 @@ Layout layout_for(const attn_params_t* p, const Problem& pr, bool backward) {
   L.sched = off;
   // work-list scratch: tile prefix, sequence order and sequence starts, then the units
   off = align_up(off + sizeof(int) * 3 * align_up((size_t)pr.n_seqs + 1, 4) + sizeof(Unit) * (size_t)L.n_units, 256);
+  if (L.n_split > 1) {
+    const size_t rows = (size_t)pr.total_tokens * (size_t)p->heads_q;
+    L.part_o = off;
+    off = align_up(off + sizeof(float) * (size_t)L.n_split * rows * (size_t)p->head_dim, 256);
+    L.part_ml = off;
+    off = align_up(off + sizeof(float) * 2 * (size_t)L.n_split * rows, 256);
+  }
   if (backward) {
     if (p->mask == ATTN_MASK_BLOCK) {
       L.csc_ptr = off;
@@ -275,6 +305,15 @@ Layout layout_for(const attn_params_t* p, const Problem& pr, bool backward) {
   }
   L.total = off;
   return L;
+}
+
+// The forward's split key range (parts and partial buffers) from the layout.
+void set_split(KParams& kp, const Layout& L, char* ws) {
+  kp.n_split = L.n_split;
+  if (L.n_split > 1) {
+    kp.part_o = reinterpret_cast<float*>(ws + L.part_o);
+    kp.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
+  }
 }
 
 attn_status_t check_ptr(const void* ptr, const char* name) {
@@ -375,6 +414,7 @@ attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, con
   kp.units = reinterpret_cast<const Unit*>(ws + L.units);
   kp.n_units = (int)L.n_units;
   kp.unit_counter = reinterpret_cast<int*>(ws + L.counter);
+  set_split(kp, L, ws);
 
   cudaError_t e = launch_build_worklist(kp, false, L.tile_rows, reinterpret_cast<Unit*>(ws + L.units),
                                         (int)L.n_units, reinterpret_cast<int*>(ws + L.sched), st);
@@ -384,6 +424,7 @@ attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, con
   if (use_tensor_cores(p, false)) e = launch_tc_fwd(kp, sms, st);
   else e = launch_simt_fwd(kp, p->dtype == ATTN_BF16, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  if (kp.n_split > 1 && (e = launch_fwd_combine(kp, st)) != cudaSuccess) return cuda_fail(e, "combine launch");
   if (g_timing_events[0][1] && (e = cudaEventRecord(g_timing_events[0][1], st)) != cudaSuccess)
     return cuda_fail(e, "timing event");
   return ATTN_OK;
@@ -441,6 +482,7 @@ attn_status_t attn_fwd_fp8(const attn_params_t* p, const void* q8, const void* k
   kp.units = reinterpret_cast<const Unit*>(ws + L.units);
   kp.n_units = (int)L.n_units;
   kp.unit_counter = reinterpret_cast<int*>(ws + L.counter);
+  set_split(kp, L, ws);
   cudaError_t e = launch_build_worklist(kp, false, L.tile_rows, reinterpret_cast<Unit*>(ws + L.units),
                                         (int)L.n_units, reinterpret_cast<int*>(ws + L.sched), st);
   if (e != cudaSuccess) return cuda_fail(e, "work-list launch");
@@ -455,6 +497,7 @@ attn_status_t attn_fwd_fp8(const attn_params_t* p, const void* q8, const void* k
   if (g_timing_events[0][0] && (e = cudaEventRecord(g_timing_events[0][0], st)) != cudaSuccess)
     return cuda_fail(e, "timing event");
   if ((e = launch_tc_fwd_fp8(kp, sms, st, f)) != cudaSuccess) return cuda_fail(e, "FP8 forward launch");
+  if (kp.n_split > 1 && (e = launch_fwd_combine(kp, st)) != cudaSuccess) return cuda_fail(e, "combine launch");
   if (g_timing_events[0][1] && (e = cudaEventRecord(g_timing_events[0][1], st)) != cudaSuccess)
     return cuda_fail(e, "timing event");
   return ATTN_OK;

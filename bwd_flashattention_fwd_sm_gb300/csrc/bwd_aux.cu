@@ -215,7 +215,57 @@ int grid_for(long long rows) {
   return (int)(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
+// Forward with a split key range: per row, the parts' unnormalised O_s, row
+// max m_s and row sum l_s (log2 units) merge as M = max_s m_s,
+// L = sum_s 2^(m_s - M) l_s, O = sum_s 2^(m_s - M) O_s / L, LSE = ln 2 (M + log2 L),
+// the same correction the online softmax applies between key tiles (zwxr.cn
+// CANN article, section 3.3).  One warp per row; a lane holds D / 32
+// consecutive columns.  Bound by device memory: reads n_split (4 D + 8) bytes
+// per row, writes 2 D + 4.
+template <int D>
+__global__ void __launch_bounds__(256) k_fwd_combine(KParams p, long long n_rows) {
+  constexpr int NC = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const int ns = p.n_split;
+  __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
+  for (long long r = warp0; r < n_rows; r += nwarps) {
+    float M = -INFINITY;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, p.part_ml[((long long)s * n_rows + r) * 2]);
+    float L = 0.f, acc[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) acc[c] = 0.f;
+    for (int s = 0; s < ns; ++s) {
+      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + ((long long)s * n_rows + r) * 2);
+      if (ml.x == -INFINITY) continue;
+      const float w = exp2f(ml.x - M);
+      L = fmaf(w, ml.y, L);
+      float v[NC];
+      load_vec<float, NC>(p.part_o + ((long long)s * n_rows + r) * D + lane * NC, v);
+#pragma unroll
+      for (int c = 0; c < NC; ++c) acc[c] = fmaf(w, v[c], acc[c]);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) acc[c] *= inv;
+    const RowRef x = row_ref(p, r);
+    store_vec<__nv_bfloat16, NC>(O + x.q + lane * NC, acc);
+    if (lane == 0) p.lse[x.lse] = L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_fwd_combine(const KParams& p, cudaStream_t st) {
+  const long long rows = total_rows(p);
+  if (rows == 0 || p.n_split <= 1) return cudaSuccess;
+  const int grid = grid_for(rows);
+  if (p.head_dim == 128) k_fwd_combine<128><<<grid, 256, 0, st>>>(p, rows);
+  else if (p.head_dim == 64) k_fwd_combine<64><<<grid, 256, 0, st>>>(p, rows);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_bwd_preprocess(const KParams& p, bool bf16, cudaStream_t st) {
   const long long rows = total_rows(p);

@@ -62,6 +62,15 @@ struct KParams {
   int n_units;
   int* unit_counter;    // persistent kernels: next unit to take (zeroed by the work-list build)
 
+  // Forward with the key range split (few units): each unit's key tiles are cut
+  // into n_split parts, one work-list entry each (its part in Unit::cost once the
+  // list is ordered); each part writes its unnormalised O (float32
+  // [n_split][rows][D]) and its row max and sum (log2 units, [n_split][rows][2])
+  // for the combine kernel.  n_split <= 1: no split.
+  int n_split;
+  float* part_o;
+  float* part_ml;
+
   int* status;               // device status word
   unsigned long long wait_limit_ns;  // bounded-wait limit for pipeline barriers
 };
@@ -146,6 +155,9 @@ cudaError_t launch_build_worklist(const KParams& p, bool backward, int tile_rows
                                   int n_units, int* scratch, cudaStream_t st);
 // Block mask: per key block, the ascending list of query blocks that list it.
 cudaError_t launch_csr_to_csc(const KParams& p, int* csc_ptr, int* csc_idx, cudaStream_t st);
+
+// Forward with a split key range: O and LSE from the parts' partial results.
+cudaError_t launch_fwd_combine(const KParams& p, cudaStream_t st);
 
 // Backward preprocess (D_i and zeroed dQ accumulator) and dQ conversion.
 cudaError_t launch_bwd_preprocess(const KParams& p, bool bf16, cudaStream_t st);

@@ -239,22 +239,26 @@ __global__ void __launch_bounds__(kThreads) k_build_worklist(KParams p, int back
   // by sequence, head by head, tile fastest, so that among equal costs (every
   // unit of a dense mask) the units running at the same time share a few heads'
   // K and V (or Q and dO) in L2 instead of touching every head at once.
+  // A forward with a split key range lists each unit once per part (u = base
+  // unit * ns + part), at the part's share of the cost.
+  const int ns = backward ? 1 : max(1, p.n_split);
   for (int u = tid; u < n_units; u += kThreads) {
-    int lo = 0, hi = n_seqs - 1;  // last n with heads * prefix[n] <= u
+    const int ub = u / ns;
+    int lo = 0, hi = n_seqs - 1;  // last n with heads * prefix[n] <= ub
     while (lo < hi) {
       int mid = (lo + hi + 1) >> 1;
-      if ((long long)heads * prefix[mid] <= u) lo = mid; else hi = mid - 1;
+      if ((long long)heads * prefix[mid] <= ub) lo = mid; else hi = mid - 1;
     }
     const int n = lo;
     const int tiles = prefix[n + 1] - prefix[n];
-    const int local = u - heads * prefix[n];
+    const int local = ub - heads * prefix[n];
     const int h = local / tiles, t = local % tiles;
     const int len = seq_info(p, n).len;
     Unit un;
     un.seq = n;
     un.head = h;
     un.tile = t;
-    un.cost = (t * tile_rows < len) ? unit_cost(p, backward, tile_rows, len, t) : 0;
+    un.cost = (t * tile_rows < len) ? cdiv(unit_cost(p, backward, tile_rows, len, t), ns) : 0;
     tmp[u] = un;
     atomicAdd(&hist[min(un.cost, kBuckets - 1)], 1);
   }
@@ -263,10 +267,11 @@ __global__ void __launch_bounds__(kThreads) k_build_worklist(KParams p, int back
   // 3. bucket starts, highest cost first
   bucket_starts_desc(hist, scan_smem);
 
-  // 4. scatter
+  // 4. scatter (a split forward's entries carry their part in `cost` from here on)
   for (int u = tid; u < n_units; u += kThreads) {
     Unit un = tmp[u];
     int pos = atomicAdd(&hist[min(un.cost, kBuckets - 1)], 1);
+    if (ns > 1) un.cost = u % ns;
     out[pos] = un;
   }
 }

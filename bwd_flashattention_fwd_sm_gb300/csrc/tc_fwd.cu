@@ -126,14 +126,44 @@ struct Waiter {
 };
 
 // Reads unit slot `u` (after its full barrier); false for the end sentinel.
+// Slot word 3 is 0 for the sentinel, else 1 + the unit's part of a split key
+// range (returned in un.cost; 0 when the range is not split).
 template <class SM>
 __device__ __forceinline__ bool read_unit(const SM& sm, int slot, Unit& un) {
   const volatile int* s = sm.unit_slot[slot];
   un.seq = s[0];
   un.head = s[1];
   un.tile = s[2];
+  un.cost = s[3] > 0 ? s[3] - 1 : 0;
   return s[3] != 0;
 }
+
+// The key tiles of a unit that one part of a split forward takes: entries
+// [lo, hi) of the unit's tile list, cut into p.n_split near-equal runs (dense
+// and causal lists, of n_dense entries; no split: the whole list).  Every role
+// walks the same entries, so the pipeline's rings stay in step.
+template <bool kSparse>
+struct PartList {
+  KvTileList2<kSparse> t;
+  int e, lo, hi;
+  __device__ void init(const KParams& p, int len, int q0, int part) {
+    t.init(p, len, q0);
+    e = 0;
+    lo = 0;
+    hi = INT_MAX;
+    if constexpr (!kSparse) {
+      if (p.n_split > 1) {
+        lo = part * t.n_dense / p.n_split;
+        hi = (part + 1) * t.n_dense / p.n_split;
+      }
+    }
+  }
+  __device__ bool next(int& kt, int& bits) {
+    while (e < hi && t.next(kt, bits))
+      if (e++ >= lo) return true;
+    return false;
+  }
+};
 
 // P = exp2(s * c - mu) for one 128-key row (two elements per packed FFMA2 /
 // FADD2), rounded to bf16 pairs and stored to tensor memory at `taddr` 8
@@ -274,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         s[0] = un.seq;
         s[1] = un.head;
         s[2] = un.tile;
-        s[3] = valid ? 1 : 0;
+        s[3] = valid ? 1 + (p.n_split > 1 ? un.cost : 0) : 0;
         ptx::mbar_arrive(&sm.unit_full[slot]);
       }
       ++n_units_seen;
@@ -284,9 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       const int h = un.head, g = h / p.group, q0 = un.tile * 2 * kTile;
       // which query tiles have work, for the Q loads
       bool act[2] = {false, false};
+      const int part = p.n_split > 1 ? un.cost : 0;
       {
-        KvTileList2<kSparse> t;
-        t.init(p, si.len, q0);
+        PartList<kSparse> t;
+        t.init(p, si.len, q0, part);
         int kt, bits;
         while (t.next(kt, bits)) {
           act[0] |= (bits & 0xF) != 0;
@@ -344,8 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         ++n_v;
         return true;
       };
-      KvTileList2<kSparse> t;
-      t.init(p, si.len, q0);
+      PartList<kSparse> t;
+      t.init(p, si.len, q0, part);
       int kt, bits;
       bool have = t.next(kt, bits);
       if (have && !load_k(kt)) { ok = false; break; }
@@ -403,11 +434,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       if (!valid) break;
 
       const SeqInfo si = seq_info(p, un.seq);
-      KvTileList2<kSparse> tl;
-      tl.init(p, si.len, un.tile * 2 * kTile);
+      PartList<kSparse> tl;
+      tl.init(p, si.len, un.tile * 2 * kTile, un.cost);
       int n_act = 0;
       {
-        KvTileList2<kSparse> t = tl;
+        PartList<kSparse> t = tl;
         int kt, bits;
         while (t.next(kt, bits)) n_act += ((bits >> (4 * q)) & 0xF) != 0;
       }
@@ -442,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         return true;
       };
 
-      KvTileList2<kSparse> t = tl;
+      PartList<kSparse> t = tl;
       int kt, bits;
       bool have = t.next(kt, bits);
       uint32_t cur_stage = 0;
@@ -577,8 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         sv_ref = mx;
       }
       int n_done = 0;
-      KvTileList2<kSparse> t;
-      t.init(p, si.len, un.tile * 2 * kTile);
+      PartList<kSparse> t;
+      t.init(p, si.len, un.tile * 2 * kTile, un.cost);
       int kt, bits8;
       while (t.next(kt, bits8)) {
         const int bits = (bits8 >> (4 * q)) & 0xF;
@@ -680,6 +711,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       if (n_done > 0) {
         if (!W.warp(&sm.o_final[q], n_o & 1)) { ok = false; break; }
         ptx::tc_fence_after();
+      }
+      if (p.n_split > 1) {
+        // one part of a split key range: the unnormalised O (times the V
+        // reference scale of FP8), the row max (log2 units) and the row sum
+        const bool row_ok = qi < si.len;
+        const long long rows = (long long)p.batch * p.heads_q * p.seqlen;
+        const long long ri = (long long)un.cost * rows + row_index(p, si, h, qi);
+        const float osc = kFp8 ? sv_ref : 1.f;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t orr[32];
+          if (n_done > 0) {
+            ptx::tmem_ld32(tmem + lane_base + col_o + cc * 32, orr);
+            ptx::tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orr[i] = 0u;
+          }
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(p.part_o + ri * D + cc * 32);
+#pragma unroll
+            for (int w4 = 0; w4 < 8; ++w4)
+              dst[w4] = make_float4(__uint_as_float(orr[w4 * 4 + 0]) * osc, __uint_as_float(orr[w4 * 4 + 1]) * osc,
+                                    __uint_as_float(orr[w4 * 4 + 2]) * osc, __uint_as_float(orr[w4 * 4 + 3]) * osc);
+          }
+        }
+        if (n_done > 0) {
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&sm.o_free[q]);
+          ++n_o;
+        }
+        if (row_ok) *reinterpret_cast<float2*>(p.part_ml + ri * 2) = make_float2(l > 0.f ? m_used : -INFINITY, l);
+        continue;
       }
       const float inv = l > 0.f ? (kFp8 ? sv_ref / l : 1.f / l) : 0.f;
       __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
