@@ -122,7 +122,9 @@ typedef struct {
  * SIZE_MAX if the parameters are invalid (attn_last_error() says why).  The
  * backward workspace holds the float32 dQ accumulator [rows, heads_q, D], the
  * per-row D_i = <dO_i, O_i>, the work list and, for block masks, the transposed
- * (per key block) tile lists.
+ * (per key block) tile lists.  The forward workspace holds the work list and,
+ * when there are few work units for long sequences (each unit's key range is
+ * then split into parts run on separate SMs), the parts' float32 partial results.
  */
 size_t attn_fwd_workspace_size(const attn_params_t* p);
 size_t attn_bwd_workspace_size(const attn_params_t* p);
