@@ -367,15 +367,22 @@ def run_ours(args, wl, rank, world, dist):
     return line
 
 
+# The sources that decide what the backward main kernel reads and writes: its
+# own code, the work-list order, the launch and tensor-map setup, and every
+# header.  A change elsewhere (the forward, FP8, LayerNorm kernels) leaves its
+# DRAM counters valid.
+TRAFFIC_SOURCES = ("tc_bwd.cu", "sched.cu", "api.cu", "tma_host.cu")
+
+
 def kernel_build_id():
-    """Hash of the kernel and header sources' contents (no paths, so it is the
-    same wherever the repository sits); profiles/traffic.json records the id of
-    the sources its counters were taken on."""
+    """Hash of the backward main kernel's sources' contents (no paths, so it is
+    the same wherever the repository sits); profiles/traffic.json records the id
+    of the sources its counters were taken on."""
     import hashlib
     h = hashlib.sha256()
     for d in (os.path.join(ROOT, "bwd_flashattention_fwd_sm_gb300", "csrc"), os.path.join(ROOT, "include")):
         for name in sorted(os.listdir(d)):
-            if name.endswith((".cu", ".cuh", ".h")):
+            if name in TRAFFIC_SOURCES or name.endswith((".cuh", ".h")):
                 h.update(name.encode())
                 with open(os.path.join(d, name), "rb") as f:
                     h.update(f.read())

@@ -165,17 +165,34 @@ struct PartList {
   }
 };
 
+// Stores P = 0 over eight tensor-memory columns (a 64-key half that no row of
+// the warp sees: nothing of it is read or exponentiated).
+__device__ __forceinline__ void zero_p8(uint32_t taddr) {
+  uint32_t z[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) z[i] = 0u;
+  ptx::tmem_st8(taddr, z);
+}
+
 // P = exp2(s * c - mu) for one 128-key row (two elements per packed FFMA2 /
 // FADD2), rounded to bf16 pairs and stored to tensor memory at `taddr` 8
-// columns at a time; keys outside the visibility threshold get P = 0 when
-// kMask.  Returns the row sum of the float32 P values.
-template <bool kMask>
+// columns at a time; keys at or past the visibility threshold get P = 0 when
+// kMask.  kHalf (block-sparse): the 64-key halves the row's block does not list
+// (lo_ok / hi_ok false, the same for the whole warp) are written as zeros
+// without reading S.  Returns the row sum of the float32 P values.
+template <bool kMask, bool kHalf>
 __device__ __forceinline__ float write_p(const uint32_t (&sr)[128], float c, float mu, int thr, bool lo_ok,
                                          bool hi_ok, uint32_t taddr) {
   const float2 c2 = make_float2(c, c), nmu2 = make_float2(-mu, -mu);
   float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
   for (int cc = 0; cc < 8; ++cc) {
+    if constexpr (kHalf) {
+      if (!(cc < 4 ? lo_ok : hi_ok)) {
+        zero_p8(taddr + cc * 8);
+        continue;
+      }
+    }
     uint32_t pk[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -183,8 +200,8 @@ __device__ __forceinline__ float write_p(const uint32_t (&sr)[128], float c, flo
       const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2, nmu2);
       float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
       if constexpr (kMask) {
-        if (!(k < thr && (k < 64 ? lo_ok : hi_ok))) pp.x = 0.f;
-        if (!(k + 1 < thr && (k + 1 < 64 ? lo_ok : hi_ok))) pp.y = 0.f;
+        if (!(k < thr)) pp.x = 0.f;
+        if (!(k + 1 < thr)) pp.y = 0.f;
       }
       rs2[i & 1] = __fadd2_rn(rs2[i & 1], pp);
       pk[i] = ptx::pack_bf16x2(pp.x, pp.y);
@@ -197,14 +214,20 @@ __device__ __forceinline__ float write_p(const uint32_t (&sr)[128], float c, flo
 // The FP8 form of write_p: P-hat = exp2(s * c - mu) rounded to e4m3 (mu also
 // carries the V tile's scale ratio, so P-hat stays below 2^8 < 448), four keys
 // per 32-bit column (key 4i + b in byte b), stored 8 columns = 32 keys at a time.
-// Returns the row sum of the float32 P-hat values.
-template <bool kMask>
+// Masks as write_p.  Returns the row sum of the float32 P-hat values.
+template <bool kMask, bool kHalf>
 __device__ __forceinline__ float write_p8(const uint32_t (&sr)[128], float c, float mu, int thr, bool lo_ok,
                                           bool hi_ok, uint32_t taddr) {
   const float2 c2 = make_float2(c, c), nmu2 = make_float2(-mu, -mu);
   float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
   for (int cc = 0; cc < 4; ++cc) {
+    if constexpr (kHalf) {
+      if (!(cc < 2 ? lo_ok : hi_ok)) {
+        zero_p8(taddr + cc * 8);
+        continue;
+      }
+    }
     uint32_t pk[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -214,11 +237,10 @@ __device__ __forceinline__ float write_p8(const uint32_t (&sr)[128], float c, fl
       float2 p0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
       float2 p1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
       if constexpr (kMask) {
-        const bool half_ok = k < 64 ? lo_ok : hi_ok;  // the four keys share a 64-key half
-        if (!(k < thr && half_ok)) p0.x = 0.f;
-        if (!(k + 1 < thr && half_ok)) p0.y = 0.f;
-        if (!(k + 2 < thr && half_ok)) p1.x = 0.f;
-        if (!(k + 3 < thr && half_ok)) p1.y = 0.f;
+        if (!(k < thr)) p0.x = 0.f;
+        if (!(k + 1 < thr)) p0.y = 0.f;
+        if (!(k + 2 < thr)) p1.x = 0.f;
+        if (!(k + 3 < thr)) p1.y = 0.f;
       }
       rs2[0] = __fadd2_rn(rs2[0], p0);
       rs2[1] = __fadd2_rn(rs2[1], p1);
@@ -623,13 +645,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         ++n_s;
         ptx::tc_fence_after();
         const int k0 = kt * kTile;
-        const bool need_mask = (k0 + kTile > si.len) || (elem_causal && k0 + kTile - 1 > q0) || bits != 0xF;
+        const bool need_mask = (k0 + kTile > si.len) || (elem_causal && k0 + kTile - 1 > q0);
         // Visibility of key k of this tile from this row: k < thr (sequence end and,
-        // for causal rows, the diagonal) and the row block's listed 64-key halves.
+        // for causal rows, the diagonal) and, block-sparse, the row block's listed
+        // 64-key halves (lo_ok / hi_ok: one row block per warp, so the same for the
+        // whole warp; an unlisted half is neither read nor exponentiated).
         int thr = si.len - k0;
         if (elem_causal) thr = min(thr, qi - k0 + 1);
-        const bool lo_ok = (bits >> row_half) & 1, hi_ok = (bits >> (row_half + 1)) & 1;
-        // The whole 128-column S row, read from tensor memory at once.
+        const bool lo_ok = !kSparse || ((bits >> row_half) & 1), hi_ok = !kSparse || ((bits >> (row_half + 1)) & 1);
+        // The 128-column S row (its listed halves), read from tensor memory at once.
         uint32_t sr[128];
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
@@ -640,7 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         // dependency chains short).  Masked keys are left out.
         if (c < 0.f) {
 #pragma unroll
-          for (int k = 0; k < 128; ++k) sr[k] ^= 0x80000000u;
+          for (int k = 0; k < 128; ++k)
+            if (k < 64 ? lo_ok : hi_ok) sr[k] ^= 0x80000000u;
         }
         const float ca = kFp8 ? fabsf(c) * sq * sk : fabsf(c);
         // FP8: P-hat = P r with r = sv / sv_ref in (0, 1], as 2^lr in the exponent
@@ -656,8 +681,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
 #pragma unroll
         for (int u = 0; u < 8; ++u) e8[u] = -INFINITY;
         if (!need_mask) {
+          if (lo_ok) {
 #pragma unroll
-          for (int k = 0; k < 128; ++k) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+            for (int k = 0; k < 64; ++k) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+          }
+          if (hi_ok) {
+#pragma unroll
+            for (int k = 64; k < 128; ++k) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+          }
         } else {
 #pragma unroll
           for (int k = 0; k < 128; ++k)
@@ -678,12 +709,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         // P = exp2(s' |c| - m) as bf16 pairs, written over S_q 8 columns at a time
         float rs;
         if constexpr (kFp8)
-          rs = (need_mask ? write_p8<true>(sr, ca, mu - lr, thr, lo_ok, hi_ok, tmem + lane_base + col_s)
-                          : write_p8<false>(sr, ca, mu - lr, thr, lo_ok, hi_ok, tmem + lane_base + col_s)) *
+          rs = (need_mask ? write_p8<true, kSparse>(sr, ca, mu - lr, thr, lo_ok, hi_ok, tmem + lane_base + col_s)
+                          : write_p8<false, kSparse>(sr, ca, mu - lr, thr, lo_ok, hi_ok, tmem + lane_base + col_s)) *
                inv_r;
         else
-          rs = need_mask ? write_p<true>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s)
-                         : write_p<false>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s);
+          rs = need_mask ? write_p<true, kSparse>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s)
+                         : write_p<false, kSparse>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s);
         // S_q of this tile was issued after the previous P_q V product and its
         // completion covers that product, so O_q is stable here; the next product
         // waits for p_full, so rescaling O_q now (after P is written) is in time.
@@ -1096,10 +1127,10 @@ __global__ void __launch_bounds__(kThreads256, 1) k_tc_fwd256(const __grid_const
         if (!W.warp(&sm.s_full[b], (n_t >> 1) & 1)) { ok = false; break; }
         ptx::tc_fence_after();
         const int k0 = kt * kTile;
-        const bool need_mask = (k0 + kTile > si.len) || (elem_causal && k0 + kTile - 1 > q0) || bits != 0xF;
+        const bool need_mask = (k0 + kTile > si.len) || (elem_causal && k0 + kTile - 1 > q0);
         int thr = si.len - k0;
         if (elem_causal) thr = min(thr, qi - k0 + 1);
-        const bool lo_ok = (bits >> row_half) & 1, hi_ok = (bits >> (row_half + 1)) & 1;
+        const bool lo_ok = !kSparse || ((bits >> row_half) & 1), hi_ok = !kSparse || ((bits >> (row_half + 1)) & 1);
         uint32_t sr[128];
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
@@ -1107,15 +1138,22 @@ __global__ void __launch_bounds__(kThreads256, 1) k_tc_fwd256(const __grid_const
         ptx::tmem_ld_wait();
         if (c < 0.f) {
 #pragma unroll
-          for (int k = 0; k < 128; ++k) sr[k] ^= 0x80000000u;
+          for (int k = 0; k < 128; ++k)
+            if (k < 64 ? lo_ok : hi_ok) sr[k] ^= 0x80000000u;
         }
         const float ca = fabsf(c);
         float e8[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) e8[u] = -INFINITY;
         if (!need_mask) {
+          if (lo_ok) {
 #pragma unroll
-          for (int k = 0; k < 128; ++k) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+            for (int k = 0; k < 64; ++k) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+          }
+          if (hi_ok) {
+#pragma unroll
+            for (int k = 64; k < 128; ++k) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+          }
         } else {
 #pragma unroll
           for (int k = 0; k < 128; ++k)
@@ -1133,8 +1171,8 @@ __global__ void __launch_bounds__(kThreads256, 1) k_tc_fwd256(const __grid_const
           m_used = m_new;
         }
         const float mu = m_used == -INFINITY ? 0.f : m_used;
-        const float rs = need_mask ? write_p<true>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s)
-                                   : write_p<false>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s);
+        const float rs = need_mask ? write_p<true, kSparse>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s)
+                                   : write_p<false, kSparse>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s);
         // Rescaling O: the previous tile's P V products may still run (S of this
         // tile was issued before them), so wait for them first.  The products
         // of this tile wait for p_full, so rescaling now is in time.
