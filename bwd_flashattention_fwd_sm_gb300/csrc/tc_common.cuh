@@ -152,9 +152,21 @@ template <bool kSparse>
 struct KvTileList2 {
   int n_dense, it, len, q0;
   const int* col;
+  // Block-sparse: per query block r, the next two listed key blocks below the
+  // sequence's block count (w0 < w1; INT_MAX past the list) and the index of the
+  // entry after them.  A key tile holds at most two of a block's entries, so the
+  // window always covers it; each call refills what it used, and those loads are
+  // first read by the next call, so no call waits on its own loads.
   int s[kSparse ? 4 : 1], e[kSparse ? 4 : 1];
+  int w0[kSparse ? 4 : 1], w1[kSparse ? 4 : 1];
   int nblk;
   bool causal;
+
+  __device__ int entry(int i, int end) const {
+    if (i >= end) return INT_MAX;
+    const int c = __ldg(col + i);
+    return c < nblk ? c : INT_MAX;  // ascending: every later entry is past the end too
+  }
 
   __device__ void init(const KParams& p, int len_, int q0_) {
     len = len_;
@@ -177,6 +189,9 @@ struct KvTileList2 {
         } else {
           s[r] = e[r] = 0;
         }
+        w0[r] = entry(s[r], e[r]);
+        w1[r] = entry(s[r] + 1, e[r]);
+        s[r] += 2;
       }
     }
   }
@@ -196,19 +211,25 @@ struct KvTileList2 {
       }
       return true;
     } else {
-      int m = INT_MAX;
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-        if (s[r] < e[r] && col[s[r]] < nblk) m = min(m, col[s[r]]);
+      const int m = min(min(w0[0], w0[1]), min(w0[2], w0[3]));
       if (m == INT_MAX) return false;
       kt = m >> 1;
       bits = 0;
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-        while (s[r] < e[r] && col[s[r]] < nblk && (col[s[r]] >> 1) == kt) {
-          bits |= 1 << (2 * r + (col[s[r]] & 1));
-          ++s[r];
+      for (int r = 0; r < 4; ++r) {
+        if ((w0[r] >> 1) != kt) continue;
+        bits |= 1 << (2 * r + (w0[r] & 1));
+        if ((w1[r] >> 1) == kt) {  // both key halves listed
+          bits |= 1 << (2 * r + (w1[r] & 1));
+          w0[r] = entry(s[r], e[r]);
+          w1[r] = entry(s[r] + 1, e[r]);
+          s[r] += 2;
+        } else {
+          w0[r] = w1[r];
+          w1[r] = entry(s[r], e[r]);
+          s[r] += 1;
         }
+      }
       return true;
     }
   }
