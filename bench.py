@@ -669,124 +669,15 @@ def run_fp8(args, wl):
 
 
 def run_d256(args):
-    """Head dim 256: the tensor-core forward at B=2, H=16, S=8192 (the step and the
-    roofline), and the float32-arithmetic backward at B=1, H=8, S=4096 (reported
-    beside it against the CUDA-core float32 FMA peak)."""
-    import ctypes
-
-    import torch
-
-    from bwd_flashattention_fwd_sm_gb300 import attn_bwd, attn_fwd, get_status
-    from bwd_flashattention_fwd_sm_gb300 import _lib
+    """Head dim 256: the forward and backward step on d256_dense_s8192 (B=2, H=16,
+    S=8192), both passes on the tensor cores, measured like the main step."""
     from bwd_flashattention_fwd_sm_gb300 import workloads as W
-
-    lib = _lib.load()
-    dev = torch.device("cuda", torch.cuda.current_device())
     wl = W.WORKLOADS["d256_dense_s8192"]
-    wb = W.WORKLOADS["d256_dense_s4096"]
-    fwd_flops, _, _ = flops_of(wl)
-    _, bwd_flops, _ = flops_of(wb)
-    inp = W.make_inputs(wl)
-    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
-    ib = W.make_inputs(wb)
-    qb, kb, vb, dob = (ib[n].to(dev) for n in ("q", "k", "v", "do"))
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-    ob, lseb = attn_fwd(qb, kb, vb, scale=wb.scale)
-    for _ in range(args.warmup):
-        attn_fwd(q, k, v, scale=wl.scale)
-        attn_bwd(qb, kb, vb, ob, dob, lseb, scale=wb.scale)
-    torch.cuda.synchronize()
-    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    fwd_ev = [(ev(), ev()) for _ in range(args.steps)]
-    step_ev = [(ev(), ev()) for _ in range(args.steps)]
-    bwd_ev = [(ev(), ev()) for _ in range(args.steps)]
-    for pair in fwd_ev + bwd_ev:
-        for e in pair:
-            e.record(stream)
-    torch.cuda.synchronize()
-    clocks = ClockSampler(gpu_identity(torch))
-    clocks.start()
-    time.sleep(0.3)
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
-        lib.attn_set_timing_events(0, ctypes.c_void_p(fwd_ev[i][0].cuda_event), ctypes.c_void_p(fwd_ev[i][1].cuda_event))
-        step_ev[i][0].record(stream)
-        attn_fwd(q, k, v, scale=wl.scale)
-        step_ev[i][1].record(stream)
-    lib.attn_set_timing_events(0, None, None)
-    bsteps = max(1, min(args.steps, 3))
-    for i in range(bsteps):
-        flush.fill_(i & 0xFF)
-        lib.attn_set_timing_events(1, ctypes.c_void_p(bwd_ev[i][0].cuda_event), ctypes.c_void_p(bwd_ev[i][1].cuda_event))
-        attn_bwd(qb, kb, vb, ob, dob, lseb, scale=wb.scale)
-    lib.attn_set_timing_events(1, None, None)
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    if get_status() != 0:
-        raise RuntimeError("device status word set during the benchmark")
-    step_ms = sum(a.elapsed_time(b) for a, b in step_ev) / args.steps
-    fwd_ms = sum(a.elapsed_time(b) for a, b in fwd_ev) / args.steps
-    bwd_ms = sum(a.elapsed_time(b) for a, b in bwd_ev[:bsteps]) / bsteps
-    value = fwd_flops / (step_ms * 1e-3) / 1e12
-    fwd_t = fwd_flops / (fwd_ms * 1e-3) / 1e12
-    bwd_t = bwd_flops / (bwd_ms * 1e-3) / 1e12
-    # end to end: inputs from pinned host memory, O and LSE back, every step
-    host_in = [t.cpu().pin_memory() for t in (q, k, v)]
-    o0, l0 = attn_fwd(q, k, v, scale=wl.scale)
-    ho = torch.empty(o0.shape, dtype=o0.dtype, pin_memory=True)
-    hl = torch.empty(l0.shape, dtype=l0.dtype, pin_memory=True)
-    e2e_steps = max(1, min(args.steps, 10))
-    torch.cuda.synchronize()
-    e0, e1 = ev(), ev()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        dq_, dk_, dv_ = (h.to(dev, non_blocking=True) for h in host_in)
-        o2, l2 = attn_fwd(dq_, dk_, dv_, scale=wl.scale)
-        ho.copy_(o2, non_blocking=True)
-        hl.copy_(l2, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e = fwd_flops * e2e_steps / (e0.elapsed_time(e1) * 1e-3) / 1e12
-    peaks, src = load_peaks()
-    peak = peak_value(peaks, "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    mhz = clk.get("sm_mhz") or 2070.0
-    fp32_peak = sms * 128 * 2 * mhz * 1e6 / 1e12
-    line = {
-        "metric": "attention forward TFLOPS at head dim 256 (bf16, S=8192) and % of GB300 BF16 tensor peak",
-        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic: Q,K,V iid N(0,1) from a fixed seed, rounded to bf16",
-        "config": {"workload": wl.name, "batch": wl.batch, "heads_q": wl.heads_q, "heads_kv": wl.heads_kv,
-                   "seq_len": wl.seqlen, "head_dim": 256, "mask": wl.mask, "step": "attn_fwd",
-                   "l2": "512 MiB L2 flush written between timed steps (outside the step events)",
-                   "fwd_flops": fwd_flops},
-        "fwd_ms": round(fwd_ms, 4), "fwd_tflops": round(fwd_t, 2),
-        "roofline": {"kernel": "head-dim-256 forward (k_tc_fwd256)", "bound": "tensor", "achieved": round(fwd_t, 2),
-                     "peak": peak, "unit": "TFLOP/s", "frac": round(fwd_t / peak, 4), "traffic": None,
-                     "peak_source": f"{src} bf16 dense"},
-        "aux": {"backward_d256": {
-            "workload": wb.name, "ms": round(bwd_ms, 3), "tflops": round(bwd_t, 3), "flops": bwd_flops,
-            "kernel": "float32-arithmetic backward (k_simt_bwd256), preprocess and dQ conversion excluded",
-            "bound": "alu", "peak": round(fp32_peak, 1),
-            "peak_source": f"{sms} SMs x 128 float32 FMA lanes x 2 FLOP x {mhz:.0f} MHz (sampled clock)",
-            "frac": round(bwd_t / fp32_peak, 4)}},
-        "e2e": {"value": round(e2e, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": sum(t.numel() * 2 for t in host_in),
-                "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4, "steps": e2e_steps},
-        "gpu_launches": 2 * args.steps + 3 * bsteps,
-        "clocks": clk,
-    }
+    line = run_ours(args, wl, 0, 1, None)
+    line["metric"] = "attention fwd+bwd TFLOPS at head dim 256 (bf16, S=8192) and % of GB300 BF16 tensor peak"
+    line["roofline"]["kernel"] = "head-dim-256 backward (k_tc_bwd256: each key tile once per head-dim half)"
     if not args.no_cpu_baseline:
-        import oracle
-        t0 = time.perf_counter()
-        one = [inp[n][0:1, 0:1].double().numpy() for n in ("q", "k", "v")]
-        oracle.attn_fwd(*one, scale=wl.scale)
-        sec = time.perf_counter() - t0
-        per_head = fwd_flops / wl.heads_q / wl.batch
-        line["cpu_baseline"] = {"value": per_head / sec / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count() or 1,
-                                "kind": "oracle", "sample": f"1 head of {wl.name} at full length, float64 forward",
-                                "seconds": round(sec, 2)}
+        line["cpu_baseline"] = cpu_baseline(wl)
     return line
 
 
@@ -803,7 +694,7 @@ def main():
     ap.add_argument("--fp8", action="store_true",
                     help="measure the FP8 (e4m3) forward (quantisation + forward) on --workload")
     ap.add_argument("--d256", action="store_true",
-                    help="measure head dim 256: the forward at S=8192 and the backward at S=4096")
+                    help="measure head dim 256: forward and backward at B=2, H=16, S=8192")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

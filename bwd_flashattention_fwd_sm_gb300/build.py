@@ -23,7 +23,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgbattn.so")
 
 SOURCES = ["api.cu", "sched.cu", "bwd_aux.cu", "simt_attn.cu", "tma_host.cu", "tc_fwd.cu", "tc_bwd.cu", "tc_dq.cu",
-           "noalloc.cu", "ln.cu", "fp8.cu"]
+           "noalloc.cu", "ln.cu", "fp8.cu", "tc_bwd256.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", CSRC, "-I", INCLUDE]

@@ -83,13 +83,11 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 // Which kernel family serves these parameters: the tensor-core kernels for bf16
-// with head_dim 64 or 128 (and the forward at 256), the float32-arithmetic
-// kernels for float32 I/O and for the bf16 backward at head_dim 256 (its dK and
-// dV accumulators for a 128-key tile would fill all of tensor memory).
+// (head_dim 64, 128 or 256; the backward at 256 takes each key tile once per
+// half of the head dim), the float32-arithmetic kernels for float32 I/O.
 bool use_tensor_cores(const attn_params_t* p, bool backward) {
   const bool avail = backward ? tc_bwd_available() : tc_fwd_available();
-  return avail && p->dtype == ATTN_BF16 &&
-         (p->head_dim == 128 || p->head_dim == 64 || (!backward && p->head_dim == 256));
+  return avail && p->dtype == ATTN_BF16 && (p->head_dim == 128 || p->head_dim == 64 || p->head_dim == 256);
 }
 
 struct Problem {
@@ -517,7 +515,7 @@ attn_status_t bwd_impl(const attn_params_t* p, const void* q, const void* k, con
   Problem pr;
   attn_status_t s = validate_params(p, &pr);
   if (s != ATTN_OK) return s;
-  if (deterministic && !use_tensor_cores(p, true))
+  if (deterministic && (!use_tensor_cores(p, true) || p->head_dim == 256))
     return fail(ATTN_ERR_UNSUPPORTED,
                 "the deterministic backward runs on the tensor-core path only (bf16, head_dim 64 or 128)");
   if (pr.empty) return ATTN_OK;
@@ -579,7 +577,8 @@ attn_status_t bwd_impl(const attn_params_t* p, const void* q, const void* k, con
     return cuda_fail(e, "timing event");
   if (g_timing_events[1][0] && (e = cudaEventRecord(g_timing_events[1][0], st)) != cudaSuccess)
     return cuda_fail(e, "timing event");
-  if (use_tensor_cores(p, true)) e = launch_tc_bwd(kp, sms, st, !deterministic);
+  if (use_tensor_cores(p, true))
+    e = p->head_dim == 256 ? launch_tc_bwd256(kp, sms, st) : launch_tc_bwd(kp, sms, st, !deterministic);
   else e = launch_simt_bwd(kp, bf16, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   if (deterministic && (e = launch_tc_dq(kq, sms, st)) != cudaSuccess) return cuda_fail(e, "dQ pass launch");

@@ -16,6 +16,9 @@ cudaError_t launch_tc_fwd(const KParams& p, int sms, cudaStream_t st);
 // with_dq: also add dQ into p.dq_accum (L2 reductions, order not fixed);
 // otherwise dK and dV only.
 cudaError_t launch_tc_bwd(const KParams& p, int sms, cudaStream_t st, bool with_dq);
+// Head dim 256: each 128-key unit taken twice (tickets 2u and 2u + 1 of
+// p.unit_counter), once per half of the head dim; dQ added into p.dq_accum.
+cudaError_t launch_tc_bwd256(const KParams& p, int sms, cudaStream_t st);
 // Query-stationary dQ (fixed summation order) straight to p.dq as bf16; needs
 // p.delta from the preprocess and the forward's work list.
 cudaError_t launch_tc_dq(const KParams& p, int sms, cudaStream_t st);

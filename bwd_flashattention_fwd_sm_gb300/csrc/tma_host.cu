@@ -83,10 +83,11 @@ cudaError_t make_byte_map(TileMap* out, const void* base, long long x_extent, lo
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t make_acc_map(TileMap* out, float* base, const KParams& p, int box_rows) {
+cudaError_t make_acc_map(TileMap* out, float* base, const KParams& p, int box_rows, int box_cols) {
   EncodeFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const long long D = p.head_dim, H = p.heads_q, E = 4;
+  const cuuint32_t bc = (cuuint32_t)(box_cols > 0 ? box_cols : D);
   cuuint64_t dims[4], strides[3];
   cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
   if (p.varlen) {
@@ -95,14 +96,14 @@ cudaError_t make_acc_map(TileMap* out, float* base, const KParams& p, int box_ro
     strides[0] = D * E;
     strides[1] = H * D * E;
     strides[2] = H * D * E * (p.total_tokens > 0 ? p.total_tokens : 1);
-    box[0] = (cuuint32_t)D; box[1] = 1; box[2] = box_rows; box[3] = 1;
+    box[0] = bc; box[1] = 1; box[2] = box_rows; box[3] = 1;
   } else {
     out->rows_inner = 1;
     dims[0] = D; dims[1] = p.seqlen; dims[2] = H; dims[3] = p.batch;
     strides[0] = D * E;
     strides[1] = (long long)p.seqlen * D * E;
     strides[2] = H * p.seqlen * D * E;
-    box[0] = (cuuint32_t)D; box[1] = box_rows; box[2] = 1; box[3] = 1;
+    box[0] = bc; box[1] = box_rows; box[2] = 1; box[3] = 1;
   }
   std::memset(&out->map, 0, sizeof(out->map));
   CUresult r = enc(&out->map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,

@@ -31,8 +31,9 @@ cudaError_t make_byte_map(TileMap* out, const void* base, long long x_extent, lo
                           long long batch, long long row_bytes);
 
 // Map of the float32 dQ accumulator (rows laid out like a contiguous q) for
-// TMA reduce-adds of 64-row x 128-column tiles (no swizzle, 512-byte rows).
+// TMA reduce-adds of box_rows x box_cols tiles (no swizzle; box_cols 0: the
+// whole head dim).
 //   fixed length: dims (d, position, head, batch); variable: (d, head, token, 1).
-cudaError_t make_acc_map(TileMap* out, float* base, const KParams& p, int box_rows);
+cudaError_t make_acc_map(TileMap* out, float* base, const KParams& p, int box_rows, int box_cols = 0);
 
 }  // namespace gbattn

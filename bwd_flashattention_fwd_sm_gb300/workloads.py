@@ -72,7 +72,6 @@ WORKLOADS = {
     "h2_causal_s8192_d64": Workload("h2_causal_s8192_d64", 2, 16, 16, 8192, 64, "bf16", "causal", seed=8),
     # head dim 256: the forward at the headline length, the backward at a quarter of it
     "d256_dense_s8192": Workload("d256_dense_s8192", 2, 16, 16, 8192, 256, "bf16", "none", seed=10),
-    "d256_dense_s4096": Workload("d256_dense_s4096", 1, 8, 8, 4096, 256, "bf16", "none", seed=10),
 }
 
 

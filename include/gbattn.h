@@ -43,8 +43,8 @@
  *                   *_stride_s (between tokens) and *_stride_h; *_stride_b ignored.
  *                   lse: contiguous float32 [heads_q, T].
  *
- * Constraints.  head_dim 64, 128 or 256 (both types; at 256 the bf16 forward
- * runs on the tensor cores and the backward on the float32-arithmetic kernels);
+ * Constraints.  head_dim 64, 128 or 256 (both types; bf16 runs on the tensor
+ * cores at every head dim, the deterministic backward at 64 and 128 only);
  * heads_q % heads_kv == 0; every tensor pointer 16-byte aligned; strides
  * multiples of 8 elements (16 bytes) for bf16 and 4 elements for float32.
  *

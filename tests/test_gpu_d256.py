@@ -1,10 +1,10 @@
 """GPU parity at head dim 256 against the float64 oracle.
 
-bf16: the forward runs on the tensor cores (one 128-row query tile per unit,
-two S buffers and a 256-column O in tensor memory); the backward runs on the
-float32-arithmetic kernels (a 128-key tile's dK and dV accumulators would fill
-all of tensor memory).  float32 I/O runs both on the float32 kernels.
-Tolerances are those of every other test (parity_util).
+bf16 runs both passes on the tensor cores.  The forward takes one 128-row query
+tile per unit, with two S buffers and a 256-column O in tensor memory.  The
+backward takes each 128-key tile twice, once per half of the head dim for dK,
+dV and dQ, in 32-row query steps.  float32 I/O runs both passes on the float32
+kernels.  Tolerances are those of every other test (parity_util).
 """
 
 import numpy as np
@@ -60,6 +60,20 @@ def test_forward_full_size_sampled_head_d256(mask, b, h):
     ref = oracle_run(wl.with_(batch=1, heads_q=1, heads_kv=1), one, passes="fwd")
     sub = {n: got[n][b:b + 1, h:h + 1] for n in ("o", "lse")}
     check_all(wl, sub, ref, names=("o", "lse"))
+
+
+@pytest.mark.parametrize("mask,b,h", [("none", 1, 5), ("causal", 0, 12)])
+def test_backward_full_size_sampled_head_d256(mask, b, h):
+    """B = 2, H = 16, S = 8192, D = 256 (the benchmarked step): forward and
+    backward of every head on the GPU, one head's O, LSE, dQ, dK and dV
+    against the oracle."""
+    wl = W.Workload("d256_s8192_bwd", 2, 16, 16, 8192, 256, "bf16", mask, seed=65)
+    inp = W.make_inputs(wl)
+    got = gpu_run(wl, inp)
+    one = {n: inp[n][b:b + 1, h:h + 1] for n in ("q", "k", "v", "do")}
+    ref = oracle_run(wl.with_(batch=1, heads_q=1, heads_kv=1), one)
+    sub = {n: got[n][b:b + 1, h:h + 1] for n in ("o", "lse", "dq", "dk", "dv")}
+    check_all(wl, sub, ref)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
