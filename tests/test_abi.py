@@ -262,7 +262,8 @@ def test_fp8_validation(lib):
 
 def test_head_dim_256_accepted(lib):
     """head_dim 256: forward and backward accepted (both dtypes); the deterministic
-    backward, which needs the tensor-core backward, is refused."""
+    backward is refused (its query-stationary dQ pass covers head dims 64 and
+    128 only)."""
     for dtype in (_lib.ATTN_BF16, _lib.ATTN_F32):
         p = params(D=256, dtype=dtype)
         assert fwd(lib, p) == _lib.ATTN_ERR_CUDA
