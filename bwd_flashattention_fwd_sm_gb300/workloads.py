@@ -70,7 +70,7 @@ WORKLOADS = {
     # head dim 64 at the headline length (bf16 on the tensor cores)
     "h2_dense_s8192_d64": Workload("h2_dense_s8192_d64", 2, 16, 16, 8192, 64, "bf16", "none", seed=8),
     "h2_causal_s8192_d64": Workload("h2_causal_s8192_d64", 2, 16, 16, 8192, 64, "bf16", "causal", seed=8),
-    # head dim 256: the forward at the headline length, the backward at a quarter of it
+    # head dim 256 at the headline length, forward and backward
     "d256_dense_s8192": Workload("d256_dense_s8192", 2, 16, 16, 8192, 256, "bf16", "none", seed=10),
 }
 

@@ -5,20 +5,35 @@ Tolerances (written here, used by every GPU test):
   float32 I/O : max |gpu - oracle| <= 1e-3 on O, LSE, dQ, dK, dV (the 1e-3
                 alignment bar of the zwxr.cn CANN ops-nn article, section 3.4,
                 read as an absolute bound).
-  bfloat16 I/O: |gpu - oracle| <= 2e-2 + 2^-7 |oracle| element-wise, and
+  bfloat16 I/O: |gpu - oracle| <= 2e-2 + half_ulp(oracle) element-wise, and
                 ||gpu - oracle||_2 / ||oracle||_2 <= 1e-2 per tensor; LSE
-                (float32) max-abs <= 2e-2.  The 2e-2 bound is for unit-scale
-                values; a bf16 output of magnitude >= 4 cannot hold it by itself
-                (its spacing is 2^-5 and above), so each element also gets one
-                bf16 unit in the last place of its own magnitude (2^-7 |x| bounds it).
-                dK and dV of a KV head are sums over its group of G query heads,
-                each head adding its own bf16 rounding of dS and P, so their
-                absolute error grows like sqrt(G): the 2e-2 term is read at the
-                largest group of the configurations (G = 4, the causal GQA one)
-                and scaled by sqrt(G / 4) above it.
+                (float32) max-abs <= 2e-2.  half_ulp(x) is half the spacing of
+                bfloat16 numbers at |x| (2^(e-8) for |x| in [2^e, 2^(e+1))): the
+                distance by which rounding the exact value to a bf16 output can
+                move it by itself.  Below |x| = 8 that is under 2^-6 < 2e-2, so
+                the term matters only for outputs the 2e-2 bar alone could not
+                hold even when rounded correctly.
+  GQA groups  : dK and dV of a KV head sum the contributions of its G query
+                heads, each product taking its own bf16 rounding of P (dV) or
+                dS (dK) with float32 accumulation, the arithmetic the method
+                prescribes.  Independent roundings add in quadrature, so the
+                error of a group sum grows like sqrt(G).  The 2e-2 term is the
+                stated bar at the largest group of the configurations (G = 4,
+                the causal GQA one) and scales by sqrt(G / 4) above it; G <= 4
+                keeps 2e-2.  tests/test_tolerance.py replays that rounding in
+                float64 for G = 1, 4, 16: its RMS error doubles with each
+                fourfold G, at G = 16 the replay itself breaks the unscaled bar,
+                and the scaled bar holds it with room to spare.
+
+Margins: with GBATTN_PARITY_LOG set to a file path, every comparison appends one
+JSON line (name, dtype, max-abs, rel-L2, the largest ratio of error to its
+bound, element count) to that file before asserting.
 """
 
 from __future__ import annotations
+
+import json
+import os
 
 import numpy as np
 import torch
@@ -30,7 +45,28 @@ from bwd_flashattention_fwd_sm_gb300 import workloads as W
 TOL_F32 = 1e-3
 TOL_BF16_ABS = 2e-2
 TOL_BF16_REL = 1e-2
-TOL_BF16_ULP = 2.0 ** -7
+
+
+def half_ulp_bf16(x):
+    """Half the spacing of bfloat16 numbers at |x| (8 significant bits): for |x|
+    in [2^e, 2^(e+1)) the spacing is 2^(e-7); 0 where x is 0."""
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    _, ex = np.frexp(x)  # x = m 2^ex with m in [0.5, 1), so e = ex - 1
+    return np.where(x > 0, np.ldexp(1.0, ex - 9), 0.0)
+
+
+def _log_margin(name, dtype, max_abs, rel, ratio, n):
+    path = os.environ.get("GBATTN_PARITY_LOG")
+    if not path:
+        return
+    with open(path, "a") as f:
+        f.write(json.dumps({"name": name, "dtype": dtype, "max_abs": max_abs, "rel_l2": rel,
+                            "worst_err_over_bound": ratio, "n": int(n)}) + "\n")
+
+
+def group_scale(group: int) -> float:
+    """Factor on the 2e-2 term for dK and dV of a KV head shared by `group` query heads."""
+    return max(1.0, (group / 4.0) ** 0.5)
 
 
 def compare(name, got, ref, dtype, abs_scale=1.0):
@@ -49,14 +85,17 @@ def compare(name, got, ref, dtype, abs_scale=1.0):
     nrm = float(np.linalg.norm(r))
     rel = float(np.linalg.norm(g - r) / nrm) if nrm > 0 else float(np.linalg.norm(g - r))
     if dtype == "f32":
-        assert max_abs <= TOL_F32, f"{name}: max-abs {max_abs:.3e} > {TOL_F32}"
+        bound = np.full_like(r, TOL_F32)
     elif name.startswith("lse"):
-        assert max_abs <= TOL_BF16_ABS, f"{name}: max-abs {max_abs:.3e} > {TOL_BF16_ABS}"
+        bound = np.full_like(r, TOL_BF16_ABS)
     else:
-        bound = TOL_BF16_ABS * abs_scale + TOL_BF16_ULP * np.abs(r)
-        worst = int(np.argmax(err - bound))
-        assert np.all(err <= bound), (f"{name}: |err| {err[worst]:.3e} > {bound[worst]:.3e} at value "
-                                      f"{r[worst]:.4f} (max-abs {max_abs:.3e})")
+        bound = TOL_BF16_ABS * abs_scale + half_ulp_bf16(r)
+    ratio = err / bound
+    worst = int(np.argmax(ratio))
+    _log_margin(name, dtype, max_abs, rel, float(ratio[worst]), g.size)
+    assert np.all(err <= bound), (f"{name}: |err| {err[worst]:.3e} > {bound[worst]:.3e} at value "
+                                  f"{r[worst]:.4f} (max-abs {max_abs:.3e})")
+    if dtype != "f32" and not name.startswith("lse"):
         assert rel <= TOL_BF16_REL, f"{name}: rel-L2 {rel:.3e} > {TOL_BF16_REL}"
     return max_abs, rel
 
@@ -112,6 +151,6 @@ def check_all(wl, got, ref, names=("o", "lse", "dq", "dk", "dv")):
     group = wl.heads_q // wl.heads_kv
     for n in names:
         if n in ref:
-            scale = max(1.0, (group / 4.0) ** 0.5) if n in ("dk", "dv") else 1.0
+            scale = group_scale(group) if n in ("dk", "dv") else 1.0
             report[n] = compare(f"{n}[{wl.name}]", got[n], ref[n], wl.dtype, abs_scale=scale)
     return report

@@ -2,8 +2,8 @@
 binding) against the float64 oracle (oracle/ln.py) on seeded inputs.
 
 Tolerances:
-  y    bf16: the bf16 bound of every other test (2e-2 + 2^-7 |ref| element-wise,
-       rel-L2 1e-2); float32: max-abs 1e-3 (the float32 bar of the attention tests).
+  y    bf16: the bf16 bound of every other test (2e-2 + half a bf16 unit in the
+       last place of ref, element-wise; rel-L2 1e-2); float32: max-abs 1e-3 (the float32 bar of the attention tests).
   h    the float32 sum rounded once to the I/O type: within half a unit in the
        last place of the exact sum (at most 2^-8 |h| for bf16, with 8 significand
        bits, and 2^-24 |h| for float32), plus 1e-30 for exact zeros.
