@@ -1,12 +1,12 @@
 // Backward pass for callers that cannot allocate device memory.
 //
-// Some callers have no way to hand the library a workspace: code that runs while
-// a stream is being captured into a CUDA graph (a plain cudaMalloc is not allowed
-// there), engines that fix their memory budget at start-up and forbid any later
-// allocation, and plug-ins living inside a host framework that owns the device
-// allocator and does not share it.  attn_bwd_noalloc serves them: its scratch
-// space is a fixed array in this library's own device memory, created when the
-// library's device code is loaded on a GPU and held until the process exits.
+// Some callers may not call cudaMalloc at all: engines that fix their device
+// memory budget at start-up and forbid any allocation afterwards, and plug-ins
+// living inside a host framework that owns the device allocator and shares none
+// of it.  They cannot hand the library a workspace.  attn_bwd_noalloc serves
+// them: its scratch space is a fixed array in this library's own device memory,
+// created when the library's device code is loaded on a GPU and held until the
+// process exits.
 //
 // The array is shared by every call: calls whose work overlaps on the GPU race on
 // it (queue them on one stream, or wait between them).  Nothing in it has to
@@ -41,6 +41,11 @@ extern "C" attn_status_t attn_bwd_noalloc(const attn_params_t* p, const void* q,
   // code before touching anything.
   if (need == SIZE_MAX) return attn_bwd(p, q, k, v, o, dout, lse, dq, dk, dv, nullptr, 0, stream);
   if (need > ATTN_NOALLOC_SCRATCH_BYTES) {
+    // attn_bwd's own pointer checks come first, so a bad pointer gets the same
+    // code here as there; with no workspace it stops at its workspace check,
+    // before anything is queued.
+    const attn_status_t s = attn_bwd(p, q, k, v, o, dout, lse, dq, dk, dv, nullptr, 0, stream);
+    if (s != ATTN_ERR_WORKSPACE) return s;
     char buf[200];
     snprintf(buf, sizeof(buf),
              "attn_bwd_noalloc: this problem needs %zu bytes of scratch, above the fixed %zu-byte array; "

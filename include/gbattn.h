@@ -225,21 +225,22 @@ attn_status_t attn_fwd_fp8(const attn_params_t* p, const void* q8, const void* k
 
 /*
  * Backward pass that allocates nothing.  The pages have no counterpart to this
- * entry point: it exists for callers that cannot allocate device memory and so
- * cannot pass a workspace -- code running while a stream is captured into a CUDA
- * graph (cudaMalloc is not allowed there), engines that fix their memory budget at
- * start-up, plug-ins inside a framework that owns the device allocator.
+ * entry point: it exists for callers that may not allocate device memory and so
+ * cannot pass a workspace -- engines that fix their device memory budget at
+ * start-up and forbid any later allocation, and plug-ins inside a host
+ * framework that owns the device allocator and shares none of it.
  *
  * Same arguments, results and errors as attn_bwd, minus the workspace: scratch
  * space is a fixed array of ATTN_NOALLOC_SCRATCH_BYTES inside the library's device
  * memory, which every GPU that loads the library holds until the process exits.
  * A problem whose attn_bwd_workspace_size() exceeds that size is rejected with
  * ATTN_ERR_WORKSPACE before anything is queued (attn_last_error() gives both
- * sizes).  The first call on each device looks up the array's device address
- * (with that device current); make that first call before any stream capture.
- * Every call shares the one array: calls whose work overlaps on the GPU race on
- * it, so queue them on one stream or wait between them.  No call depends on what
- * a previous call left in the array.
+ * sizes), after the argument checks attn_bwd makes, so an invalid argument gets
+ * attn_bwd's code.  The first call on each device looks up the array's device
+ * address (with that device current); make that first call before any stream
+ * capture.  Every call shares the one array: calls whose work overlaps on the
+ * GPU race on it, so queue them on one stream or wait between them.  No call
+ * depends on what a previous call left in the array.
  */
 #define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 attn_status_t attn_bwd_noalloc(const attn_params_t* p, const void* q, const void* k, const void* v,
