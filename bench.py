@@ -389,6 +389,25 @@ def kernel_build_id():
     return h.hexdigest()[:16]
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu's "Model name", else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
 def cpu_baseline(wl, budget_s=20.0, rank=0):
     """The float64 oracle on a bounded sample of the workload: whole heads at full length."""
     import oracle
@@ -423,9 +442,10 @@ def cpu_baseline(wl, budget_s=20.0, rank=0):
         if time.perf_counter() - t0 >= budget_s * 0.5 or heads_done >= 4:
             break
     dt = time.perf_counter() - t0
-    return {"value": flops_done / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+    return {"value": flops_done / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "cpu_model": cpu_model(),
+            "kind": "oracle",
             "sample": f"{heads_done} head(s) of {wl.name} at full length (fwd+bwd, float64), {dt:.1f} s",
-            "seconds": round(dt, 2)}
+            "seconds": round(dt, 2), "heads": heads_done}
 
 
 def run_reference(args, wl):
@@ -449,8 +469,10 @@ def run_reference(args, wl):
                    "seq_len": wl.seqlen, "head_dim": wl.head_dim, "mask": wl.mask,
                    "sample": "each step: whole heads at full length, bounded to a few seconds"},
         "impl": "reference",
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": base["cores"], "kind": "oracle",
-                         "sample": base["sample"]},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": base["cores"],
+                         "cpu_model": base["cpu_model"], "kind": "oracle", "sample": base["sample"],
+                         "seconds_per_step": statistics.mean(r["seconds"] for r in per_step),
+                         "heads_per_step": base["heads"]},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     return line

@@ -111,19 +111,30 @@ _lock = threading.Lock()
 _lib = None
 
 
+def checked_mode() -> bool:
+    """GBATTN_CHECKED=1 in the environment selects the checked library: every
+    device-computed index is compared with its tensor's extent before the access
+    (a failure records ATTN_ERR_DEVICE_BOUNDS and skips the access)."""
+    return os.environ.get("GBATTN_CHECKED", "0") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.LIB_CHECKED if checked_mode() else _build.LIB
 
 
 def load(build_if_missing: bool = True):
-    """Load libgbattn.so (building it first if needed) and set up signatures."""
+    """Load libgbattn.so, or libgbattn_checked.so under GBATTN_CHECKED=1 (building
+    both first if needed), and set up signatures."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.build() if build_if_missing else _build.LIB
+        if build_if_missing:
+            _build.build()
+        path = library_path()
         if not os.path.exists(path):
-            raise RuntimeError(f"libgbattn.so not found at {path}; build it with bwd_flashattention_fwd_sm_gb300.build")
+            raise RuntimeError(f"{os.path.basename(path)} not found at {path}; "
+                               "build it with bwd_flashattention_fwd_sm_gb300.build")
         lib = ctypes.CDLL(path)
         for name, (res, args) in SIGNATURES.items():
             fn = getattr(lib, name)

@@ -247,6 +247,7 @@ KParams base_kparams(const attn_params_t* p, const Problem& pr) {
     k.col_idx = p->block_mask->col_idx;
     k.n_row_blocks = p->block_mask->n_row_blocks;
     k.n_col_blocks = p->block_mask->n_col_blocks;
+    k.nnz = p->block_mask->nnz;
     k.causal_in_block = p->block_mask->causal_in_block ? 1 : 0;
   }
   k.wait_limit_ns = wait_limit_ns();
@@ -652,7 +653,7 @@ attn_status_t attn_set_timing_events(int which, void* start, void* stop) {
   return ATTN_OK;
 }
 
-const char* attn_version(void) { return "gbattn 0.1.0 sm_103a"; }
+const char* attn_version(void) { return GBATTN_CHECKED ? "gbattn 0.1.0 sm_103a checked" : "gbattn 0.1.0 sm_103a"; }
 
 attn_status_t attn_selftest_bounded_wait(unsigned int limit_us, void* stream) {
   if (limit_us == 0 || limit_us > 1000000u)

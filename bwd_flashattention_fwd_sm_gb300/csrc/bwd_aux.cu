@@ -57,6 +57,7 @@ struct RowRef {
   long long q;      // element offset in q-like tensors
   long long lse;    // index into lse / delta
   long long acc;    // element offset in the dQ accumulator
+  bool ok;          // checked builds: the row's batch entry, head and position lie in the tensors
 };
 
 // Flat row r (over all positions of all sequences and all query heads) to offsets.
@@ -71,6 +72,8 @@ __device__ __forceinline__ RowRef row_ref(const KParams& p, long long r) {
     x.q = (long long)tok * p.q_ss + (long long)h * p.q_sh;
     x.lse = (long long)h * p.total_tokens + tok;
     x.acc = r * (long long)p.head_dim;
+    x.ok = bounds_ok(!GBATTN_CHECKED || row_in_range(1, 1, p.seqlen, p.total_tokens, p.heads_q, 0, h, 0, tok),
+                     p.status);
   } else {
     const unsigned S = (unsigned)p.seqlen;
     const unsigned bh = ur / S;
@@ -79,6 +82,7 @@ __device__ __forceinline__ RowRef row_ref(const KParams& p, long long r) {
     x.q = (long long)b * p.q_sb + (long long)h * p.q_sh + pos * p.q_ss;
     x.lse = r;
     x.acc = r * (long long)p.head_dim;
+    x.ok = bounds_ok(!GBATTN_CHECKED || row_in_range(0, p.batch, p.seqlen, 0, p.heads_q, b, h, 0, pos), p.status);
   }
   return x;
 }
@@ -114,8 +118,8 @@ __global__ void __launch_bounds__(256) k_bwd_preprocess(KParams p, long long n_r
 #pragma unroll
     for (int j = 0; j < NL; ++j) {
       const long long r = r0 + j * RP + part;
-      if (r < n_rows) {
-        x[j] = row_ref(p, r);
+      x[j].ok = false;
+      if (r < n_rows && (x[j] = row_ref(p, r)).ok) {
 #pragma unroll
         for (int v = 0; v < E / E0; ++v) {
           load_vec<T, E0>(o + x[j].q + (sub + v * L) * E0, a[j] + v * E0);
@@ -134,7 +138,7 @@ __global__ void __launch_bounds__(256) k_bwd_preprocess(KParams p, long long n_r
       for (int i = 0; i < E; ++i) s = fmaf(a[j][i], b[j][i], s);
 #pragma unroll
       for (int off = L / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-      if (sub == 0 && r < n_rows) p.delta[x[j].lse] = s;
+      if (sub == 0 && r < n_rows && x[j].ok) p.delta[x[j].lse] = s;
     }
     if (p.dq_accum) {  // no accumulator in the deterministic (query-stationary dQ) mode
       // zero the rows' float32 accumulator: LZ lanes of 16 bytes per row, NZ stores each
@@ -175,8 +179,8 @@ __global__ void __launch_bounds__(256) k_dq_convert(KParams p, long long n_rows)
 #pragma unroll
     for (int j = 0; j < NL; ++j) {
       const long long r = r0 + j * RP + part;
-      if (r < n_rows) {
-        x[j] = row_ref(p, r);
+      x[j].ok = false;
+      if (r < n_rows && (x[j] = row_ref(p, r)).ok) {
 #pragma unroll
         for (int w = 0; w < E / E0; ++w) {
           const float4* src = reinterpret_cast<const float4*>(p.dq_accum + x[j].acc + (sub + w * L) * E0);
@@ -192,7 +196,7 @@ __global__ void __launch_bounds__(256) k_dq_convert(KParams p, long long n_rows)
 #pragma unroll
     for (int j = 0; j < NL; ++j) {
       const long long r = r0 + j * RP + part;
-      if (r >= n_rows) continue;
+      if (r >= n_rows || !x[j].ok) continue;
 #pragma unroll
       for (int i = 0; i < E; ++i) a[j][i] *= p.scale;
 #pragma unroll
@@ -250,6 +254,7 @@ __global__ void __launch_bounds__(256) k_fwd_combine(KParams p, long long n_rows
 #pragma unroll
     for (int c = 0; c < NC; ++c) acc[c] *= inv;
     const RowRef x = row_ref(p, r);
+    if (!x.ok) continue;
     store_vec<__nv_bfloat16, NC>(O + x.q + lane * NC, acc);
     if (lane == 0) p.lse[x.lse] = L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
   }

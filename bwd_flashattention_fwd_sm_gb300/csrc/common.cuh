@@ -52,6 +52,7 @@ struct KParams {
   const int* row_ptr;   // block mask CSR (device)
   const int* col_idx;
   int n_row_blocks, n_col_blocks, causal_in_block;
+  int nnz;              // block mask: listed tiles (the host copy's count)
   const int* csc_ptr;   // block mask transposed: query blocks per key block (device)
   const int* csc_idx;
 
@@ -74,6 +75,50 @@ struct KParams {
   int* status;               // device status word
   unsigned long long wait_limit_ns;  // bounded-wait limit for pipeline barriers
 };
+
+__device__ __forceinline__ void set_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// Checked builds
+// ---------------------------------------------------------------------------
+//
+// A library built with GBATTN_CHECKED=1 compares every index it computes on the
+// device (work-list entries, block-mask entries, the positions, heads and batch
+// entries behind each tile load, reduce-add, row read and row store) with the
+// extent of the tensor it addresses before the access.  A failed check records
+// kStatusBounds in the status word and the access is skipped (a tile load whose
+// start is out of range still runs, since the tensor map clips it; its data are
+// not used as a valid result).  The host validates all arguments before any
+// launch, so with valid arguments no check fails; the checks catch a device-side
+// index bug instead of letting it read or write another tensor's memory.  Other
+// builds compile every check to `true`.
+#ifndef GBATTN_CHECKED
+#define GBATTN_CHECKED 0
+#endif
+
+__device__ __forceinline__ bool bounds_ok(bool ok, int* status) {
+#if GBATTN_CHECKED
+  if (!ok) set_status(status, kStatusBounds);
+  return ok;
+#else
+  (void)ok;
+  (void)status;
+  return true;
+#endif
+}
+
+// Extents of the tensors the kernels address, from the launch parameters:
+// position `pos` (relative to the sequence start s_tok0) of batch entry b and
+// head h lies inside a q-like (heads = heads_q) or kv-like (heads_kv) tensor.
+__host__ __device__ inline bool row_in_range(int varlen, int batch, long long seqlen, long long total_tokens,
+                                             int heads, int b, int h, long long s_tok0, long long pos) {
+  const long long rows = varlen ? total_tokens : seqlen;
+  const int nb = varlen ? 1 : batch;
+  const long long r = s_tok0 + pos;
+  return b >= 0 && b < nb && h >= 0 && h < heads && pos >= 0 && r >= 0 && r < rows;
+}
 
 // ---------------------------------------------------------------------------
 // Sequence geometry
@@ -112,6 +157,35 @@ __device__ __forceinline__ long long row_index(const KParams& p, const SeqInfo& 
   if (p.varlen) return (long long)h * p.total_tokens + s.tok0 + pos;
   return ((long long)s.b * p.heads_q + h) * p.seqlen + pos;
 }
+// Checked-build guards for one row of a q-like / kv-like tensor (see above).
+__device__ __forceinline__ bool check_q_row(const KParams& p, const SeqInfo& s, int h, long long pos) {
+  return bounds_ok(!GBATTN_CHECKED ||
+                       row_in_range(p.varlen, p.batch, p.seqlen, p.total_tokens, p.heads_q, s.b, h, s.tok0, pos),
+                   p.status);
+}
+__device__ __forceinline__ bool check_kv_row(const KParams& p, const SeqInfo& s, int h, long long pos) {
+  return bounds_ok(!GBATTN_CHECKED ||
+                       row_in_range(p.varlen, p.batch, p.seqlen, p.total_tokens, p.heads_kv, s.b, h, s.tok0, pos),
+                   p.status);
+}
+// A work-list unit names an existing sequence and head (q heads for the forward,
+// kv heads for the backward) and a tile that starts inside the sequence.
+__device__ __forceinline__ bool check_unit(const KParams& p, const Unit& u, bool backward, int tile_rows) {
+  if (!GBATTN_CHECKED) return true;
+  const int n_seq = p.varlen ? p.n_seqs : p.batch;
+  bool ok = u.seq >= 0 && u.seq < n_seq && u.head >= 0 && u.head < (backward ? p.heads_kv : p.heads_q) &&
+            u.tile >= 0;
+  if (ok) {
+    const SeqInfo s = seq_info(p, u.seq);
+    ok = (long long)u.tile * tile_rows < s.len;
+  }
+  return bounds_ok(ok, p.status);
+}
+// A block-mask entry (a 64-row or 64-column block index) lies inside the mask.
+__device__ __forceinline__ bool check_block(const KParams& p, int blk, int n_blocks) {
+  return bounds_ok(!GBATTN_CHECKED || (blk >= 0 && blk < n_blocks), p.status);
+}
+
 // Element offset of a row of the float32 dQ accumulator (contiguous, like q).
 __device__ __forceinline__ long long dqacc_off(const KParams& p, const SeqInfo& s, int h, int pos) {
   if (p.varlen) return ((s.tok0 + pos) * p.heads_q + h) * (long long)p.head_dim;
@@ -139,10 +213,6 @@ __device__ __forceinline__ float fast_log2(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-__device__ __forceinline__ void set_status(int* status, int code) {
-  if (status) atomicCAS(status, 0, code);
 }
 
 // ---------------------------------------------------------------------------

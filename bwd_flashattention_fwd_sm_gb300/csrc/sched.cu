@@ -147,6 +147,14 @@ __global__ void __launch_bounds__(kThreads) k_build_worklist(KParams p, int back
     local += cdiv(seq_info(p, n).len, tile_rows);
   int total;
   int base = block_exclusive_scan(local, scan_smem, &total);
+  // The device's sequence lengths give as many units as the host counted from
+  // its copy (a checked build stops here otherwise: the list would not fit).
+  if (!bounds_ok(!GBATTN_CHECKED ||
+                     (long long)total * heads * (backward ? 1 : max(1, p.n_split)) == (long long)n_units,
+                 p.status)) {
+    if (tid == 0 && p.unit_counter) *p.unit_counter = n_units;  // the kernels take no unit
+    return;
+  }
   for (int n = tid * chunk; n < min(n_seqs, (tid + 1) * chunk); ++n) {
     prefix[n] = base;
     base += cdiv(seq_info(p, n).len, tile_rows);
@@ -202,7 +210,8 @@ __global__ void __launch_bounds__(kThreads) k_build_worklist(KParams p, int back
       un.tile = t;
       un.cost = (t * tile_rows < len) ? unit_cost(p, backward, tile_rows, len, t) : 0;
       const int r = (p.mask == kMaskCausal && !backward) ? tiles - 1 - t : t;
-      out[seq_start[n] + h * tiles + r] = un;
+      const int at = seq_start[n] + h * tiles + r;
+      if (bounds_ok(!GBATTN_CHECKED || (at >= 0 && at < n_units), p.status)) out[at] = un;
     }
     return;
   }
@@ -230,7 +239,8 @@ __global__ void __launch_bounds__(kThreads) k_build_worklist(KParams p, int back
       un.tile = t;
       un.cost = (t * tile_rows < len) ? unit_cost(p, backward, tile_rows, len, t) : 0;
       const int g = t / tg, sz = min(tg, nt - g * tg);
-      out[g * tg * n_pairs + pair * sz + (t - g * tg)] = un;
+      const int at = g * tg * n_pairs + pair * sz + (t - g * tg);
+      if (bounds_ok(!GBATTN_CHECKED || (at >= 0 && at < n_units), p.status)) out[at] = un;
     }
     return;
   }
@@ -272,7 +282,7 @@ __global__ void __launch_bounds__(kThreads) k_build_worklist(KParams p, int back
     Unit un = tmp[u];
     int pos = atomicAdd(&hist[min(un.cost, kBuckets - 1)], 1);
     if (ns > 1) un.cost = u % ns;
-    out[pos] = un;
+    if (bounds_ok(!GBATTN_CHECKED || (pos >= 0 && pos < n_units), p.status)) out[pos] = un;
   }
 }
 
@@ -284,6 +294,8 @@ __global__ void __launch_bounds__(kThreads) k_csr_to_csc(KParams p, int* csc_ptr
   const int c0 = threadIdx.x * chunk, c1 = min(ncb, c0 + chunk);
   auto listed = [&](int r, int c) {
     int lo = p.row_ptr[r], hi = p.row_ptr[r + 1] - 1;
+    // the device copy of row r lies inside the column array
+    if (!bounds_ok(!GBATTN_CHECKED || (0 <= lo && hi < p.nnz), p.status)) return false;
     while (lo <= hi) {
       int mid = (lo + hi) >> 1;
       int v = p.col_idx[mid];
@@ -300,7 +312,7 @@ __global__ void __launch_bounds__(kThreads) k_csr_to_csc(KParams p, int* csc_ptr
   for (int c = c0; c < c1; ++c) {
     csc_ptr[c] = base;
     for (int r = 0; r < nrb; ++r)
-      if (listed(r, c)) csc_idx[base++] = r;
+      if (listed(r, c) && bounds_ok(!GBATTN_CHECKED || base < p.nnz, p.status)) csc_idx[base++] = r;
   }
   if (threadIdx.x == 0) csc_ptr[ncb] = total;
 }

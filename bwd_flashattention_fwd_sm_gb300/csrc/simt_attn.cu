@@ -31,7 +31,9 @@ struct KeyBlocks {
   int e0;       // block mask: first CSR entry
   int mode;     // mask kind
   __device__ int get(const KParams& p, int i) const {
-    return mode == kMaskBlock ? p.col_idx[e0 + i] : i;
+    if (mode != kMaskBlock) return i;
+    const int c = p.col_idx[e0 + i];
+    return check_block(p, c, p.n_col_blocks) ? c : INT_MAX / (2 * kCols);  // failed: past every sequence
   }
 };
 
@@ -51,6 +53,7 @@ __global__ void __launch_bounds__(kThreads) k_simt_fwd(KParams p) {
   float* Ps = Vs + kCols * D;             // [8 warps][8 rows][64]
 
   const Unit u = p.units[blockIdx.x];
+  if (!check_unit(p, u, false, kRows)) return;
   const SeqInfo si = seq_info(p, u.seq);
   const int h = u.head, g = h / p.group;
   const int q0 = u.tile * kRows;
@@ -61,7 +64,7 @@ __global__ void __launch_bounds__(kThreads) k_simt_fwd(KParams p) {
   const T* V = static_cast<const T*>(p.v);
 
   for (int r = warp; r < kRows; r += kThreads / 32) {
-    const bool ok = q0 + r < si.len;
+    const bool ok = q0 + r < si.len && check_q_row(p, si, h, q0 + r);
     load_row_f32(Qs + r * D, Q + (ok ? q_off(p, si, h, q0 + r) : 0), D, ok, lane, 32);
   }
 
@@ -93,7 +96,7 @@ __global__ void __launch_bounds__(kThreads) k_simt_fwd(KParams p) {
     if (k0 >= si.len) continue;
     __syncthreads();  // previous block's K/V no longer in use
     for (int r = warp; r < kCols; r += kThreads / 32) {
-      const bool ok = k0 + r < si.len;
+      const bool ok = k0 + r < si.len && check_kv_row(p, si, g, k0 + r);
       const long long off = ok ? kv_off(p, si, g, k0 + r) : 0;
       for (int d = lane; d < D; d += 32) {
         Ks[r * KS + d] = ok ? to_f32(K[off + d]) : 0.f;
@@ -162,7 +165,7 @@ __global__ void __launch_bounds__(kThreads) k_simt_fwd(KParams p) {
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
     const int i = q0 + warp * 8 + r;
-    if (i >= si.len) continue;
+    if (i >= si.len || !check_q_row(p, si, h, i)) continue;
     const float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
     const long long off = q_off(p, si, h, i);
 #pragma unroll
@@ -191,6 +194,7 @@ __global__ void __launch_bounds__(kThreads) k_simt_bwd(KParams p) {
   float* dlt = lse2 + kCols;        // [64]
 
   const Unit u = p.units[blockIdx.x];
+  if (!check_unit(p, u, true, kRows)) return;
   const SeqInfo si = seq_info(p, u.seq);
   const int g = u.head;
   const int k0 = u.tile * kRows;
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(kThreads) k_simt_bwd(KParams p) {
   const T* V = static_cast<const T*>(p.v);
   const T* dO = static_cast<const T*>(p.dout);
 
-  const bool kvalid = k0 + j < si.len;
+  const bool kvalid = k0 + j < si.len && check_kv_row(p, si, g, k0 + j);
   float kr[NT], vr[NT], dk[NT], dv[NT];
   {
     const long long off = kvalid ? kv_off(p, si, g, k0 + j) : 0;
@@ -230,12 +234,13 @@ __global__ void __launch_bounds__(kThreads) k_simt_bwd(KParams p) {
   for (int hh = 0; hh < p.group; ++hh) {
     const int h = g * p.group + hh;
     for (int it = 0; it < qb_count; ++it) {
-      const int qb = p.mask == kMaskBlock ? p.csc_idx[e0 + it] : qb_begin + it;
+      int qb = p.mask == kMaskBlock ? p.csc_idx[e0 + it] : qb_begin + it;
+      if (p.mask == kMaskBlock && !check_block(p, qb, p.n_row_blocks)) qb = INT_MAX / (2 * kCols);
       const int q0 = qb * kCols;
       if (q0 >= si.len) continue;
       __syncthreads();  // previous step done with Qs, dOs, dSs
       for (int r = warp; r < kCols; r += kThreads / 32) {
-        const bool ok = q0 + r < si.len;
+        const bool ok = q0 + r < si.len && check_q_row(p, si, h, q0 + r);
         const long long off = ok ? q_off(p, si, h, q0 + r) : 0;
         for (int d = lane; d < D; d += 32) {
           Qs[r * D + d] = ok ? to_f32(Q[off + d]) : 0.f;
@@ -243,7 +248,7 @@ __global__ void __launch_bounds__(kThreads) k_simt_bwd(KParams p) {
         }
       }
       if (tid < kCols) {
-        const bool ok = q0 + tid < si.len;
+        const bool ok = q0 + tid < si.len && check_q_row(p, si, h, q0 + tid);
         const long long ri = ok ? row_index(p, si, h, q0 + tid) : 0;
         const float L = ok ? p.lse[ri] : -INFINITY;
         lse2[tid] = L * 1.4426950408889634f;
@@ -284,7 +289,7 @@ __global__ void __launch_bounds__(kThreads) k_simt_bwd(KParams p) {
       // dQ rows of this block: row i = tid/4, columns 4t + part
       {
         const int i = tid >> 2;
-        if (q0 + i < si.len) {
+        if (q0 + i < si.len && check_q_row(p, si, h, q0 + i)) {
           float a[NT];
 #pragma unroll
           for (int t = 0; t < NT; ++t) a[t] = 0.f;
@@ -336,6 +341,7 @@ __global__ void __launch_bounds__(kThreads) k_simt_bwd256(KParams p) {
   float* dlt = lse2 + kQStep256;       // [32]
 
   const Unit u = p.units[blockIdx.x];
+  if (!check_unit(p, u, true, kRows)) return;
   const SeqInfo si = seq_info(p, u.seq);
   const int g = u.head;
   const int k0 = u.tile * kRows;
@@ -348,14 +354,14 @@ __global__ void __launch_bounds__(kThreads) k_simt_bwd256(KParams p) {
   const T* dO = static_cast<const T*>(p.dout);
 
   for (int r = warp; r < kRows; r += kThreads / 32) {
-    const bool ok = k0 + r < si.len;
+    const bool ok = k0 + r < si.len && check_kv_row(p, si, g, k0 + r);
     const long long off = ok ? kv_off(p, si, g, k0 + r) : 0;
     for (int d = lane; d < D; d += 32) {
       Ks[r * KS + d] = ok ? to_f32(K[off + d]) : 0.f;
       Vs[r * KS + d] = ok ? to_f32(V[off + d]) : 0.f;
     }
   }
-  const bool kvalid = k0 + j < si.len;
+  const bool kvalid = k0 + j < si.len && check_kv_row(p, si, g, k0 + j);
   float dk[NT], dv[NT];
 #pragma unroll
   for (int t = 0; t < NT; ++t) dk[t] = dv[t] = 0.f;
@@ -377,13 +383,14 @@ __global__ void __launch_bounds__(kThreads) k_simt_bwd256(KParams p) {
   for (int hh = 0; hh < p.group; ++hh) {
     const int h = g * p.group + hh;
     for (int it = 0; it < qb_count; ++it) {
-      const int qb = p.mask == kMaskBlock ? p.csc_idx[e0 + it] : qb_begin + it;
+      int qb = p.mask == kMaskBlock ? p.csc_idx[e0 + it] : qb_begin + it;
+      if (p.mask == kMaskBlock && !check_block(p, qb, p.n_row_blocks)) qb = INT_MAX / (2 * kCols);
       for (int half = 0; half < kCols / kQStep256; ++half) {
         const int q0 = qb * kCols + half * kQStep256;
         if (q0 >= si.len) continue;
         __syncthreads();  // previous step done with Qs, dOs, dSs (and K, V written)
         for (int r = warp; r < kQStep256; r += kThreads / 32) {
-          const bool ok = q0 + r < si.len;
+          const bool ok = q0 + r < si.len && check_q_row(p, si, h, q0 + r);
           const long long off = ok ? q_off(p, si, h, q0 + r) : 0;
           for (int d = lane; d < D; d += 32) {
             Qs[r * D + d] = ok ? to_f32(Q[off + d]) : 0.f;
@@ -391,7 +398,7 @@ __global__ void __launch_bounds__(kThreads) k_simt_bwd256(KParams p) {
           }
         }
         if (tid < kQStep256) {
-          const bool ok = q0 + tid < si.len;
+          const bool ok = q0 + tid < si.len && check_q_row(p, si, h, q0 + tid);
           const long long ri = ok ? row_index(p, si, h, q0 + tid) : 0;
           const float L = ok ? p.lse[ri] : -INFINITY;
           lse2[tid] = L * 1.4426950408889634f;
@@ -429,7 +436,7 @@ __global__ void __launch_bounds__(kThreads) k_simt_bwd256(KParams p) {
         // dQ rows of this step: row i = tid / 8, columns 8t + sub
         {
           const int i = tid >> 3, sub = tid & 7;
-          if (q0 + i < si.len) {
+          if (q0 + i < si.len && check_q_row(p, si, h, q0 + i)) {
             float a[D / 8];
 #pragma unroll
             for (int t = 0; t < D / 8; ++t) a[t] = 0.f;

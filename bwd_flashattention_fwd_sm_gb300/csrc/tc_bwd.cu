@@ -149,7 +149,7 @@ __device__ __forceinline__ void dq_sync() { asm volatile("bar.sync 2, 128;" ::: 
 template <int D>
 __device__ __forceinline__ void store_kv_rows(uint32_t taddr_row, bool have, float scale, int row,
                                               const KParams& p, const SeqInfo& si, int g, int k0, void* out) {
-  const bool ok = k0 + row < si.len;
+  const bool ok = k0 + row < si.len && check_kv_row(p, si, g, k0 + row);
   __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + (ok ? kv_off(p, si, g, k0 + row) : 0);
 #pragma unroll
   for (int cc = 0; cc < D / 32; ++cc) {
@@ -240,9 +240,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       int idx = 0;
       if (lane == 0) idx = atomicAdd(p.unit_counter, 1);
       idx = __shfl_sync(0xffffffffu, idx, 0);
-      const bool valid = idx < p.n_units;
+      bool valid = idx < p.n_units;
       Unit un{0, 0, 0, 0};
-      if (valid) un = p.units[idx];
+      if (valid) {
+        un = p.units[idx];
+        valid = check_unit(p, un, true, kTile);
+      }
       if (lane == 0) {
         volatile int* s = sm.unit_slot[slot];
         s[0] = un.seq;
@@ -263,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       // K and V of the unit, once the previous unit's products are done with them
       if (!W.warp(&sm.kv_empty, (n_units & 1) ^ 1)) break;
       if (lane == 0) {
+        check_kv_row(p, si, g, k0);
         ptx::mbar_arrive_expect_tx(&sm.kv_full, 2 * tile_bytes<D>());
         tma_tile(sm.k, &a.tk, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b, kHalfTileBytes, D / 64);
         tma_tile(sm.v, &a.tv, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b, kHalfTileBytes, D / 64);
@@ -280,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
         if (!W.warp(&sm.qdo_empty[st], ph ^ 1)) { ok = false; break; }
         const int h = g * p.group + hh, q0 = qb * kQB;
         if (lane == 0) {
+          check_q_row(p, si, h, q0);
           ptx::mbar_arrive_expect_tx(&sm.qdo_full[st], 2 * kQBoxBytes * (D / 64));
           tma_tile(sm.q[st], &a.tq, a.q_rows_inner, &sm.qdo_full[st], map_row(si, q0), h, si.b, kQBoxBytes, D / 64);
           tma_tile(sm.dO[st], &a.tdo, a.q_rows_inner, &sm.qdo_full[st], map_row(si, q0), h, si.b, kQBoxBytes,
@@ -289,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
         for (int c2 = 0; c2 < 2; ++c2) {
           const int c = lane + 32 * c2, qi = q0 + c;
           float nl2 = -INFINITY, ndl = 0.f;
-          if (qi < si.len) {
+          if (qi < si.len && check_q_row(p, si, h, qi)) {
             const long long ri = row_index(p, si, h, qi);
             const float L = p.lse[ri];
             nl2 = L == -INFINITY ? -INFINITY : -L * 1.4426950408889634f;
@@ -624,6 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
           // rows past the sequence end carry exact zeros (their P is 0); the map
           // clips rows past the tensor end
           const int h = un.head * p.group + hh, q0 = qb * kQB;
+          check_q_row(p, si, h, q0);
           if (a.acc_rows_inner) ptx::tma_reduce_add_4d(&a.tacc, sm.dq, 0, (int)(si.tok0 + q0), h, si.b);
           else ptx::tma_reduce_add_4d(&a.tacc, sm.dq, 0, h, (int)(si.tok0 + q0), 0);
           ptx::bulk_commit_group();

@@ -191,7 +191,7 @@ __device__ __forceinline__ void tma_tile4(uint8_t* dst, const CUtensorMap* map, 
 __device__ __forceinline__ void store_half_rows(uint32_t taddr_row, bool have, float scale, int row,
                                                 const KParams& p, const SeqInfo& si, int g, int k0,
                                                 __nv_bfloat16* out) {
-  const bool ok = k0 + row < si.len;
+  const bool ok = k0 + row < si.len && check_kv_row(p, si, g, k0 + row);
   __nv_bfloat16* dst = out + (ok ? kv_off(p, si, g, k0 + row) : 0);
 #pragma unroll
   for (int cc = 0; cc < kDH / 32; ++cc) {
@@ -273,9 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
       int idx = 0;
       if (lane == 0) idx = atomicAdd(p.unit_counter, 1);
       idx = __shfl_sync(0xffffffffu, idx, 0);
-      const bool valid = idx < n_tickets;
+      bool valid = idx < n_tickets;
       Unit un{0, 0, 0, 0};
-      if (valid) un = p.units[idx >> 1];
+      if (valid) {
+        un = p.units[idx >> 1];
+        valid = check_unit(p, un, true, kTile);
+      }
       const int half = idx & 1;
       if (lane == 0) {
         volatile int* s = sm.unit_slot[slot];
@@ -291,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
       // K and V of the unit, once the previous unit's products are done with them
       if (!W.warp(&sm.kv_empty, (n_units & 1) ^ 1)) break;
       if (lane == 0) {
+        check_kv_row(p, si, g, k0);
         ptx::mbar_arrive_expect_tx(&sm.kv_full, 2 * kKVBytes);
         tma_tile4(sm.k, &a.tk, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b, kKBox);
         tma_tile4(sm.v, &a.tv, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b, kKBox);
@@ -308,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
         if (!W.warp(&sm.qdo_empty[st], ph ^ 1)) { ok = false; break; }
         const int h = g * p.group + hh;
         if (lane == 0) {
+          check_q_row(p, si, h, q0);
           ptx::mbar_arrive_expect_tx(&sm.qdo_full[st], 2 * kQTileBytes);
           tma_tile4(sm.q[st], &a.tq, a.q_rows_inner, &sm.qdo_full[st], map_row(si, q0), h, si.b, kQBox);
           tma_tile4(sm.dO[st], &a.tdo, a.q_rows_inner, &sm.qdo_full[st], map_row(si, q0), h, si.b, kQBox);
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
         {
           const int qi = q0 + lane;  // one query row per lane
           float nl2 = -INFINITY, ndl = 0.f;
-          if (qi < si.len) {
+          if (qi < si.len && check_q_row(p, si, h, qi)) {
             const long long ri = row_index(p, si, h, qi);
             const float L = p.lse[ri];
             nl2 = L == -INFINITY ? -INFINITY : -L * 1.4426950408889634f;
@@ -656,6 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
           // rows past the sequence end carry exact zeros (their P is 0); the map
           // clips rows past the tensor end
           const int h = un.head * p.group + hh;
+          check_q_row(p, si, h, q0);
           if (a.acc_rows_inner) ptx::tma_reduce_add_4d(&a.tacc, sm.dq, half * kDH, (int)(si.tok0 + q0), h, si.b);
           else ptx::tma_reduce_add_4d(&a.tacc, sm.dq, half * kDH, h, (int)(si.tok0 + q0), 0);
           ptx::bulk_commit_group();

@@ -59,8 +59,19 @@ struct QBlockList {
   const int* row;            // transposed lists (query blocks per key block)
   int a0, ea, b0, eb, ia, ib;
   int nblk;
+  const KParams* kp;         // checked builds: extents and status word
+
+  // Transposed-list entry i in [s, e): a query block below the sequence's block
+  // count, else INT_MAX (ascending: every later entry is past the end too).
+  __device__ int entry(int i, int e) const {
+    if (i >= e) return INT_MAX;
+    const int r = row[i];
+    if (!check_block(*kp, r, kp->n_row_blocks)) return INT_MAX;
+    return r < nblk ? r : INT_MAX;
+  }
 
   __device__ void init(const KParams& p, int len, int kt) {
+    kp = &p;
     mode = p.mask;
     nblk = (len + 63) / 64;
     it = 0;
@@ -75,14 +86,21 @@ struct QBlockList {
     } else {
       row = p.csc_idx;
       const int cb0 = 2 * kt, cb1 = cb0 + 1;
-      a0 = p.csc_ptr[cb0];
-      ea = p.csc_ptr[cb0 + 1];
+      if (check_block(p, cb0, p.n_col_blocks)) {
+        a0 = p.csc_ptr[cb0];
+        ea = p.csc_ptr[cb0 + 1];
+      }
       if (cb1 < p.n_col_blocks && cb1 * 64 < len) {
         b0 = p.csc_ptr[cb1];
         eb = p.csc_ptr[cb1 + 1];
       } else {
         b0 = eb = 0;
       }
+      // each key block's list lies inside the transposed index array
+      const int nnz = p.csc_ptr[p.n_col_blocks];
+      if (!bounds_ok(!GBATTN_CHECKED || (0 <= a0 && a0 <= ea && ea <= nnz && 0 <= b0 && b0 <= eb && eb <= nnz),
+                     p.status))
+        a0 = ea = b0 = eb = 0;
     }
     restart();
   }
@@ -100,8 +118,8 @@ struct QBlockList {
       bits = 3;
       return true;
     }
-    const int a = (ia < ea && row[ia] < nblk) ? row[ia] : INT_MAX;
-    const int b = (ib < eb && row[ib] < nblk) ? row[ib] : INT_MAX;
+    const int a = entry(ia, ea);
+    const int b = entry(ib, eb);
     const int m = a < b ? a : b;
     if (m == INT_MAX) return false;
     qb = m;
@@ -162,13 +180,19 @@ struct KvTileList2 {
   int nblk;
   bool causal;
 
+  int* status;
+  int n_col_blocks;
+
   __device__ int entry(int i, int end) const {
     if (i >= end) return INT_MAX;
     const int c = __ldg(col + i);
+    if (!bounds_ok(!GBATTN_CHECKED || (c >= 0 && c < n_col_blocks), status)) return INT_MAX;
     return c < nblk ? c : INT_MAX;  // ascending: every later entry is past the end too
   }
 
   __device__ void init(const KParams& p, int len_, int q0_) {
+    status = p.status;
+    n_col_blocks = p.n_col_blocks;
     len = len_;
     q0 = q0_;
     it = 0;

@@ -153,9 +153,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
       int idx = 0;
       if (lane == 0) idx = atomicAdd(p.unit_counter, 1);
       idx = __shfl_sync(0xffffffffu, idx, 0);
-      const bool valid = idx < p.n_units;
+      bool valid = idx < p.n_units;
       Unit un{0, 0, 0, 0};
-      if (valid) un = p.units[idx];
+      if (valid) {
+        un = p.units[idx];
+        valid = check_unit(p, un, false, 2 * kTile);
+      }
       if (lane == 0) {
         volatile int* s = sm.unit_slot[slot];
         s[0] = un.seq;
@@ -173,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
         if (q0 >= si.len || count_active<kSparse>(p, si.len, q0u, q) == 0) continue;
         if (!W.warp(&sm.qd_empty, (n_qd & 1) ^ 1)) { ok = false; break; }
         if (lane == 0) {
+          check_q_row(p, si, h, q0);
           ptx::mbar_arrive_expect_tx(&sm.qd_full, 2 * tile_bytes<D>());
           tma_tile(sm.q, &a.tq, a.q_rows_inner, &sm.qd_full, map_row(si, q0), h, si.b, kHalfTileBytes, D / 64);
           tma_tile(sm.dO, &a.tdo, a.q_rows_inner, &sm.qd_full, map_row(si, q0), h, si.b, kHalfTileBytes, D / 64);
@@ -188,6 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
           const uint32_t ph = (n_kv / kStages) & 1;
           if (!W.warp(&sm.k_empty[st], ph ^ 1) || !W.warp(&sm.v_empty[st], ph ^ 1)) { ok = false; break; }
           if (lane == 0) {
+            check_kv_row(p, si, g, kt * kTile);
             ptx::mbar_arrive_expect_tx(&sm.k_full[st], tile_bytes<D>());
             tma_tile(sm.k[st], &a.tk, a.kv_rows_inner, &sm.k_full[st], map_row(si, kt * kTile), g, si.b,
                      kHalfTileBytes, D / 64);
@@ -338,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
         const int q0 = q0u + q * kTile;
         if (q0 >= si.len) continue;
         const int qi = q0 + r;
-        const bool row_ok = qi < si.len;
+        const bool row_ok = qi < si.len && check_q_row(p, si, h, qi);
         const int n_act = count_active<kSparse>(p, si.len, q0u, q);
         __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.dq) + (row_ok ? q_off(p, si, h, qi) : 0);
         if (n_act == 0) {  // no visible key: dQ rows are zero

@@ -318,9 +318,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       int idx = 0;
       if (lane == 0) idx = atomicAdd(p.unit_counter, 1);
       idx = __shfl_sync(0xffffffffu, idx, 0);
-      const bool valid = idx < p.n_units;
+      bool valid = idx < p.n_units;
       Unit un{0, 0, 0, 0};
-      if (valid) un = p.units[idx];
+      if (valid) {
+        un = p.units[idx];
+        valid = check_unit(p, un, false, 2 * kTile);
+      }
       if (lane == 0) {
         volatile int* s = sm.unit_slot[slot];
         s[0] = un.seq;
@@ -351,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         const uint32_t c = n_q_loads[q];
         if (!W.warp(&sm.q_empty[q], ((c & 1) ^ 1))) { ok = false; break; }
         if (lane == 0) {
+          check_q_row(p, si, h, q0 + q * kTile);
           ptx::mbar_arrive_expect_tx(&sm.q_full[q], kLoadBytes);
           if constexpr (kFp8)
             ptx::tma_load_4d(sm.q[q], &a.tq, &sm.q_full[q], 0, q0 + q * kTile, h, si.b);
@@ -370,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         const uint32_t ph = (n_k / kKStages) & 1;
         if (!W.warp(&sm.k_empty[st], ph ^ 1)) return false;
         if (lane == 0) {
+          check_kv_row(p, si, g, kt_ * kTile);
           ptx::mbar_arrive_expect_tx(&sm.k_full[st], kLoadBytes);
           if constexpr (kFp8)
             ptx::tma_load_4d(sm.k[st], &a.tk, &sm.k_full[st], 0, kt_ * kTile, g, si.b);
@@ -386,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         const uint32_t ph = (n_v / kVStages) & 1;
         if (!W.warp(&sm.v_empty[st], ph ^ 1)) return false;
         if (lane == 0) {
+          check_kv_row(p, si, g, kt_ * kTile);
           ptx::mbar_arrive_expect_tx(&sm.v_full[st], kLoadBytes);
           if constexpr (kFp8)  // V transposed: keys along x, head dim along y
             ptx::tma_load_4d(sm.v[st], &a.tv, &sm.v_full[st], kt_ * kTile, 0, g, si.b);
@@ -746,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       if (p.n_split > 1) {
         // one part of a split key range: the unnormalised O (times the V
         // reference scale of FP8), the row max (log2 units) and the row sum
-        const bool row_ok = qi < si.len;
+        const bool row_ok = qi < si.len && check_q_row(p, si, h, qi);
         const long long rows = (long long)p.batch * p.heads_q * p.seqlen;
         const long long ri = (long long)un.cost * rows + row_index(p, si, h, qi);
         const float osc = kFp8 ? sv_ref : 1.f;
@@ -779,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       }
       const float inv = l > 0.f ? (kFp8 ? sv_ref / l : 1.f / l) : 0.f;
       __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
-      const bool row_ok = qi < si.len;
+      const bool row_ok = qi < si.len && check_q_row(p, si, h, qi);
       __nv_bfloat16* orow = O + (row_ok ? q_off(p, si, h, qi) : 0);
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -909,9 +915,12 @@ __global__ void __launch_bounds__(kThreads256, 1) k_tc_fwd256(const __grid_const
       int idx = 0;
       if (lane == 0) idx = atomicAdd(p.unit_counter, 1);
       idx = __shfl_sync(0xffffffffu, idx, 0);
-      const bool valid = idx < p.n_units;
+      bool valid = idx < p.n_units;
       Unit un{0, 0, 0, 0};
-      if (valid) un = p.units[idx];
+      if (valid) {
+        un = p.units[idx];
+        valid = check_unit(p, un, false, kTile);
+      }
       if (lane == 0) {
         volatile int* s = sm.unit_slot[slot];
         s[0] = un.seq;
@@ -934,6 +943,7 @@ __global__ void __launch_bounds__(kThreads256, 1) k_tc_fwd256(const __grid_const
       if (!any) continue;
       if (!W.warp(&sm.q_empty, (n_q & 1) ^ 1)) { ok = false; break; }
       if (lane == 0) {
+        check_q_row(p, si, h, q0);
         ptx::mbar_arrive_expect_tx(&sm.q_full, 4 * kHalfTileBytes);
         for (int c = 0; c < 4; ++c) {
           if (a.q_rows_inner) ptx::tma_load_4d(sm.q[c], &a.tq, &sm.q_full, c * 64, map_row(si, q0), h, si.b);
@@ -949,6 +959,7 @@ __global__ void __launch_bounds__(kThreads256, 1) k_tc_fwd256(const __grid_const
           const uint32_t ph = (n_c / kRing256) & 1;
           if (!W.warp(&sm.c_empty[st], ph ^ 1)) return false;
           if (lane == 0) {
+            check_kv_row(p, si, g, kt_ * kTile);
             ptx::mbar_arrive_expect_tx(&sm.c_full[st], kChunk256);
             for (int c = 0; c < 2; ++c) {
               const int x = half * 128 + c * 64;
@@ -1205,7 +1216,7 @@ __global__ void __launch_bounds__(kThreads256, 1) k_tc_fwd256(const __grid_const
       }
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
-      const bool row_ok = qi < si.len;
+      const bool row_ok = qi < si.len && check_q_row(p, si, h, qi);
       __nv_bfloat16* orow = O + (row_ok ? q_off(p, si, h, qi) : 0);
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {

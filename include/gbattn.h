@@ -50,8 +50,17 @@
  *
  * Errors.  Every argument error is detected on the host and returned before any
  * device work is queued; outputs are then left untouched.  Errors found on the
- * device (a bounded wait that ran out, an index outside its tensor) are recorded
- * in the device status word and returned by attn_get_status().
+ * device are recorded in the device status word and returned by
+ * attn_get_status(): a bounded pipeline wait that ran out
+ * (ATTN_ERR_DEVICE_TIMEOUT), and, in the checked build of this library
+ * (libgbattn_checked.so, compiled with GBATTN_CHECKED=1; attn_version() ends in
+ * " checked"), an index computed on the device that lies outside its tensor
+ * (ATTN_ERR_DEVICE_BOUNDS).  The checked build compares every work-list entry,
+ * block-mask entry read on the device, and the sequence, head and position
+ * behind each tile load, reduce-add, row read and row store of the attention
+ * kernels with the tensor's extent before the access, and skips the access if
+ * the check fails.  With valid arguments no check fails; the plain build
+ * carries no checks.
  *
  * Asynchrony.  attn_fwd and attn_bwd only queue work on `stream` (a cudaStream_t;
  * NULL = the legacy default stream) and return; outputs are ready once the
