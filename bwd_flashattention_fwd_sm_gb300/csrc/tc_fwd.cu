@@ -182,17 +182,55 @@ __device__ __forceinline__ void zero_p8(uint32_t taddr) {
 // without reading S.  Returns the row sum of the float32 P values.
 template <bool kMask, bool kHalf>
 __device__ __forceinline__ float write_p(const uint32_t (&sr)[128], float c, float mu, int thr, bool lo_ok,
+                                         bool hi_ok, uint32_t taddr);
+
+// The P of keys [K0, K0 + 64) of one row (see write_p), accumulated into rs2.
+template <bool kMask, int K0>
+__device__ __forceinline__ void write_p_half(const uint32_t (&sr)[128], float2 c2, float2 nmu2, int thr,
+                                             uint32_t taddr, float2 (&rs2)[2]) {
+#pragma unroll
+  for (int cc = K0 / 16; cc < K0 / 16 + 4; ++cc) {
+    uint32_t pk[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int k = cc * 16 + 2 * i;
+      const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2, nmu2);
+      float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+      if constexpr (kMask) {
+        if (!(k < thr)) pp.x = 0.f;
+        if (!(k + 1 < thr)) pp.y = 0.f;
+      }
+      rs2[i & 1] = __fadd2_rn(rs2[i & 1], pp);
+      pk[i] = ptx::pack_bf16x2(pp.x, pp.y);
+    }
+    ptx::tmem_st8(taddr + cc * 8, pk);
+  }
+}
+
+template <bool kMask, bool kHalf>
+__device__ __forceinline__ float write_p(const uint32_t (&sr)[128], float c, float mu, int thr, bool lo_ok,
                                          bool hi_ok, uint32_t taddr) {
   const float2 c2 = make_float2(c, c), nmu2 = make_float2(-mu, -mu);
   float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  if constexpr (kHalf) {
+    // Block-sparse: lo_ok and hi_ok are the same for the whole warp, so each
+    // half is one straight run of exponentials (or of zeros), decided once.
+    if (lo_ok) {
+      write_p_half<kMask, 0>(sr, c2, nmu2, thr, taddr, rs2);
+    } else {
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) zero_p8(taddr + cc * 8);
+    }
+    if (hi_ok) {
+      write_p_half<kMask, 64>(sr, c2, nmu2, thr, taddr, rs2);
+    } else {
+#pragma unroll
+      for (int cc = 4; cc < 8; ++cc) zero_p8(taddr + cc * 8);
+    }
+    return (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
+  }
 #pragma unroll
   for (int cc = 0; cc < 8; ++cc) {
-    if constexpr (kHalf) {
-      if (!(cc < 4 ? lo_ok : hi_ok)) {
-        zero_p8(taddr + cc * 8);
-        continue;
-      }
-    }
     uint32_t pk[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
