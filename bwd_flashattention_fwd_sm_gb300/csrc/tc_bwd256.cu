@@ -20,23 +20,29 @@
 // work.  The two passes of a key tile take consecutive tickets, so they run at
 // the same time on two SMs and the second reads K and V from L2.
 //
-// Shared memory holds the whole K and V tile (2 x 64 KiB), so query rows come
-// in steps of 32 (two per 64-row mask block): Q_i and dO_i (32 x 256) in a
-// two-stage ring, dS^T (128 keys x 32 queries, 64-byte swizzled rows) double
-// buffered, and the dQ_i half (32 x 128 float32) staged for the reduce.
+// Shared memory holds the whole K and V tile (2 x 64 KiB), which leaves room
+// for one 64-row step of Q_i and dO_i (2 x 32 KiB), dS^T (128 keys x 64
+// queries) and a 32-row dQ staging buffer, but not for a second stage.  So
+// each head-dim half of Q_i and of dO_i is loaded and released on its own
+// barrier, in the order the products let go of them: the half this unit does
+// not write (read only by S^T and dP^T) is free early, the unit's own half of
+// dO_i after dV, of Q_i after dK.  The next step's S^T and dP^T start on the
+// early halves while dK and dQ^T of this step run; only the own half of Q_i
+// waits for dK.
 //
-// Tensor memory: dV half [0,128)  dK half [128,256)  S^T 2 x 32 [256,320)
-//                dP^T [320,352)  dQ^T half [352,384).
+// Tensor memory: dV half [0,128)  dK half [128,256)  S^T 2 x 64 [256,384)
+//                dP^T [384,448)  dQ^T half [448,512)   (as at head dim 128)
 // Warp roles (480 threads), as in the head-dim-128 kernel:
 //   warps 0-7    compute: warp w covers TMEM lane quarter w % 4 (key rows) and
-//                query columns 16 (w / 4) .. +15 of the step: P^T and dS^T;
+//                query columns 32 (w / 4) .. +31 of the step: P^T and dS^T;
 //                unit epilogue: warps 0-3 dK, warps 4-7 dV (their half)
-//   warp 8       TMA producer (K, V per unit; Q_i, dO_i; LSE and D rows)
+//   warp 8       TMA producer (K, V per unit; the four half-tiles of Q_i and
+//                dO_i; LSE and D rows)
 //   warp 9       tensor-core issuer for S^T, dP^T and dV
 //   warp 14      tensor-core issuer for dK and dQ^T
-//   warps 10-13  dQ writers: dQ_i^T (128 head-dim rows x 32 queries) from tensor
-//                memory to shared memory as [query][head dim], then one TMA
-//                reduce-add into the float32 accumulator
+//   warps 10-13  dQ writers: dQ_i^T (128 head-dim rows x 64 queries) from tensor
+//                memory to shared memory as [query][head dim], 32 queries at a
+//                time, each added into the float32 accumulator by a TMA reduce
 // Every mbarrier wait is bounded; a CTA that gives up records
 // ATTN_ERR_DEVICE_TIMEOUT, drains its copies and tensor-core work, frees tensor
 // memory and returns.
@@ -51,17 +57,16 @@ namespace gbattn {
 namespace {
 
 constexpr int kD = 256, kDH = 128;                  // head dim; the half a unit writes
-constexpr int kQB = 32;                             // query rows per step
+constexpr int kQB = 64;                             // query rows per step
+constexpr int kDqRows = 32;                         // query rows per dQ reduce
 constexpr uint32_t kKBox = kHalfTileBytes;          // 128 rows x 64 bf16 = 16 KiB
 constexpr uint32_t kKVBytes = 4 * kKBox;            // 128 x 256 bf16
-constexpr uint32_t kQBox = kQB * 128;               // 32 rows x 64 bf16 = 4 KiB
-constexpr uint32_t kQTileBytes = 4 * kQBox;         // 32 x 256 bf16
-constexpr uint32_t kDsRow = kQB * 2;                // dS^T row: 32 bf16 = 64 bytes
-constexpr uint32_t kDsBytes = kTile * kDsRow;       // 128 x 32 bf16
-constexpr int kStages = 2;
+constexpr uint32_t kQBox = kQB * 128;               // 64 rows x 64 bf16 = 8 KiB
+constexpr uint32_t kQHalfBytes = 2 * kQBox;         // 64 rows x 128 bf16 (one head-dim half)
+constexpr uint32_t kDsBytes = kTile * kQB * 2;      // dS^T: 128 key rows x 64 bf16 query columns
 constexpr int kThreads = 480;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 320, kColDQ = 352;
+constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384, kColDQ = 448;
 
 struct BwdArgs {
   CUtensorMap tq, tk, tv, tdo, tacc;
@@ -69,18 +74,21 @@ struct BwdArgs {
   KParams p;
 };
 
+// Q_i and dO_i by head-dim half: index 0 the half this unit writes ("own"),
+// index 1 the other half.
 struct Smem {
   uint8_t k[kKVBytes];
   uint8_t v[kKVBytes];
-  uint8_t q[kStages][kQTileBytes];
-  uint8_t dO[kStages][kQTileBytes];
-  uint8_t ds[2][kDsBytes];     // dS^T (64-byte swizzled rows)
-  float dq[kQB * kDH];         // dQ_i half staging, row-major [query][head dim]
-  float nlse2[kStages][kQB];   // -LSE * log2(e) of the stage's query rows (-inf: none / past the end)
-  float ndlt[kStages][kQB];    // -D of the stage's query rows
+  uint8_t q[2][kQHalfBytes];
+  uint8_t dO[2][kQHalfBytes];
+  uint8_t ds[kDsBytes];        // dS^T (128-byte swizzled rows)
+  float dq[kDqRows * kDH];     // dQ_i half staging, row-major [query][head dim]
+  float nlse2[2][kQB];         // by step parity: -LSE * log2(e) (-inf: no key / past the end)
+  float ndlt[2][kQB];          // by step parity: -D
   uint64_t unit_full[2], unit_empty[2];
-  uint64_t kv_full, kv_empty, qdo_full[kStages], qdo_empty[kStages];
-  uint64_t st_full[2], pt_full[2], dp_full, dp_free, ds_full[2], ds_free[2], dq_full, dq_free;
+  uint64_t kv_full, kv_empty;
+  uint64_t qo_full, qo_free, qh_full, qh_free, doo_full, doo_free, doh_full, doh_free;
+  uint64_t st_full[2], pt_full[2], dp_full, dp_free, ds_full, ds_free, dq_full, dq_free;
   uint64_t acc_done, acc_free, drain[2];
   int unit_slot[2][4];  // seq, kv head, key tile, 1 + head-dim half (0: end)
   uint32_t tmem_base;
@@ -145,43 +153,25 @@ __device__ __forceinline__ bool dq_all(bool pred) {
 }
 __device__ __forceinline__ void dq_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
-// The 32-row query steps of a unit: each 64-row block of the head-dim-128
-// kernel's list as two steps (rows past the sequence end are skipped), with
-// the block's 2-bit mask of listed key halves.
-struct Steps32 {
-  BwdSteps blocks;
-  int hh, qb, bits, sub, len;
-  __device__ void init(const KParams& p, int len_, int kt) {
-    blocks.init(p, len_, kt);
-    hh = qb = bits = 0;
-    sub = 2;
-    len = len_;
-  }
-  __device__ bool next(int& head_off, int& q0, int& b) {
-    for (;;) {
-      if (sub < 2) {
-        const int r = qb * 64 + kQB * sub++;
-        if (r < len) {
-          head_off = hh;
-          q0 = r;
-          b = bits;
-          return true;
-        }
-        continue;
-      }
-      if (!blocks.next(hh, qb, bits)) return false;
-      sub = 0;
-    }
-  }
-};
-
-// The four 64-column boxes of a 256-column tile.
+// The four 64-column boxes of a 256-column K or V tile.
 __device__ __forceinline__ void tma_tile4(uint8_t* dst, const CUtensorMap* map, int rows_inner, uint64_t* bar,
-                                          int row, int head, int b, uint32_t box_bytes) {
+                                          int row, int head, int b) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    if (rows_inner) ptx::tma_load_4d(dst + c * box_bytes, map, bar, c * 64, row, head, b);
-    else ptx::tma_load_4d(dst + c * box_bytes, map, bar, c * 64, head, row, b);
+    if (rows_inner) ptx::tma_load_4d(dst + c * kKBox, map, bar, c * 64, row, head, b);
+    else ptx::tma_load_4d(dst + c * kKBox, map, bar, c * 64, head, row, b);
+  }
+}
+
+// Head-dim half `hd` (columns 128 hd .. +127) of a 64-row Q or dO tile: two
+// 64-column boxes.
+__device__ __forceinline__ void tma_half(uint8_t* dst, const CUtensorMap* map, int rows_inner, uint64_t* bar,
+                                         int hd, int row, int head, int b) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int col = hd * kDH + c * 64;
+    if (rows_inner) ptx::tma_load_4d(dst + c * kQBox, map, bar, col, row, head, b);
+    else ptx::tma_load_4d(dst + c * kQBox, map, bar, col, head, row, b);
   }
 }
 
@@ -226,22 +216,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
   Waiter W{sm, p};
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(&sm.qdo_full[s], 2);   // TMA transaction arrival + LSE/D rows written
-      ptx::mbar_init(&sm.qdo_empty[s], 2);  // one commit per MMA warp
-    }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&sm.unit_full[s], 1);
       ptx::mbar_init(&sm.unit_empty[s], 14);  // 2 MMA warps + 8 compute warps + 4 dQ writers
       ptx::mbar_init(&sm.st_full[s], 1);
       ptx::mbar_init(&sm.pt_full[s], 8);
-      ptx::mbar_init(&sm.ds_full[s], 8);
-      ptx::mbar_init(&sm.ds_free[s], 1);
     }
     ptx::mbar_init(&sm.kv_full, 1);
     ptx::mbar_init(&sm.kv_empty, 2);  // one commit per MMA warp
+    // the half-tiles of Q_i / dO_i: one TMA transaction each (the own half of
+    // Q_i also waits for the LSE and D rows), freed by one commit each
+    ptx::mbar_init(&sm.qo_full, 1);
+    ptx::mbar_init(&sm.qh_full, 2);
+    ptx::mbar_init(&sm.doo_full, 1);
+    ptx::mbar_init(&sm.doh_full, 1);
+    ptx::mbar_init(&sm.qo_free, 1);   // S^T's other-half products (dQ^T-free issuer)
+    ptx::mbar_init(&sm.doo_free, 1);  // dP^T's other-half products
+    ptx::mbar_init(&sm.doh_free, 1);  // dV
+    ptx::mbar_init(&sm.qh_free, 1);   // dK
     ptx::mbar_init(&sm.dp_full, 1);
     ptx::mbar_init(&sm.dp_free, 8);
+    ptx::mbar_init(&sm.ds_full, 8);
+    ptx::mbar_init(&sm.ds_free, 1);
     ptx::mbar_init(&sm.dq_full, 1);
     ptx::mbar_init(&sm.dq_free, 4);   // dQ writer warps
     ptx::mbar_init(&sm.acc_done, 2);  // dV issuer + dK issuer
@@ -263,8 +259,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
 
   if (warp == 8) {
     // ================================================================ producer
+    // Each half-tile barrier completes once per step: before loading step j the
+    // producer waits for completion j - 1 of the matching free barrier.
     uint32_t n_units = 0, n_steps = 0;
-    int last_qdo_phase[kStages] = {-1, -1};
+    int last_qo = -1, last_qh = -1, last_doo = -1, last_doh = -1;
     bool kv_loaded = false;
     uint32_t last_kv_phase = 0;
     for (;;) {
@@ -296,29 +294,50 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
       if (lane == 0) {
         check_kv_row(p, si, g, k0);
         ptx::mbar_arrive_expect_tx(&sm.kv_full, 2 * kKVBytes);
-        tma_tile4(sm.k, &a.tk, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b, kKBox);
-        tma_tile4(sm.v, &a.tv, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b, kKBox);
+        tma_tile4(sm.k, &a.tk, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b);
+        tma_tile4(sm.v, &a.tv, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b);
       }
       kv_loaded = true;
       last_kv_phase = n_units & 1;
       ++n_units;
-      Steps32 steps;
+      BwdSteps steps;
       steps.init(p, si.len, un.tile);
-      int hh, q0, bits;
+      int hh, qb, bits;
       bool ok = true;
-      while (steps.next(hh, q0, bits)) {
-        const int st = n_steps % kStages;
-        const uint32_t ph = (n_steps / kStages) & 1;
-        if (!W.warp(&sm.qdo_empty[st], ph ^ 1)) { ok = false; break; }
-        const int h = g * p.group + hh;
+      while (steps.next(hh, qb, bits)) {
+        const uint32_t ph = n_steps & 1;
+        const int h = g * p.group + hh, q0 = qb * kQB, row = map_row(si, q0);
+        if (lane == 0) check_q_row(p, si, h, q0);
+        // the other head-dim half of Q_i, then of dO_i (freed first), then the
+        // own half of dO_i (after dV) and of Q_i (after dK)
+        if (!W.warp(&sm.qo_free, ph ^ 1)) { ok = false; break; }
         if (lane == 0) {
-          check_q_row(p, si, h, q0);
-          ptx::mbar_arrive_expect_tx(&sm.qdo_full[st], 2 * kQTileBytes);
-          tma_tile4(sm.q[st], &a.tq, a.q_rows_inner, &sm.qdo_full[st], map_row(si, q0), h, si.b, kQBox);
-          tma_tile4(sm.dO[st], &a.tdo, a.q_rows_inner, &sm.qdo_full[st], map_row(si, q0), h, si.b, kQBox);
+          ptx::mbar_arrive_expect_tx(&sm.qo_full, kQHalfBytes);
+          tma_half(sm.q[1], &a.tq, a.q_rows_inner, &sm.qo_full, 1 - half, row, h, si.b);
         }
-        {
-          const int qi = q0 + lane;  // one query row per lane
+        last_qo = (int)ph;
+        if (!W.warp(&sm.doo_free, ph ^ 1)) { ok = false; break; }
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&sm.doo_full, kQHalfBytes);
+          tma_half(sm.dO[1], &a.tdo, a.q_rows_inner, &sm.doo_full, 1 - half, row, h, si.b);
+        }
+        last_doo = (int)ph;
+        if (!W.warp(&sm.doh_free, ph ^ 1)) { ok = false; break; }
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&sm.doh_full, kQHalfBytes);
+          tma_half(sm.dO[0], &a.tdo, a.q_rows_inner, &sm.doh_full, half, row, h, si.b);
+        }
+        last_doh = (int)ph;
+        if (!W.warp(&sm.qh_free, ph ^ 1)) { ok = false; break; }
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&sm.qh_full, kQHalfBytes);
+          tma_half(sm.q[0], &a.tq, a.q_rows_inner, &sm.qh_full, half, row, h, si.b);
+        }
+        // LSE and D rows of the step, in the buffer of step j - 2, whose
+        // readers finished before the dK of step j - 1 freed the wait above
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int c = lane + 32 * c2, qi = q0 + c;
           float nl2 = -INFINITY, ndl = 0.f;
           if (qi < si.len && check_q_row(p, si, h, qi)) {
             const long long ri = row_index(p, si, h, qi);
@@ -326,20 +345,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
             nl2 = L == -INFINITY ? -INFINITY : -L * 1.4426950408889634f;
             ndl = -p.delta[ri];
           }
-          sm.nlse2[st][lane] = nl2;
-          sm.ndlt[st][lane] = ndl;
+          sm.nlse2[ph][c] = nl2;
+          sm.ndlt[ph][c] = ndl;
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm.qdo_full[st]);
-        last_qdo_phase[st] = (int)ph;
+        if (lane == 0) ptx::mbar_arrive(&sm.qh_full);
+        last_qh = (int)ph;
+        (void)bits;
         ++n_steps;
       }
       if (!ok) break;
     }
     if (lane == 0) {
       if (kv_loaded) W.drain(&sm.kv_full, last_kv_phase);
-      for (int s = 0; s < kStages; ++s)
-        if (last_qdo_phase[s] >= 0) W.drain(&sm.qdo_full[s], (uint32_t)last_qdo_phase[s]);
+      if (last_qo >= 0) W.drain(&sm.qo_full, (uint32_t)last_qo);
+      if (last_doo >= 0) W.drain(&sm.doo_full, (uint32_t)last_doo);
+      if (last_doh >= 0) W.drain(&sm.doh_full, (uint32_t)last_doh);
+      if (last_qh >= 0) W.drain(&sm.qh_full, (uint32_t)last_qh);
     }
   } else if (warp == 9 || warp == 14) {
     // ================================================================ MMA issuers
@@ -352,41 +374,62 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
     constexpr uint32_t id_acc = ptx::idesc_bf16(128, kDH, false, true);  // dV, dK
     constexpr uint32_t id_dq = ptx::idesc_bf16(128, kQB, true, true);    // dQ^T
     const uint32_t k_addr = ptx::smem_u32(sm.k), v_addr = ptx::smem_u32(sm.v);
+    const uint32_t ds_addr = ptx::smem_u32(sm.ds);
     uint32_t n_units = 0, gi = 0;  // gi: global step counter (all units)
+    int half = 0;
     bool ok = true;
 
-    // S^T_i = K Q_i^T over all 256 head-dim columns: A = K (K-major, four
-    // 64-column boxes), B = Q_i (K-major, four boxes of 32 rows)
-    auto issue_s = [&](uint32_t i) -> bool {
-      const int st = i & 1, qs = i % kStages;
-      if (!W.warp(&sm.qdo_full[qs], (i / kStages) & 1)) return false;
-      ptx::tc_fence_after();
-      const uint32_t q_addr = ptx::smem_u32(sm.q[qs]);
-      if (ptx::elect_one()) {
+    // Half `own` of a score-like product over the head dim: A = K or V (K-major,
+    // boxes 2 hd, 2 hd + 1 of the tile), B = the matching half of Q_i or dO_i.
+    // The other half goes first (it starts the accumulator).
+    auto issue_part = [&](uint32_t a_addr, uint32_t b_addr, uint32_t col, int hd, bool first) {
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint64_t ad = ptx::sdesc_sw128(k_addr + (kk >> 2) * kKBox + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = ptx::sdesc_sw128(q_addr + (kk >> 2) * kQBox + (kk & 3) * 32, 16, 1024);
-          ptx::mma_ss(tmem + kColS + st * kQB, ad, bd, id_st, kk > 0 ? 1u : 0u);
-        }
-        ptx::mma_commit(&sm.st_full[st]);
+      for (int kk = 0; kk < kDH / 16; ++kk) {
+        const uint64_t ad = ptx::sdesc_sw128(a_addr + (2 * hd + (kk >> 2)) * kKBox + (kk & 3) * 32, 16, 1024);
+        const uint64_t bd = ptx::sdesc_sw128(b_addr + (kk >> 2) * kQBox + (kk & 3) * 32, 16, 1024);
+        ptx::mma_ss(tmem + col, ad, bd, id_st, (first && kk == 0) ? 0u : 1u);
+      }
+    };
+    // S^T_i = K Q_i^T, the other half of the head dim (frees that half of Q_i)
+    auto s_other = [&](uint32_t i) -> bool {
+      if (!W.warp(&sm.qo_full, i & 1)) return false;
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) {
+        issue_part(k_addr, ptx::smem_u32(sm.q[1]), kColS + (i & 1) * kQB, 1 - half, true);
+        ptx::mma_commit(&sm.qo_free);
       }
       __syncwarp();
       return true;
     };
-    // dP^T_i = V dO_i^T (stage known loaded)
-    auto issue_dp = [&](uint32_t i) -> bool {
-      const int qs = i % kStages;
-      if (i > 0 && !W.warp(&sm.dp_free, (i - 1) & 1)) return false;
+    // ... and the own half (S^T_i complete)
+    auto s_own = [&](uint32_t i) -> bool {
+      if (!W.warp(&sm.qh_full, i & 1)) return false;
       ptx::tc_fence_after();
-      const uint32_t do_addr = ptx::smem_u32(sm.dO[qs]);
       if (ptx::elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint64_t ad = ptx::sdesc_sw128(v_addr + (kk >> 2) * kKBox + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = ptx::sdesc_sw128(do_addr + (kk >> 2) * kQBox + (kk & 3) * 32, 16, 1024);
-          ptx::mma_ss(tmem + kColDP, ad, bd, id_st, kk > 0 ? 1u : 0u);
-        }
+        issue_part(k_addr, ptx::smem_u32(sm.q[0]), kColS + (i & 1) * kQB, half, false);
+        ptx::mma_commit(&sm.st_full[i & 1]);
+      }
+      __syncwarp();
+      return true;
+    };
+    // dP^T_i = V dO_i^T, other half first: it overwrites dP^T_{i-1}, so the
+    // compute warps must have read that
+    auto dp_other = [&](uint32_t i) -> bool {
+      if (i > 0 && !W.warp(&sm.dp_free, (i - 1) & 1)) return false;
+      if (!W.warp(&sm.doo_full, i & 1)) return false;
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) {
+        issue_part(v_addr, ptx::smem_u32(sm.dO[1]), kColDP, 1 - half, true);
+        ptx::mma_commit(&sm.doo_free);
+      }
+      __syncwarp();
+      return true;
+    };
+    auto dp_own = [&](uint32_t i) -> bool {
+      if (!W.warp(&sm.doh_full, i & 1)) return false;
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) {
+        issue_part(v_addr, ptx::smem_u32(sm.dO[0]), kColDP, half, false);
         ptx::mma_commit(&sm.dp_full);
       }
       __syncwarp();
@@ -397,7 +440,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
       const int slot = n_units & 1;
       if (!W.warp(&sm.unit_full[slot], (n_units >> 1) & 1)) { ok = false; break; }
       Unit un;
-      int half;
       const bool valid = read_unit(sm, slot, un, half);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&sm.unit_empty[slot]);
@@ -405,80 +447,76 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
       const SeqInfo si = seq_info(p, un.seq);
       int n = 0;
       {
-        Steps32 t;
+        BwdSteps t;
         t.init(p, si.len, un.tile);
-        int hh, q0, bits;
-        while (t.next(hh, q0, bits)) ++n;
+        int hh, qb, bits;
+        while (t.next(hh, qb, bits)) ++n;
       }
-      // this unit's head-dim half of Q_i / dO_i (boxes 2 half, 2 half + 1) and K
-      const uint32_t half_q = 2 * half * kQBox, half_k = 2 * half * kKBox;
+      const uint32_t half_k = 2 * half * kKBox;  // this unit's half of K (dQ^T's A operand)
       if (!W.warp(&sm.kv_full, n_units & 1)) { ok = false; break; }
       ptx::tc_fence_after();
       if (side == 0) {
-        if (n > 0) ok = issue_s(gi) && issue_dp(gi);
+        if (n > 0) ok = s_other(gi) && s_own(gi) && dp_other(gi) && dp_own(gi);
         for (int s = 0; ok && s < n; ++s) {
           const uint32_t i = gi + s;
-          const int st = i & 1, qs = i % kStages;
-          if (s + 1 < n && !issue_s(i + 1)) { ok = false; break; }
-          // dV += P^T_i dO_i: A = P^T from tensor memory, B = the dO_i half as
-          // (head dim, query) MN-major
+          const int st = i & 1;
+          // the next step's S^T starts on its early half while P^T_i is formed
+          if (s + 1 < n && !s_other(i + 1)) { ok = false; break; }
+          // dV += P^T_i dO_i: A = P^T from tensor memory, B = the own half of
+          // dO_i as (query, head dim) MN-major
           if (!W.warp(&sm.pt_full[st], (i >> 1) & 1)) { ok = false; break; }
           // before the unit's first dV product: the previous unit's epilogue has
           // read the accumulators
           if (s == 0 && !W.warp(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
           ptx::tc_fence_after();
-          const uint32_t do_addr = ptx::smem_u32(sm.dO[qs]) + half_q;
+          const uint32_t do_addr = ptx::smem_u32(sm.dO[0]);
           if (ptx::elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < kQB / 16; ++kk) {
-              // P^T of query columns 16 kk .. +15: compute warps kk * 4 .. +3 write
-              // their 8 packed columns at 16 kk within the S^T buffer
-              const uint32_t a_col = kColS + st * kQB + 16 * kk;
+              // P^T of query columns 16 kk .. +15: the compute warps of column half
+              // kk / 2 write their 16 packed columns at 32 (kk / 2) within the S^T buffer
+              const uint32_t a_col = kColS + st * kQB + 32 * (kk >> 1) + (kk & 1) * 8;
               const uint64_t bd = ptx::sdesc_sw128(do_addr + kk * 2048, kQBox, 1024);
               ptx::mma_ts(tmem + kColDV, tmem + a_col, bd, id_acc, (s > 0 || kk > 0) ? 1u : 0u);
             }
+            ptx::mma_commit(&sm.doh_free);
           }
           __syncwarp();
-          if (s + 1 < n && !issue_dp(i + 1)) { ok = false; break; }
-          // this side is done with Q_i / dO_i once S^T_i, dP^T_i and dV's product are
-          if (ptx::elect_one()) ptx::mma_commit(&sm.qdo_empty[qs]);
-          __syncwarp();
+          if (s + 1 < n && !(dp_other(i + 1) && s_own(i + 1) && dp_own(i + 1))) { ok = false; break; }
         }
       } else {
         for (int s = 0; ok && s < n; ++s) {
           const uint32_t i = gi + s;
-          const int st = i & 1, qs = i % kStages;
-          // dK += dS^T_i Q_i: A = dS^T (key rows of 32 queries, 64-byte
-          // swizzle, K-major), B = the Q_i half MN-major
-          if (!W.warp(&sm.qdo_full[qs], (i / kStages) & 1)) { ok = false; break; }
-          if (!W.warp(&sm.ds_full[st], (i >> 1) & 1)) { ok = false; break; }
+          // dK += dS^T_i Q_i: A = dS^T (key rows, query contiguous), B = the own
+          // half of Q_i MN-major
+          if (!W.warp(&sm.qh_full, i & 1)) { ok = false; break; }
+          if (!W.warp(&sm.ds_full, i & 1)) { ok = false; break; }
           if (s == 0 && !W.warp(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
           ptx::tc_fence_after();
-          const uint32_t q_addr = ptx::smem_u32(sm.q[qs]) + half_q, ds_addr = ptx::smem_u32(sm.ds[st]);
+          const uint32_t q_addr = ptx::smem_u32(sm.q[0]);
           if (ptx::elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < kQB / 16; ++kk) {
-              const uint64_t ad = ptx::sdesc_sw64(ds_addr + kk * 32, 16, 8 * kDsRow);
+              const uint64_t ad = ptx::sdesc_sw128(ds_addr + kk * 32, 16, 1024);
               const uint64_t bd = ptx::sdesc_sw128(q_addr + kk * 2048, kQBox, 1024);
               ptx::mma_ss(tmem + kColDK, ad, bd, id_acc, (s > 0 || kk > 0) ? 1u : 0u);
             }
+            ptx::mma_commit(&sm.qh_free);
           }
           __syncwarp();
           // dQ_i^T = K^T dS^T_i for the half: A = the K half transposed (head dim
-          // contiguous: MN-major), B = dS^T as (query, key), query contiguous:
-          // MN-major, one 32-query atom
+          // contiguous: MN-major), B = dS^T as (query, key), query contiguous: MN-major
           if (i > 0 && !W.warp(&sm.dq_free, (i - 1) & 1)) { ok = false; break; }
           ptx::tc_fence_after();
           if (ptx::elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
               const uint64_t ad = ptx::sdesc_sw128(k_addr + half_k + kk * 2048, kKBox, 1024);
-              const uint64_t bd = ptx::sdesc_sw64(ds_addr + kk * 16 * kDsRow, kDsBytes, 8 * kDsRow);
+              const uint64_t bd = ptx::sdesc_sw128(ds_addr + kk * 2048, kDsBytes, 1024);
               ptx::mma_ss(tmem + kColDQ, ad, bd, id_dq, kk > 0 ? 1u : 0u);
             }
             ptx::mma_commit(&sm.dq_full);
-            ptx::mma_commit(&sm.qdo_empty[qs]);
-            ptx::mma_commit(&sm.ds_free[st]);
+            ptx::mma_commit(&sm.ds_free);
           }
           __syncwarp();
         }
@@ -501,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
     __syncwarp();
   } else if (warp < 8) {
     // ================================================================ compute warps
-    const int qr = warp & 3, ch = warp >> 2;  // TMEM lane quarter, 16-query column group
+    const int qr = warp & 3, ch = warp >> 2;  // TMEM lane quarter, query-column half
     const int t = qr * 32 + lane;              // key row of S^T / dP^T
     const uint32_t lane_base = (uint32_t)(qr * 32) << 16;
     const float c = p.scale_log2;
@@ -518,45 +556,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
       if (!valid) break;
       const SeqInfo si = seq_info(p, un.seq);
       const int g = un.head, k0 = un.tile * kTile, kj = k0 + t;
-      Steps32 steps;
+      BwdSteps steps;
       steps.init(p, si.len, un.tile);
-      int hh, q0, bits, n = 0;
+      int hh, qb, bits, n = 0;
       // A warp whose wait gave up skips the rest of the unit's steps but still
       // reaches the unit's group-wide agreement below, like every other warp.
       bool alive = true;
-      while (steps.next(hh, q0, bits)) {
-        const int st = i & 1, qs = i % kStages;
-        bool mine = alive && W.warp(&sm.qdo_full[qs], (i / kStages) & 1) && W.warp(&sm.st_full[st], (i >> 1) & 1);
-        float pv[16];
+      while (steps.next(hh, qb, bits)) {
+        const int st = i & 1, rs = i & 1;
+        const int q0 = qb * kQB;
+        // the own half of Q_i arrives with the step's LSE and D rows
+        bool mine = alive && W.warp(&sm.qh_full, i & 1) && W.warp(&sm.st_full[st], (i >> 1) & 1);
+        float pv[32];
         if (mine) {
-          // P^T = exp2(S^T * scale * log2 e - LSE * log2 e) for 16 query columns
+          // P^T = exp2(S^T * scale * log2 e - LSE * log2 e) for 32 query columns
           ptx::tc_fence_after();
-          uint32_t sr[16];
-          ptx::tmem_ld16(tmem + lane_base + kColS + st * kQB + 16 * ch, sr);
+          uint32_t sr[32];
+          ptx::tmem_ld32(tmem + lane_base + kColS + st * kQB + 32 * ch, sr);
           ptx::tmem_ld_wait();
           const bool need_mask = (k0 + kTile > si.len) || (elem_causal && q0 < k0 + kTile - 1) || bits != 3;
           // visible: key listed for this query block, inside the sequence and
-          // (causal) not after the query: q0 + 16 ch + cc >= kj
+          // (causal) not after the query: q0 + 32 ch + cc >= kj
           const bool row_ok = ((bits >> key_half) & 1) && kj < si.len;
-          const int lo = elem_causal ? kj - q0 - 16 * ch : -1;
+          const int lo = elem_causal ? kj - q0 - 32 * ch : -1;
+          uint32_t pk[16];
           const float2 c2 = make_float2(c, c);
-          const float2* nl2 = reinterpret_cast<const float2*>(&sm.nlse2[qs][16 * ch]);
+          const float2* nl2 = reinterpret_cast<const float2*>(&sm.nlse2[rs][32 * ch]);
 #pragma unroll
-          for (int w = 0; w < 8; ++w) {
+          for (int w = 0; w < 16; ++w) {
             const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * w]), __uint_as_float(sr[2 * w + 1])), c2, nl2[w]);
             pv[2 * w] = fast_exp2(x.x);
             pv[2 * w + 1] = fast_exp2(x.y);
           }
           if (need_mask) {
 #pragma unroll
-            for (int cc = 0; cc < 16; ++cc)
+            for (int cc = 0; cc < 32; ++cc)
               if (!(row_ok && cc >= lo)) pv[cc] = 0.f;
           }
-          uint32_t pk[8];
 #pragma unroll
-          for (int w = 0; w < 8; ++w) pk[w] = ptx::pack_bf16x2(pv[2 * w], pv[2 * w + 1]);
-          // P^T packed over the first 8 of this warp's 16 S^T columns
-          ptx::tmem_st8(tmem + lane_base + kColS + st * kQB + 16 * ch, pk);
+          for (int w = 0; w < 16; ++w) pk[w] = ptx::pack_bf16x2(pv[2 * w], pv[2 * w + 1]);
+          ptx::tmem_st16(tmem + lane_base + kColS + st * kQB + 32 * ch, pk);
           ptx::tmem_st_wait();
           ptx::tc_fence_before();
           __syncwarp();
@@ -565,20 +604,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
         }
         if (mine) {
           ptx::tc_fence_after();
-          uint32_t dr[16];
-          ptx::tmem_ld16(tmem + lane_base + kColDP + 16 * ch, dr);
+          uint32_t dr[32];
+          ptx::tmem_ld32(tmem + lane_base + kColDP + 32 * ch, dr);
           ptx::tmem_ld_wait();
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&sm.dp_free);
-          mine = W.warp(&sm.ds_free[st], ((i >> 1) & 1) ^ 1);
+          // dS^T_{i-1} has been read by its dK and dQ^T products
+          mine = W.warp(&sm.ds_free, (i & 1) ^ 1);
           if (mine) {
-            // dS^T = P^T o (dP^T - D), bf16, row t of the dS^T tile: 64-byte rows,
-            // 16-byte chunk c stored at c ^ ((t >> 1) & 3)
-            uint8_t* dsrow = sm.ds[st] + t * kDsRow;
-            const float2* nd2 = reinterpret_cast<const float2*>(&sm.ndlt[qs][16 * ch]);
+            // dS^T = P^T o (dP^T - D), bf16, 128-byte swizzled row t of the dS^T tile
+            uint8_t* dsrow = sm.ds + t * 128;
+            const float2* nd2 = reinterpret_cast<const float2*>(&sm.ndlt[rs][32 * ch]);
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
+            for (int j = 0; j < 4; ++j) {
               float d[8];
 #pragma unroll
               for (int e = 0; e < 8; e += 2) {
@@ -593,12 +632,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
               o.y = ptx::pack_bf16x2(d[2], d[3]);
               o.z = ptx::pack_bf16x2(d[4], d[5]);
               o.w = ptx::pack_bf16x2(d[6], d[7]);
-              const int chunk = 2 * ch + j;
-              *reinterpret_cast<uint4*>(dsrow + ((chunk ^ ((t >> 1) & 3)) * 16)) = o;
+              const int chunk = 4 * ch + j;
+              *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (t & 7)) * 16)) = o;
             }
             ptx::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&sm.ds_full[st]);
+            if (lane == 0) ptx::mbar_arrive(&sm.ds_full);
           }
         }
         alive = mine;
@@ -638,33 +677,47 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
       if (lane == 0) ptx::mbar_arrive(&sm.unit_empty[slot]);
       if (!valid) break;
       const SeqInfo si = seq_info(p, un.seq);
-      Steps32 steps;
+      BwdSteps steps;
       steps.init(p, si.len, un.tile);
-      int hh, q0, bits;
-      while (steps.next(hh, q0, bits)) {
+      int hh, qb, bits;
+      while (steps.next(hh, qb, bits)) {
         // named barriers below: the four warps agree on the wait first
         if (!dq_all(W.warp(&sm.dq_full, i & 1))) { ok = false; break; }
         ptx::tc_fence_after();
-        uint32_t v[32];
-        ptx::tmem_ld32(tmem + lane_base + kColDQ, v);
+        uint32_t v0[32], v1[32];
+        ptx::tmem_ld32(tmem + lane_base + kColDQ, v0);
+        ptx::tmem_ld32(tmem + lane_base + kColDQ + 32, v1);
         ptx::tmem_ld_wait();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sm.dq_free);
-        if (issuer) ptx::bulk_wait_group_read<0>();  // the previous tile has left the staging buffer
-        dq_sync();
+        const int h = un.head * p.group + hh, q0 = qb * kQB;
+        // two reduce-adds of 32 query rows each through the one staging buffer;
+        // rows past the sequence end carry exact zeros (their P is 0) and the
+        // map clips rows past the tensor end.  A half that starts past the
+        // sequence end holds only zeros and is not sent.
+        const int n_hq = q0 + kDqRows < si.len ? 2 : 1;
 #pragma unroll
-        for (int cc = 0; cc < kQB; ++cc) sm.dq[cc * kDH + d] = __uint_as_float(v[cc]);
-        ptx::fence_proxy_async_smem();
-        dq_sync();
-        if (issuer) {
-          // rows past the sequence end carry exact zeros (their P is 0); the map
-          // clips rows past the tensor end
-          const int h = un.head * p.group + hh;
-          check_q_row(p, si, h, q0);
-          if (a.acc_rows_inner) ptx::tma_reduce_add_4d(&a.tacc, sm.dq, half * kDH, (int)(si.tok0 + q0), h, si.b);
-          else ptx::tma_reduce_add_4d(&a.tacc, sm.dq, half * kDH, h, (int)(si.tok0 + q0), 0);
-          ptx::bulk_commit_group();
+        for (int hq = 0; hq < 2; ++hq) {
+          if (hq >= n_hq) break;
+          if (issuer) ptx::bulk_wait_group_read<0>();  // the previous tile has left the staging buffer
+          dq_sync();
+          if (hq == 0) {
+#pragma unroll
+            for (int cc = 0; cc < kDqRows; ++cc) sm.dq[cc * kDH + d] = __uint_as_float(v0[cc]);
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < kDqRows; ++cc) sm.dq[cc * kDH + d] = __uint_as_float(v1[cc]);
+          }
+          ptx::fence_proxy_async_smem();
+          dq_sync();
+          if (issuer) {
+            const int r0 = q0 + hq * kDqRows;
+            check_q_row(p, si, h, r0);
+            if (a.acc_rows_inner) ptx::tma_reduce_add_4d(&a.tacc, sm.dq, half * kDH, (int)(si.tok0 + r0), h, si.b);
+            else ptx::tma_reduce_add_4d(&a.tacc, sm.dq, half * kDH, h, (int)(si.tok0 + r0), 0);
+            ptx::bulk_commit_group();
+          }
         }
         (void)bits;
         ++i;
@@ -696,7 +749,7 @@ cudaError_t launch_tc_bwd256(const KParams& p, int sms, cudaStream_t st) {
   if ((e = make_tile_map(&mdo, p.dout, p, false, kQB)) != cudaSuccess) return e;
   if ((e = make_tile_map(&mk, p.k, p, true)) != cudaSuccess) return e;
   if ((e = make_tile_map(&mv, p.v, p, true)) != cudaSuccess) return e;
-  if ((e = make_acc_map(&macc, p.dq_accum, p, kQB, kDH)) != cudaSuccess) return e;
+  if ((e = make_acc_map(&macc, p.dq_accum, p, kDqRows, kDH)) != cudaSuccess) return e;
   a.tq = mq.map;
   a.tdo = mdo.map;
   a.tk = mk.map;

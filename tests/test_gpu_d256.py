@@ -3,7 +3,7 @@
 bf16 runs both passes on the tensor cores.  The forward takes one 128-row query
 tile per unit, with two S buffers and a 256-column O in tensor memory.  The
 backward takes each 128-key tile twice, once per half of the head dim for dK,
-dV and dQ, in 32-row query steps.  float32 I/O runs both passes on the float32
+dV and dQ, in 64-row query steps.  float32 I/O runs both passes on the float32
 kernels.  Tolerances are those of every other test (parity_util).
 """
 
