@@ -308,6 +308,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
         const uint32_t ph = n_steps & 1;
         const int h = g * p.group + hh, q0 = qb * kQB, row = map_row(si, q0);
         if (lane == 0) check_q_row(p, si, h, q0);
+        // LSE and D of the step's rows, two per lane: the loads go out now and
+        // are used only when the own half of Q_i is sent, so their latency is
+        // spent in the waits below rather than on the step's critical path
+        float lse_r[2], dlt_r[2];
+        bool have_r[2];
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int qi = q0 + lane + 32 * c2;
+          have_r[c2] = qi < si.len && check_q_row(p, si, h, qi);
+          lse_r[c2] = 0.f;
+          dlt_r[c2] = 0.f;
+          if (have_r[c2]) {
+            const long long ri = row_index(p, si, h, qi);
+            lse_r[c2] = __ldg(p.lse + ri);
+            dlt_r[c2] = __ldg(p.delta + ri);
+          }
+        }
         // the other head-dim half of Q_i, then of dO_i (freed first), then the
         // own half of dO_i (after dV) and of Q_i (after dK)
         if (!W.warp(&sm.qo_free, ph ^ 1)) { ok = false; break; }
@@ -333,17 +350,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
           ptx::mbar_arrive_expect_tx(&sm.qh_full, kQHalfBytes);
           tma_half(sm.q[0], &a.tq, a.q_rows_inner, &sm.qh_full, half, row, h, si.b);
         }
-        // LSE and D rows of the step, in the buffer of step j - 2, whose
-        // readers finished before the dK of step j - 1 freed the wait above
+        // the rows go to the buffer of step j - 2, whose readers finished
+        // before the dK of step j - 1 freed the wait above
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
-          const int c = lane + 32 * c2, qi = q0 + c;
+          const int c = lane + 32 * c2;
           float nl2 = -INFINITY, ndl = 0.f;
-          if (qi < si.len && check_q_row(p, si, h, qi)) {
-            const long long ri = row_index(p, si, h, qi);
-            const float L = p.lse[ri];
+          if (have_r[c2]) {
+            const float L = lse_r[c2];
             nl2 = L == -INFINITY ? -INFINITY : -L * 1.4426950408889634f;
-            ndl = -p.delta[ri];
+            ndl = -dlt_r[c2];
           }
           sm.nlse2[ph][c] = nl2;
           sm.ndlt[ph][c] = ndl;
