@@ -20,24 +20,27 @@
 // work.  The two passes of a key tile take consecutive tickets, so they run at
 // the same time on two SMs and the second reads K and V from L2.
 //
-// Shared memory holds the whole K and V tile (2 x 64 KiB), which leaves room
-// for one 64-row step of Q_i and dO_i (2 x 32 KiB), dS^T (128 keys x 64
-// queries) and a 32-row dQ staging buffer, but not for a second stage.  So
-// each head-dim half of Q_i and of dO_i is loaded and released on its own
-// barrier, in the order the products let go of them: the half this unit does
-// not write (read only by S^T and dP^T) is free early, the unit's own half of
-// dO_i after dV, of Q_i after dK.  The next step's S^T and dP^T start on the
-// early halves while dK and dQ^T of this step run; only the own half of Q_i
-// waits for dK.
+// V is the A operand of dP^T = V dO_i^T only, so it lives in tensor memory
+// (128 key rows x 256 head-dim columns as packed bf16 pairs: 128 columns),
+// written once per unit by the compute warps from global memory.  That takes
+// it off the shared-memory port (the products read only dO_i there) and leaves
+// shared memory for the whole K tile (64 KiB), a two-stage ring of 64-row Q_i
+// and dO_i (2 x 64 KiB), dS^T (128 keys x 64 queries) and a 32-row dQ staging
+// buffer.
 //
-// Tensor memory: dV half [0,128)  dK half [128,256)  S^T 2 x 64 [256,384)
-//                dP^T [384,448)  dQ^T half [448,512)   (as at head dim 128)
+// Tensor memory: dV half [0,128)  dK half [128,256)  V [256,384)
+//                S^T / P^T [384,448)  dP^T, then dQ^T [448,512)
+// One S^T buffer: the next step's S^T is issued after this step's dV product
+// (which reads P^T in place).  dP^T and dQ^T share columns: dQ^T_i is written
+// once the compute warps have read dP^T_i (they have when dS^T_i is complete),
+// and dP^T_{i+1} once the dQ writers have read dQ^T_i.
 // Warp roles (480 threads), as in the head-dim-128 kernel:
 //   warps 0-7    compute: warp w covers TMEM lane quarter w % 4 (key rows) and
 //                query columns 32 (w / 4) .. +31 of the step: P^T and dS^T;
-//                unit epilogue: warps 0-3 dK, warps 4-7 dV (their half)
-//   warp 8       TMA producer (K, V per unit; the four half-tiles of Q_i and
-//                dO_i; LSE and D rows)
+//                per unit: V head-dim columns 128 (w / 4) .. +127 of their key
+//                rows into tensor memory; unit epilogue: warps 0-3 dK, warps
+//                4-7 dV (their half)
+//   warp 8       TMA producer (K per unit; Q_i, dO_i; LSE and D rows)
 //   warp 9       tensor-core issuer for S^T, dP^T and dV
 //   warp 14      tensor-core issuer for dK and dQ^T
 //   warps 10-13  dQ writers: dQ_i^T (128 head-dim rows x 64 queries) from tensor
@@ -59,36 +62,33 @@ namespace {
 constexpr int kD = 256, kDH = 128;                  // head dim; the half a unit writes
 constexpr int kQB = 64;                             // query rows per step
 constexpr int kDqRows = 32;                         // query rows per dQ reduce
+constexpr int kStages = 2;                          // Q_i / dO_i ring
 constexpr uint32_t kKBox = kHalfTileBytes;          // 128 rows x 64 bf16 = 16 KiB
-constexpr uint32_t kKVBytes = 4 * kKBox;            // 128 x 256 bf16
+constexpr uint32_t kKBytes = 4 * kKBox;             // 128 x 256 bf16
 constexpr uint32_t kQBox = kQB * 128;               // 64 rows x 64 bf16 = 8 KiB
-constexpr uint32_t kQHalfBytes = 2 * kQBox;         // 64 rows x 128 bf16 (one head-dim half)
+constexpr uint32_t kQTileBytes = 4 * kQBox;         // 64 x 256 bf16
 constexpr uint32_t kDsBytes = kTile * kQB * 2;      // dS^T: 128 key rows x 64 bf16 query columns
 constexpr int kThreads = 480;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384, kColDQ = 448;
+constexpr uint32_t kColDV = 0, kColDK = 128, kColV = 256, kColS = 384, kColDPQ = 448;
 
 struct BwdArgs {
-  CUtensorMap tq, tk, tv, tdo, tacc;
+  CUtensorMap tq, tk, tdo, tacc;
   int q_rows_inner, kv_rows_inner, acc_rows_inner;
   KParams p;
 };
 
-// Q_i and dO_i by head-dim half: index 0 the half this unit writes ("own"),
-// index 1 the other half.
 struct Smem {
-  uint8_t k[kKVBytes];
-  uint8_t v[kKVBytes];
-  uint8_t q[2][kQHalfBytes];
-  uint8_t dO[2][kQHalfBytes];
+  uint8_t k[kKBytes];
+  uint8_t q[kStages][kQTileBytes];
+  uint8_t dO[kStages][kQTileBytes];
   uint8_t ds[kDsBytes];        // dS^T (128-byte swizzled rows)
   float dq[kDqRows * kDH];     // dQ_i half staging, row-major [query][head dim]
-  float nlse2[2][kQB];         // by step parity: -LSE * log2(e) (-inf: no key / past the end)
-  float ndlt[2][kQB];          // by step parity: -D
+  float nlse2[kStages][kQB];   // -LSE * log2(e) of the stage's query rows (-inf: no key / past the end)
+  float ndlt[kStages][kQB];    // -D of the stage's query rows
   uint64_t unit_full[2], unit_empty[2];
-  uint64_t kv_full, kv_empty;
-  uint64_t qo_full, qo_free, qh_full, qh_free, doo_full, doo_free, doh_full, doh_free;
-  uint64_t st_full[2], pt_full[2], dp_full, dp_free, ds_full, ds_free, dq_full, dq_free;
+  uint64_t k_full, k_empty, v_full, qdo_full[kStages], qdo_empty[kStages];
+  uint64_t st_full, pt_full, dp_full, ds_full, ds_free, dq_full, dq_free;
   uint64_t acc_done, acc_free, drain[2];
   int unit_slot[2][4];  // seq, kv head, key tile, 1 + head-dim half (0: end)
   uint32_t tmem_base;
@@ -153,25 +153,13 @@ __device__ __forceinline__ bool dq_all(bool pred) {
 }
 __device__ __forceinline__ void dq_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
-// The four 64-column boxes of a 256-column K or V tile.
+// The four 64-column boxes of a 256-column tile (box_bytes apart).
 __device__ __forceinline__ void tma_tile4(uint8_t* dst, const CUtensorMap* map, int rows_inner, uint64_t* bar,
-                                          int row, int head, int b) {
+                                          int row, int head, int b, uint32_t box_bytes) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    if (rows_inner) ptx::tma_load_4d(dst + c * kKBox, map, bar, c * 64, row, head, b);
-    else ptx::tma_load_4d(dst + c * kKBox, map, bar, c * 64, head, row, b);
-  }
-}
-
-// Head-dim half `hd` (columns 128 hd .. +127) of a 64-row Q or dO tile: two
-// 64-column boxes.
-__device__ __forceinline__ void tma_half(uint8_t* dst, const CUtensorMap* map, int rows_inner, uint64_t* bar,
-                                         int hd, int row, int head, int b) {
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    const int col = hd * kDH + c * 64;
-    if (rows_inner) ptx::tma_load_4d(dst + c * kQBox, map, bar, col, row, head, b);
-    else ptx::tma_load_4d(dst + c * kQBox, map, bar, col, head, row, b);
+    if (rows_inner) ptx::tma_load_4d(dst + c * box_bytes, map, bar, c * 64, row, head, b);
+    else ptx::tma_load_4d(dst + c * box_bytes, map, bar, c * 64, head, row, b);
   }
 }
 
@@ -207,6 +195,31 @@ __device__ __forceinline__ void store_half_rows(uint32_t taddr_row, bool have, f
   }
 }
 
+// One warp copies head-dim columns c0 .. c0 + 127 of its 32 key rows of V
+// (row k0 + row of head g; zeros past the sequence end) into tensor memory at
+// taddr_row, 64 columns of packed bf16 pairs: the layout of an A operand read
+// from tensor memory (column j holds elements 2j and 2j + 1 of the row).
+__device__ __forceinline__ void load_v_rows(uint32_t taddr_row, int row, int c0, const KParams& p,
+                                            const SeqInfo& si, int g, int k0) {
+  const bool ok = k0 + row < si.len && check_kv_row(p, si, g, k0 + row);
+  const uint4* src =
+      reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.v) + (ok ? kv_off(p, si, g, k0 + row) : 0) + c0);
+#pragma unroll
+  for (int part = 0; part < 2; ++part) {
+    uint32_t r[32];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 x = ok ? __ldg(src + part * 8 + j) : make_uint4(0u, 0u, 0u, 0u);
+      r[4 * j] = x.x;
+      r[4 * j + 1] = x.y;
+      r[4 * j + 2] = x.z;
+      r[4 * j + 3] = x.w;
+    }
+    ptx::tmem_st32(taddr_row + part * 32, r);
+  }
+  ptx::tmem_st_wait();
+}
+
 __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant__ BwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -216,26 +229,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
   Waiter W{sm, p};
 
   if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&sm.qdo_full[s], 2);   // TMA transaction arrival + LSE/D rows written
+      ptx::mbar_init(&sm.qdo_empty[s], 2);  // one commit per MMA warp
+    }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(&sm.unit_full[s], 1);
       ptx::mbar_init(&sm.unit_empty[s], 14);  // 2 MMA warps + 8 compute warps + 4 dQ writers
-      ptx::mbar_init(&sm.st_full[s], 1);
-      ptx::mbar_init(&sm.pt_full[s], 8);
     }
-    ptx::mbar_init(&sm.kv_full, 1);
-    ptx::mbar_init(&sm.kv_empty, 2);  // one commit per MMA warp
-    // the half-tiles of Q_i / dO_i: one TMA transaction each (the own half of
-    // Q_i also waits for the LSE and D rows), freed by one commit each
-    ptx::mbar_init(&sm.qo_full, 1);
-    ptx::mbar_init(&sm.qh_full, 2);
-    ptx::mbar_init(&sm.doo_full, 1);
-    ptx::mbar_init(&sm.doh_full, 1);
-    ptx::mbar_init(&sm.qo_free, 1);   // S^T's other-half products (dQ^T-free issuer)
-    ptx::mbar_init(&sm.doo_free, 1);  // dP^T's other-half products
-    ptx::mbar_init(&sm.doh_free, 1);  // dV
-    ptx::mbar_init(&sm.qh_free, 1);   // dK
+    ptx::mbar_init(&sm.k_full, 1);
+    ptx::mbar_init(&sm.k_empty, 2);  // one commit per MMA warp
+    ptx::mbar_init(&sm.v_full, 8);   // compute warps
+    ptx::mbar_init(&sm.st_full, 1);
+    ptx::mbar_init(&sm.pt_full, 8);
     ptx::mbar_init(&sm.dp_full, 1);
-    ptx::mbar_init(&sm.dp_free, 8);
     ptx::mbar_init(&sm.ds_full, 8);
     ptx::mbar_init(&sm.ds_free, 1);
     ptx::mbar_init(&sm.dq_full, 1);
@@ -259,12 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
 
   if (warp == 8) {
     // ================================================================ producer
-    // Each half-tile barrier completes once per step: before loading step j the
-    // producer waits for completion j - 1 of the matching free barrier.
     uint32_t n_units = 0, n_steps = 0;
-    int last_qo = -1, last_qh = -1, last_doo = -1, last_doh = -1;
-    bool kv_loaded = false;
-    uint32_t last_kv_phase = 0;
+    int last_qdo_phase[kStages] = {-1, -1};
+    bool k_loaded = false;
+    uint32_t last_k_phase = 0;
     for (;;) {
       const int slot = n_units & 1;
       if (!W.warp(&sm.unit_empty[slot], ((n_units >> 1) & 1) ^ 1)) break;
@@ -289,95 +294,56 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
       if (!valid) break;
       const SeqInfo si = seq_info(p, un.seq);
       const int g = un.head, k0 = un.tile * kTile;
-      // K and V of the unit, once the previous unit's products are done with them
-      if (!W.warp(&sm.kv_empty, (n_units & 1) ^ 1)) break;
+      // K of the unit, once the previous unit's products are done with it
+      if (!W.warp(&sm.k_empty, (n_units & 1) ^ 1)) break;
       if (lane == 0) {
         check_kv_row(p, si, g, k0);
-        ptx::mbar_arrive_expect_tx(&sm.kv_full, 2 * kKVBytes);
-        tma_tile4(sm.k, &a.tk, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b);
-        tma_tile4(sm.v, &a.tv, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b);
+        ptx::mbar_arrive_expect_tx(&sm.k_full, kKBytes);
+        tma_tile4(sm.k, &a.tk, a.kv_rows_inner, &sm.k_full, map_row(si, k0), g, si.b, kKBox);
       }
-      kv_loaded = true;
-      last_kv_phase = n_units & 1;
+      k_loaded = true;
+      last_k_phase = n_units & 1;
       ++n_units;
       BwdSteps steps;
       steps.init(p, si.len, un.tile);
       int hh, qb, bits;
       bool ok = true;
       while (steps.next(hh, qb, bits)) {
-        const uint32_t ph = n_steps & 1;
-        const int h = g * p.group + hh, q0 = qb * kQB, row = map_row(si, q0);
-        if (lane == 0) check_q_row(p, si, h, q0);
-        // LSE and D of the step's rows, two per lane: the loads go out now and
-        // are used only when the own half of Q_i is sent, so their latency is
-        // spent in the waits below rather than on the step's critical path
-        float lse_r[2], dlt_r[2];
-        bool have_r[2];
+        const int st = n_steps % kStages;
+        const uint32_t ph = (n_steps / kStages) & 1;
+        if (!W.warp(&sm.qdo_empty[st], ph ^ 1)) { ok = false; break; }
+        const int h = g * p.group + hh, q0 = qb * kQB;
+        if (lane == 0) {
+          check_q_row(p, si, h, q0);
+          ptx::mbar_arrive_expect_tx(&sm.qdo_full[st], 2 * kQTileBytes);
+          tma_tile4(sm.q[st], &a.tq, a.q_rows_inner, &sm.qdo_full[st], map_row(si, q0), h, si.b, kQBox);
+          tma_tile4(sm.dO[st], &a.tdo, a.q_rows_inner, &sm.qdo_full[st], map_row(si, q0), h, si.b, kQBox);
+        }
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
-          const int qi = q0 + lane + 32 * c2;
-          have_r[c2] = qi < si.len && check_q_row(p, si, h, qi);
-          lse_r[c2] = 0.f;
-          dlt_r[c2] = 0.f;
-          if (have_r[c2]) {
-            const long long ri = row_index(p, si, h, qi);
-            lse_r[c2] = __ldg(p.lse + ri);
-            dlt_r[c2] = __ldg(p.delta + ri);
-          }
-        }
-        // the other head-dim half of Q_i, then of dO_i (freed first), then the
-        // own half of dO_i (after dV) and of Q_i (after dK)
-        if (!W.warp(&sm.qo_free, ph ^ 1)) { ok = false; break; }
-        if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&sm.qo_full, kQHalfBytes);
-          tma_half(sm.q[1], &a.tq, a.q_rows_inner, &sm.qo_full, 1 - half, row, h, si.b);
-        }
-        last_qo = (int)ph;
-        if (!W.warp(&sm.doo_free, ph ^ 1)) { ok = false; break; }
-        if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&sm.doo_full, kQHalfBytes);
-          tma_half(sm.dO[1], &a.tdo, a.q_rows_inner, &sm.doo_full, 1 - half, row, h, si.b);
-        }
-        last_doo = (int)ph;
-        if (!W.warp(&sm.doh_free, ph ^ 1)) { ok = false; break; }
-        if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&sm.doh_full, kQHalfBytes);
-          tma_half(sm.dO[0], &a.tdo, a.q_rows_inner, &sm.doh_full, half, row, h, si.b);
-        }
-        last_doh = (int)ph;
-        if (!W.warp(&sm.qh_free, ph ^ 1)) { ok = false; break; }
-        if (lane == 0) {
-          ptx::mbar_arrive_expect_tx(&sm.qh_full, kQHalfBytes);
-          tma_half(sm.q[0], &a.tq, a.q_rows_inner, &sm.qh_full, half, row, h, si.b);
-        }
-        // the rows go to the buffer of step j - 2, whose readers finished
-        // before the dK of step j - 1 freed the wait above
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const int c = lane + 32 * c2;
+          const int c = lane + 32 * c2, qi = q0 + c;
           float nl2 = -INFINITY, ndl = 0.f;
-          if (have_r[c2]) {
-            const float L = lse_r[c2];
+          if (qi < si.len && check_q_row(p, si, h, qi)) {
+            const long long ri = row_index(p, si, h, qi);
+            const float L = p.lse[ri];
             nl2 = L == -INFINITY ? -INFINITY : -L * 1.4426950408889634f;
-            ndl = -dlt_r[c2];
+            ndl = -p.delta[ri];
           }
-          sm.nlse2[ph][c] = nl2;
-          sm.ndlt[ph][c] = ndl;
+          sm.nlse2[st][c] = nl2;
+          sm.ndlt[st][c] = ndl;
         }
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&sm.qh_full);
-        last_qh = (int)ph;
+        if (lane == 0) ptx::mbar_arrive(&sm.qdo_full[st]);
+        last_qdo_phase[st] = (int)ph;
         (void)bits;
         ++n_steps;
       }
       if (!ok) break;
     }
     if (lane == 0) {
-      if (kv_loaded) W.drain(&sm.kv_full, last_kv_phase);
-      if (last_qo >= 0) W.drain(&sm.qo_full, (uint32_t)last_qo);
-      if (last_doo >= 0) W.drain(&sm.doo_full, (uint32_t)last_doo);
-      if (last_doh >= 0) W.drain(&sm.doh_full, (uint32_t)last_doh);
-      if (last_qh >= 0) W.drain(&sm.qh_full, (uint32_t)last_qh);
+      if (k_loaded) W.drain(&sm.k_full, last_k_phase);
+      for (int s = 0; s < kStages; ++s)
+        if (last_qdo_phase[s] >= 0) W.drain(&sm.qdo_full[s], (uint32_t)last_qdo_phase[s]);
     }
   } else if (warp == 9 || warp == 14) {
     // ================================================================ MMA issuers
@@ -389,63 +355,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
     constexpr uint32_t id_st = ptx::idesc_bf16(128, kQB, false, false);  // S^T, dP^T
     constexpr uint32_t id_acc = ptx::idesc_bf16(128, kDH, false, true);  // dV, dK
     constexpr uint32_t id_dq = ptx::idesc_bf16(128, kQB, true, true);    // dQ^T
-    const uint32_t k_addr = ptx::smem_u32(sm.k), v_addr = ptx::smem_u32(sm.v);
-    const uint32_t ds_addr = ptx::smem_u32(sm.ds);
+    const uint32_t k_addr = ptx::smem_u32(sm.k), ds_addr = ptx::smem_u32(sm.ds);
     uint32_t n_units = 0, gi = 0;  // gi: global step counter (all units)
-    int half = 0;
     bool ok = true;
 
-    // Half `own` of a score-like product over the head dim: A = K or V (K-major,
-    // boxes 2 hd, 2 hd + 1 of the tile), B = the matching half of Q_i or dO_i.
-    // The other half goes first (it starts the accumulator).
-    auto issue_part = [&](uint32_t a_addr, uint32_t b_addr, uint32_t col, int hd, bool first) {
+    // S^T_i = K Q_i^T over all 256 head-dim columns: A = K (K-major, four
+    // 64-column boxes), B = Q_i (K-major, four boxes)
+    auto issue_s = [&](uint32_t i) -> bool {
+      const int qs = i % kStages;
+      if (!W.warp(&sm.qdo_full[qs], (i / kStages) & 1)) return false;
+      ptx::tc_fence_after();
+      const uint32_t q_addr = ptx::smem_u32(sm.q[qs]);
+      if (ptx::elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < kDH / 16; ++kk) {
-        const uint64_t ad = ptx::sdesc_sw128(a_addr + (2 * hd + (kk >> 2)) * kKBox + (kk & 3) * 32, 16, 1024);
-        const uint64_t bd = ptx::sdesc_sw128(b_addr + (kk >> 2) * kQBox + (kk & 3) * 32, 16, 1024);
-        ptx::mma_ss(tmem + col, ad, bd, id_st, (first && kk == 0) ? 0u : 1u);
-      }
-    };
-    // S^T_i = K Q_i^T, the other half of the head dim (frees that half of Q_i)
-    auto s_other = [&](uint32_t i) -> bool {
-      if (!W.warp(&sm.qo_full, i & 1)) return false;
-      ptx::tc_fence_after();
-      if (ptx::elect_one()) {
-        issue_part(k_addr, ptx::smem_u32(sm.q[1]), kColS + (i & 1) * kQB, 1 - half, true);
-        ptx::mma_commit(&sm.qo_free);
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint64_t ad = ptx::sdesc_sw128(k_addr + (kk >> 2) * kKBox + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = ptx::sdesc_sw128(q_addr + (kk >> 2) * kQBox + (kk & 3) * 32, 16, 1024);
+          ptx::mma_ss(tmem + kColS, ad, bd, id_st, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(&sm.st_full);
       }
       __syncwarp();
       return true;
     };
-    // ... and the own half (S^T_i complete)
-    auto s_own = [&](uint32_t i) -> bool {
-      if (!W.warp(&sm.qh_full, i & 1)) return false;
+    // dP^T_i = V dO_i^T: A = V from tensor memory (8 packed columns per 16
+    // head-dim columns), B = dO_i (K-major).  It overwrites dQ^T_{i-1}, so the
+    // dQ writers must have read that.
+    auto issue_dp = [&](uint32_t i) -> bool {
+      const int qs = i % kStages;
+      if (i > 0 && !W.warp(&sm.dq_free, (i - 1) & 1)) return false;
       ptx::tc_fence_after();
+      const uint32_t do_addr = ptx::smem_u32(sm.dO[qs]);
       if (ptx::elect_one()) {
-        issue_part(k_addr, ptx::smem_u32(sm.q[0]), kColS + (i & 1) * kQB, half, false);
-        ptx::mma_commit(&sm.st_full[i & 1]);
-      }
-      __syncwarp();
-      return true;
-    };
-    // dP^T_i = V dO_i^T, other half first: it overwrites dP^T_{i-1}, so the
-    // compute warps must have read that
-    auto dp_other = [&](uint32_t i) -> bool {
-      if (i > 0 && !W.warp(&sm.dp_free, (i - 1) & 1)) return false;
-      if (!W.warp(&sm.doo_full, i & 1)) return false;
-      ptx::tc_fence_after();
-      if (ptx::elect_one()) {
-        issue_part(v_addr, ptx::smem_u32(sm.dO[1]), kColDP, 1 - half, true);
-        ptx::mma_commit(&sm.doo_free);
-      }
-      __syncwarp();
-      return true;
-    };
-    auto dp_own = [&](uint32_t i) -> bool {
-      if (!W.warp(&sm.doh_full, i & 1)) return false;
-      ptx::tc_fence_after();
-      if (ptx::elect_one()) {
-        issue_part(v_addr, ptx::smem_u32(sm.dO[0]), kColDP, half, false);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint64_t bd = ptx::sdesc_sw128(do_addr + (kk >> 2) * kQBox + (kk & 3) * 32, 16, 1024);
+          ptx::mma_ts(tmem + kColDPQ, tmem + kColV + 8 * kk, bd, id_st, kk > 0 ? 1u : 0u);
+        }
         ptx::mma_commit(&sm.dp_full);
       }
       __syncwarp();
@@ -456,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
       const int slot = n_units & 1;
       if (!W.warp(&sm.unit_full[slot], (n_units >> 1) & 1)) { ok = false; break; }
       Unit un;
+      int half;
       const bool valid = read_unit(sm, slot, un, half);
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&sm.unit_empty[slot]);
@@ -468,48 +415,59 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
         int hh, qb, bits;
         while (t.next(hh, qb, bits)) ++n;
       }
-      const uint32_t half_k = 2 * half * kKBox;  // this unit's half of K (dQ^T's A operand)
-      if (!W.warp(&sm.kv_full, n_units & 1)) { ok = false; break; }
+      // this unit's head-dim half of Q_i / dO_i (boxes 2 half, 2 half + 1) and K
+      const uint32_t half_q = 2 * half * kQBox, half_k = 2 * half * kKBox;
+      if (!W.warp(&sm.k_full, n_units & 1)) { ok = false; break; }
       ptx::tc_fence_after();
       if (side == 0) {
-        if (n > 0) ok = s_other(gi) && s_own(gi) && dp_other(gi) && dp_own(gi);
+        if (n > 0) {
+          ok = issue_s(gi);
+          // the unit's V is in tensor memory before its first dP^T product
+          ok = ok && W.warp(&sm.v_full, n_units & 1);
+          if (ok) ptx::tc_fence_after();
+          ok = ok && issue_dp(gi);
+        } else {
+          ok = W.warp(&sm.v_full, n_units & 1);
+        }
         for (int s = 0; ok && s < n; ++s) {
           const uint32_t i = gi + s;
-          const int st = i & 1;
-          // the next step's S^T starts on its early half while P^T_i is formed
-          if (s + 1 < n && !s_other(i + 1)) { ok = false; break; }
-          // dV += P^T_i dO_i: A = P^T from tensor memory, B = the own half of
-          // dO_i as (query, head dim) MN-major
-          if (!W.warp(&sm.pt_full[st], (i >> 1) & 1)) { ok = false; break; }
+          const int qs = i % kStages;
+          // dV += P^T_i dO_i: A = P^T from tensor memory, B = the dO_i half as
+          // (query, head dim) MN-major
+          if (!W.warp(&sm.pt_full, i & 1)) { ok = false; break; }
           // before the unit's first dV product: the previous unit's epilogue has
           // read the accumulators
           if (s == 0 && !W.warp(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
           ptx::tc_fence_after();
-          const uint32_t do_addr = ptx::smem_u32(sm.dO[0]);
+          const uint32_t do_addr = ptx::smem_u32(sm.dO[qs]) + half_q;
           if (ptx::elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < kQB / 16; ++kk) {
               // P^T of query columns 16 kk .. +15: the compute warps of column half
-              // kk / 2 write their 16 packed columns at 32 (kk / 2) within the S^T buffer
-              const uint32_t a_col = kColS + st * kQB + 32 * (kk >> 1) + (kk & 1) * 8;
+              // kk / 2 write their 16 packed columns at 32 (kk / 2) within S^T
+              const uint32_t a_col = kColS + 32 * (kk >> 1) + (kk & 1) * 8;
               const uint64_t bd = ptx::sdesc_sw128(do_addr + kk * 2048, kQBox, 1024);
               ptx::mma_ts(tmem + kColDV, tmem + a_col, bd, id_acc, (s > 0 || kk > 0) ? 1u : 0u);
             }
-            ptx::mma_commit(&sm.doh_free);
+            // this side is done with Q_i / dO_i once S^T_i, dP^T_i and dV's product are
+            ptx::mma_commit(&sm.qdo_empty[qs]);
           }
           __syncwarp();
-          if (s + 1 < n && !(dp_other(i + 1) && s_own(i + 1) && dp_own(i + 1))) { ok = false; break; }
+          // the next step's S^T overwrites P^T_i in place after the dV product
+          // just issued has read it (products of one thread run in order)
+          if (s + 1 < n && !(issue_s(i + 1) && issue_dp(i + 1))) { ok = false; break; }
         }
       } else {
         for (int s = 0; ok && s < n; ++s) {
           const uint32_t i = gi + s;
-          // dK += dS^T_i Q_i: A = dS^T (key rows, query contiguous), B = the own
-          // half of Q_i MN-major
-          if (!W.warp(&sm.qh_full, i & 1)) { ok = false; break; }
+          const int qs = i % kStages;
+          // dK += dS^T_i Q_i: A = dS^T (key rows, query contiguous), B = the Q_i
+          // half MN-major
+          if (!W.warp(&sm.qdo_full[qs], (i / kStages) & 1)) { ok = false; break; }
           if (!W.warp(&sm.ds_full, i & 1)) { ok = false; break; }
           if (s == 0 && !W.warp(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
           ptx::tc_fence_after();
-          const uint32_t q_addr = ptx::smem_u32(sm.q[0]);
+          const uint32_t q_addr = ptx::smem_u32(sm.q[qs]) + half_q;
           if (ptx::elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < kQB / 16; ++kk) {
@@ -517,19 +475,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
               const uint64_t bd = ptx::sdesc_sw128(q_addr + kk * 2048, kQBox, 1024);
               ptx::mma_ss(tmem + kColDK, ad, bd, id_acc, (s > 0 || kk > 0) ? 1u : 0u);
             }
-            ptx::mma_commit(&sm.qh_free);
-          }
-          __syncwarp();
-          // dQ_i^T = K^T dS^T_i for the half: A = the K half transposed (head dim
-          // contiguous: MN-major), B = dS^T as (query, key), query contiguous: MN-major
-          if (i > 0 && !W.warp(&sm.dq_free, (i - 1) & 1)) { ok = false; break; }
-          ptx::tc_fence_after();
-          if (ptx::elect_one()) {
+            ptx::mma_commit(&sm.qdo_empty[qs]);
+            // dQ_i^T = K^T dS^T_i for the half: A = the K half transposed (head
+            // dim contiguous: MN-major), B = dS^T as (query, key), query
+            // contiguous: MN-major.  The compute warps have read dP^T_i (dS^T_i
+            // is complete), so dQ^T_i takes its columns.
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
               const uint64_t ad = ptx::sdesc_sw128(k_addr + half_k + kk * 2048, kKBox, 1024);
               const uint64_t bd = ptx::sdesc_sw128(ds_addr + kk * 2048, kDsBytes, 1024);
-              ptx::mma_ss(tmem + kColDQ, ad, bd, id_dq, kk > 0 ? 1u : 0u);
+              ptx::mma_ss(tmem + kColDPQ, ad, bd, id_dq, kk > 0 ? 1u : 0u);
             }
             ptx::mma_commit(&sm.dq_full);
             ptx::mma_commit(&sm.ds_free);
@@ -541,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
       if (n == 0 && !W.warp(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
       gi += n;
       if (ptx::elect_one()) {
-        ptx::mma_commit(&sm.kv_empty);
+        ptx::mma_commit(&sm.k_empty);
         ptx::mma_commit(&sm.acc_done);
       }
       __syncwarp();
@@ -572,6 +527,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
       if (!valid) break;
       const SeqInfo si = seq_info(p, un.seq);
       const int g = un.head, k0 = un.tile * kTile, kj = k0 + t;
+      // V of the unit into tensor memory.  Its previous readers, the dP^T
+      // products of the previous unit, completed before that unit's last
+      // dp_full, which every compute warp has seen.
+      load_v_rows(tmem + lane_base + kColV + 64 * ch, t, 128 * ch, p, si, g, k0);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sm.v_full);
       BwdSteps steps;
       steps.init(p, si.len, un.tile);
       int hh, qb, bits, n = 0;
@@ -579,16 +541,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
       // reaches the unit's group-wide agreement below, like every other warp.
       bool alive = true;
       while (steps.next(hh, qb, bits)) {
-        const int st = i & 1, rs = i & 1;
+        const int qs = i % kStages;
         const int q0 = qb * kQB;
-        // the own half of Q_i arrives with the step's LSE and D rows
-        bool mine = alive && W.warp(&sm.qh_full, i & 1) && W.warp(&sm.st_full[st], (i >> 1) & 1);
+        bool mine = alive && W.warp(&sm.qdo_full[qs], (i / kStages) & 1) && W.warp(&sm.st_full, i & 1);
         float pv[32];
         if (mine) {
           // P^T = exp2(S^T * scale * log2 e - LSE * log2 e) for 32 query columns
           ptx::tc_fence_after();
           uint32_t sr[32];
-          ptx::tmem_ld32(tmem + lane_base + kColS + st * kQB + 32 * ch, sr);
+          ptx::tmem_ld32(tmem + lane_base + kColS + 32 * ch, sr);
           ptx::tmem_ld_wait();
           const bool need_mask = (k0 + kTile > si.len) || (elem_causal && q0 < k0 + kTile - 1) || bits != 3;
           // visible: key listed for this query block, inside the sequence and
@@ -597,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
           const int lo = elem_causal ? kj - q0 - 32 * ch : -1;
           uint32_t pk[16];
           const float2 c2 = make_float2(c, c);
-          const float2* nl2 = reinterpret_cast<const float2*>(&sm.nlse2[rs][32 * ch]);
+          const float2* nl2 = reinterpret_cast<const float2*>(&sm.nlse2[qs][32 * ch]);
 #pragma unroll
           for (int w = 0; w < 16; ++w) {
             const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * w]), __uint_as_float(sr[2 * w + 1])), c2, nl2[w]);
@@ -611,27 +572,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
           }
 #pragma unroll
           for (int w = 0; w < 16; ++w) pk[w] = ptx::pack_bf16x2(pv[2 * w], pv[2 * w + 1]);
-          ptx::tmem_st16(tmem + lane_base + kColS + st * kQB + 32 * ch, pk);
+          ptx::tmem_st16(tmem + lane_base + kColS + 32 * ch, pk);
           ptx::tmem_st_wait();
           ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&sm.pt_full[st]);
+          if (lane == 0) ptx::mbar_arrive(&sm.pt_full);
           mine = W.warp(&sm.dp_full, i & 1);
         }
         if (mine) {
           ptx::tc_fence_after();
           uint32_t dr[32];
-          ptx::tmem_ld32(tmem + lane_base + kColDP + 32 * ch, dr);
+          ptx::tmem_ld32(tmem + lane_base + kColDPQ + 32 * ch, dr);
           ptx::tmem_ld_wait();
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&sm.dp_free);
           // dS^T_{i-1} has been read by its dK and dQ^T products
           mine = W.warp(&sm.ds_free, (i & 1) ^ 1);
           if (mine) {
             // dS^T = P^T o (dP^T - D), bf16, 128-byte swizzled row t of the dS^T tile
             uint8_t* dsrow = sm.ds + t * 128;
-            const float2* nd2 = reinterpret_cast<const float2*>(&sm.ndlt[rs][32 * ch]);
+            const float2* nd2 = reinterpret_cast<const float2*>(&sm.ndlt[qs][32 * ch]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               float d[8];
@@ -651,6 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
               const int chunk = 4 * ch + j;
               *reinterpret_cast<uint4*>(dsrow + ((chunk ^ (t & 7)) * 16)) = o;
             }
+            // the dP^T_i reads above are complete (tmem_ld_wait) before this
+            // arrival lets dQ^T_i overwrite those columns
+            ptx::tc_fence_before();
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&sm.ds_full);
@@ -701,8 +662,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd256(const __grid_constant
         if (!dq_all(W.warp(&sm.dq_full, i & 1))) { ok = false; break; }
         ptx::tc_fence_after();
         uint32_t v0[32], v1[32];
-        ptx::tmem_ld32(tmem + lane_base + kColDQ, v0);
-        ptx::tmem_ld32(tmem + lane_base + kColDQ + 32, v1);
+        ptx::tmem_ld32(tmem + lane_base + kColDPQ, v0);
+        ptx::tmem_ld32(tmem + lane_base + kColDPQ + 32, v1);
         ptx::tmem_ld_wait();
         ptx::tc_fence_before();
         __syncwarp();
@@ -759,17 +720,15 @@ cudaError_t launch_tc_bwd256(const KParams& p, int sms, cudaStream_t st) {
   if (p.n_units == 0) return cudaSuccess;
   if (p.head_dim != kD || !p.dq_accum) return cudaErrorInvalidValue;
   BwdArgs a;
-  TileMap mq, mk, mv, mdo, macc;
+  TileMap mq, mk, mdo, macc;
   cudaError_t e;
   if ((e = make_tile_map(&mq, p.q, p, false, kQB)) != cudaSuccess) return e;
   if ((e = make_tile_map(&mdo, p.dout, p, false, kQB)) != cudaSuccess) return e;
   if ((e = make_tile_map(&mk, p.k, p, true)) != cudaSuccess) return e;
-  if ((e = make_tile_map(&mv, p.v, p, true)) != cudaSuccess) return e;
   if ((e = make_acc_map(&macc, p.dq_accum, p, kDqRows, kDH)) != cudaSuccess) return e;
   a.tq = mq.map;
   a.tdo = mdo.map;
   a.tk = mk.map;
-  a.tv = mv.map;
   a.tacc = macc.map;
   a.q_rows_inner = mq.rows_inner;
   a.kv_rows_inner = mk.rows_inner;
