@@ -22,11 +22,21 @@
 // section 4.2: whoever finishes first takes the next block) and hands it to the
 // other roles through a two-slot ring in shared memory.
 //
-// Warp roles (448 threads):
+// V is the A operand of dP^T only, so it sits in tensor memory (packed bf16
+// pairs, D / 2 columns), written once per unit by the compute warps: dP^T then
+// reads only dO_i from shared memory, and its N = 64 products run at the full
+// rate instead of being paced by shared-memory reads.  Tensor memory:
+//   dV [0,128)  dK [128,256)  S^T / P^T [256,320)  V [320,384)  dP^T [384,448)
+//   dQ^T [448,512).
+// With one S^T buffer, the next step's S^T is issued after this step's dV
+// product, which reads P^T in place.
+//
+// Warp roles (480 threads):
 //   warps 0-7    compute: warp w covers TMEM lane quarter w % 4 (key rows) and
 //                query columns 32 (w / 4) .. +31 of the step.  Per step: P^T and
-//                dS^T.  Unit epilogue: warps 0-3 dK, warps 4-7 dV.
-//   warp 8       TMA producer (K, V per unit; Q_i, dO_i in a 3-stage ring; LSE, D rows)
+//                dS^T.  Per unit: head-dim half w / 4 of V for their key rows
+//                into tensor memory.  Unit epilogue: warps 0-3 dK, warps 4-7 dV.
+//   warp 8       TMA producer (K per unit; Q_i, dO_i in a 3-stage ring; LSE, D rows)
 //   warp 9       tensor-core issuer for S^T, dP^T and dV (whole warp, one
 //                elected lane issues)
 //   warp 14      tensor-core issuer for dK and dQ^T.  tcgen05.mma holds its
@@ -60,18 +70,17 @@ constexpr uint32_t kDsBytes = kTile * kQB * 2;    // dS^T: 128 key rows x 64 bf1
 constexpr int kStages = 3;  // Q_i / dO_i ring: loads run two steps ahead of the products
 constexpr int kThreads = 480;
 constexpr uint32_t kTmemCols = 512;
-// dV [0,128) dK [128,256) S^T [256,320) [320,384) dP^T [384,448) dQ^T [448,512)
-constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384, kColDQ = 448;
+// dV [0,128) dK [128,256) S^T [256,320) V [320,384) dP^T [384,448) dQ^T [448,512)
+constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColV = 320, kColDP = 384, kColDQ = 448;
 
 struct BwdArgs {
-  CUtensorMap tq, tk, tv, tdo, tacc;
+  CUtensorMap tq, tk, tdo, tacc;
   int q_rows_inner, kv_rows_inner, acc_rows_inner;
   KParams p;
 };
 
 struct Smem {
   uint8_t k[kTileBytes];
-  uint8_t v[kTileBytes];
   uint8_t q[kStages][kQTileBytes];
   uint8_t dO[kStages][kQTileBytes];
   uint8_t ds[2][kDsBytes];   // dS^T (128-byte swizzled rows)
@@ -79,7 +88,7 @@ struct Smem {
   float nlse2[kStages][kQB];  // -LSE * log2(e) of the stage's query rows (-inf: no key / past the end)
   float ndlt[kStages][kQB];   // -D of the stage's query rows
   uint64_t unit_full[2], unit_empty[2];
-  uint64_t kv_full, kv_empty, qdo_full[kStages], qdo_empty[kStages];
+  uint64_t k_full, k_empty, v_full, qdo_full[kStages], qdo_empty[kStages];
   uint64_t st_full[2], pt_full[2], dp_full, dp_free, ds_full[2], ds_free[2], dq_full, dq_free;
   uint64_t acc_done, acc_free, drain[2];
   int unit_slot[2][4];
@@ -175,6 +184,31 @@ __device__ __forceinline__ void store_kv_rows(uint32_t taddr_row, bool have, flo
   }
 }
 
+// One warp copies head-dim columns c0 .. c0 + D / 2 - 1 of its 32 key rows of
+// V (row k0 + row of head g; zeros past the sequence end) into tensor memory at
+// taddr_row as packed bf16 pairs, the layout of an A operand read from tensor
+// memory (column j holds elements 2j and 2j + 1 of the row).
+template <int D>
+__device__ __forceinline__ void load_v_rows(uint32_t taddr_row, int row, int c0, const KParams& p,
+                                            const SeqInfo& si, int g, int k0) {
+  constexpr int kCols = D / 4;  // packed columns per warp: D / 2 elements
+  const bool ok = k0 + row < si.len && check_kv_row(p, si, g, k0 + row);
+  const uint4* src =
+      reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.v) + (ok ? kv_off(p, si, g, k0 + row) : 0) + c0);
+  uint32_t r[kCols];
+#pragma unroll
+  for (int j = 0; j < kCols / 4; ++j) {
+    const uint4 x = ok ? __ldg(src + j) : make_uint4(0u, 0u, 0u, 0u);
+    r[4 * j] = x.x;
+    r[4 * j + 1] = x.y;
+    r[4 * j + 2] = x.z;
+    r[4 * j + 3] = x.w;
+  }
+  if constexpr (kCols == 32) ptx::tmem_st32(taddr_row, r);
+  else ptx::tmem_st16(taddr_row, r);
+  ptx::tmem_st_wait();
+}
+
 // kDq false: dK and dV only (dQ comes from the query-stationary pass).
 // D: head dim, 64 or 128 (shared memory is laid out for 128 either way).  With
 // D = 64 the dQ^T product still runs with M = 128: the upper half of the K tile
@@ -200,8 +234,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       ptx::mbar_init(&sm.ds_full[s], 8);
       ptx::mbar_init(&sm.ds_free[s], 1);
     }
-    ptx::mbar_init(&sm.kv_full, 1);
-    ptx::mbar_init(&sm.kv_empty, 2);  // one commit per MMA warp
+    ptx::mbar_init(&sm.k_full, 1);
+    ptx::mbar_init(&sm.k_empty, 2);  // one commit per MMA warp
+    ptx::mbar_init(&sm.v_full, 8);   // compute warps
     ptx::mbar_init(&sm.dp_full, 1);
     ptx::mbar_init(&sm.dp_free, 8);
     ptx::mbar_init(&sm.dq_full, 1);
@@ -258,18 +293,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       const SeqInfo si = seq_info(p, un.seq);
       const int g = un.head, k0 = un.tile * kTile;
       // The unit is known a few steps before the previous one ends: start its K
-      // and V on their way into L2, so the load below does not wait on memory.
-      if (lane == 0) {
-        tma_prefetch_tile(&a.tk, a.kv_rows_inner, map_row(si, k0), g, si.b, D / 64);
-        tma_prefetch_tile(&a.tv, a.kv_rows_inner, map_row(si, k0), g, si.b, D / 64);
-      }
-      // K and V of the unit, once the previous unit's products are done with them
-      if (!W.warp(&sm.kv_empty, (n_units & 1) ^ 1)) break;
+      // on its way into L2, so the load below does not wait on memory.
+      if (lane == 0) tma_prefetch_tile(&a.tk, a.kv_rows_inner, map_row(si, k0), g, si.b, D / 64);
+      // K of the unit, once the previous unit's products are done with it
+      if (!W.warp(&sm.k_empty, (n_units & 1) ^ 1)) break;
       if (lane == 0) {
         check_kv_row(p, si, g, k0);
-        ptx::mbar_arrive_expect_tx(&sm.kv_full, 2 * tile_bytes<D>());
-        tma_tile(sm.k, &a.tk, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b, kHalfTileBytes, D / 64);
-        tma_tile(sm.v, &a.tv, a.kv_rows_inner, &sm.kv_full, map_row(si, k0), g, si.b, kHalfTileBytes, D / 64);
+        ptx::mbar_arrive_expect_tx(&sm.k_full, tile_bytes<D>());
+        tma_tile(sm.k, &a.tk, a.kv_rows_inner, &sm.k_full, map_row(si, k0), g, si.b, kHalfTileBytes, D / 64);
       }
       kv_loaded = true;
       last_kv_phase = n_units & 1;
@@ -311,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       if (!ok) break;
     }
     if (lane == 0) {
-      if (kv_loaded) W.drain(&sm.kv_full, last_kv_phase);
+      if (kv_loaded) W.drain(&sm.k_full, last_kv_phase);
       for (int s = 0; s < kStages; ++s)
         if (last_qdo_phase[s] >= 0) W.drain(&sm.qdo_full[s], (uint32_t)last_qdo_phase[s]);
     }
@@ -328,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
     constexpr uint32_t id_st = ptx::idesc_bf16(128, 64, false, false);   // S^T, dP^T
     constexpr uint32_t id_acc = ptx::idesc_bf16(128, D, false, true);    // dV, dK
     constexpr uint32_t id_dq = ptx::idesc_bf16(128, 64, true, true);     // dQ^T
-    const uint32_t k_addr = ptx::smem_u32(sm.k), v_addr = ptx::smem_u32(sm.v);
+    const uint32_t k_addr = ptx::smem_u32(sm.k);
     uint32_t n_units = 0, gi = 0;  // gi: global step counter (all units)
     bool ok = true;
 
@@ -342,14 +373,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ad = ptx::sdesc_sw128(k_addr + (kk >> 2) * kHalfTileBytes + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = ptx::sdesc_sw128(q_addr + (kk >> 2) * kQBoxBytes + (kk & 3) * 32, 16, 1024);
-          ptx::mma_ss(tmem + kColS + st * 64, ad, bd, id_st, kk > 0 ? 1u : 0u);
+          ptx::mma_ss(tmem + kColS, ad, bd, id_st, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(&sm.st_full[st]);
       }
       __syncwarp();
       return true;
     };
-    auto issue_dp = [&](uint32_t i) -> bool {  // dP^T_i = V dO_i^T (stage known loaded)
+    // dP^T_i = V dO_i^T (stage known loaded): A = V from tensor memory (8
+    // packed columns per 16 head-dim columns), B = dO_i K-major.  It overwrites
+    // dP^T_{i-1}, so the compute warps must have read that.
+    auto issue_dp = [&](uint32_t i) -> bool {
       const int qs = i % kStages;
       if (i > 0 && !W.warp(&sm.dp_free, (i - 1) & 1)) return false;
       ptx::tc_fence_after();
@@ -357,9 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       if (ptx::elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = ptx::sdesc_sw128(v_addr + (kk >> 2) * kHalfTileBytes + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = ptx::sdesc_sw128(do_addr + (kk >> 2) * kQBoxBytes + (kk & 3) * 32, 16, 1024);
-          ptx::mma_ss(tmem + kColDP, ad, bd, id_st, kk > 0 ? 1u : 0u);
+          ptx::mma_ts(tmem + kColDP, tmem + kColV + 8 * kk, bd, id_st, kk > 0 ? 1u : 0u);
         }
         ptx::mma_commit(&sm.dp_full);
       }
@@ -383,14 +416,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
         int hh, qb, bits;
         while (t.next(hh, qb, bits)) ++n;
       }
-      if (!W.warp(&sm.kv_full, n_units & 1)) { ok = false; break; }
+      if (!W.warp(&sm.k_full, n_units & 1)) { ok = false; break; }
       ptx::tc_fence_after();
       if (side == 0) {
-        if (n > 0) ok = issue_s(gi) && issue_dp(gi);
+        // the unit's V is in tensor memory before its first dP^T product
+        if (n > 0) ok = issue_s(gi) && W.warp(&sm.v_full, n_units & 1) && issue_dp(gi);
+        else ok = W.warp(&sm.v_full, n_units & 1);
         for (int s = 0; ok && s < n; ++s) {
           const uint32_t i = gi + s;
           const int st = i & 1, qs = i % kStages;
-          if (s + 1 < n && !issue_s(i + 1)) { ok = false; break; }
           // dV += P^T_i dO_i: A = P^T from tensor memory, B = dO_i as (head dim, query) MN-major
           if (!W.warp(&sm.pt_full[st], (i >> 1) & 1)) { ok = false; break; }
           // before the unit's first dV product: the previous unit's epilogue has
@@ -403,16 +437,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
             for (int kk = 0; kk < 4; ++kk) {
               // P^T of query columns 16 kk .. +15: the compute warps of column half
               // kk / 2 write their 16 packed columns at 32 (kk / 2) within the S^T buffer
-              const uint32_t a_col = kColS + st * 64 + 32 * (kk >> 1) + (kk & 1) * 8;
+              const uint32_t a_col = kColS + 32 * (kk >> 1) + (kk & 1) * 8;
               const uint64_t bd = ptx::sdesc_sw128(do_addr + kk * 2048, kQBoxBytes, 1024);
               ptx::mma_ts(tmem + kColDV, tmem + a_col, bd, id_acc, (s > 0 || kk > 0) ? 1u : 0u);
             }
+            // this side is done with Q_i / dO_i once S^T_i, dP^T_i and dV's product are
+            ptx::mma_commit(&sm.qdo_empty[qs]);
           }
           __syncwarp();
-          if (s + 1 < n && !issue_dp(i + 1)) { ok = false; break; }
-          // this side is done with Q_i / dO_i once S^T_i, dP^T_i and dV's product are
-          if (ptx::elect_one()) ptx::mma_commit(&sm.qdo_empty[qs]);
-          __syncwarp();
+          // one S^T buffer: the next S^T overwrites P^T_i after the dV product just
+          // issued has read it (products of one thread run in order)
+          if (s + 1 < n && !(issue_s(i + 1) && issue_dp(i + 1))) { ok = false; break; }
         }
       } else {
         for (int s = 0; ok && s < n; ++s) {
@@ -457,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       if (n == 0 && !W.warp(&sm.acc_free, (n_units & 1) ^ 1)) { ok = false; break; }
       gi += n;
       if (ptx::elect_one()) {
-        ptx::mma_commit(&sm.kv_empty);
+        ptx::mma_commit(&sm.k_empty);
         ptx::mma_commit(&sm.acc_done);
       }
       __syncwarp();
@@ -487,6 +522,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
       if (!valid) break;
       const SeqInfo si = seq_info(p, un.seq);
       const int g = un.head, k0 = un.tile * kTile, kj = k0 + t;
+      // V of the unit into tensor memory (warp column half ch: head-dim columns
+      // D/2 ch ..).  Its previous readers, the dP^T products of the previous
+      // unit, completed before that unit's last dp_full, which this warp has seen.
+      load_v_rows<D>(tmem + lane_base + kColV + (D / 4) * ch, t, (D / 2) * ch, p, si, g, k0);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&sm.v_full);
       BwdSteps steps;
       steps.init(p, si.len, un.tile);
       int hh, qb, bits, n = 0;
@@ -502,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
           // P^T = exp2(S^T * scale * log2 e - LSE * log2 e) for 32 query columns
           ptx::tc_fence_after();
           uint32_t sr[32];
-          ptx::tmem_ld32(tmem + lane_base + kColS + st * 64 + 32 * ch, sr);
+          ptx::tmem_ld32(tmem + lane_base + kColS + 32 * ch, sr);
           ptx::tmem_ld_wait();
           const bool need_mask = (k0 + kTile > si.len) || (elem_causal && q0 < k0 + kTile - 1) || bits != 3;
           // visible: key listed for this query block, inside the sequence and
@@ -525,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_bwd(const __grid_constant__ 
           }
 #pragma unroll
           for (int w = 0; w < 16; ++w) pk[w] = ptx::pack_bf16x2(pv[2 * w], pv[2 * w + 1]);
-          ptx::tmem_st16(tmem + lane_base + kColS + st * 64 + 32 * ch, pk);
+          ptx::tmem_st16(tmem + lane_base + kColS + 32 * ch, pk);
           ptx::tmem_st_wait();
           ptx::tc_fence_before();
           __syncwarp();
@@ -659,18 +701,16 @@ bool tc_bwd_available() { return true; }
 cudaError_t launch_tc_bwd(const KParams& p, int sms, cudaStream_t st, bool with_dq) {
   if (p.n_units == 0) return cudaSuccess;
   BwdArgs a;
-  TileMap mq, mk, mv, mdo, macc;
+  TileMap mq, mk, mdo, macc;
   cudaError_t e;
   if ((e = make_tile_map(&mq, p.q, p, false, kQB)) != cudaSuccess) return e;
   if ((e = make_tile_map(&mdo, p.dout, p, false, kQB)) != cudaSuccess) return e;
   if ((e = make_tile_map(&mk, p.k, p, true)) != cudaSuccess) return e;
-  if ((e = make_tile_map(&mv, p.v, p, true)) != cudaSuccess) return e;
   if (with_dq && (e = make_acc_map(&macc, p.dq_accum, p, kQB)) != cudaSuccess) return e;
   if (!with_dq) std::memset(&macc, 0, sizeof(macc));
   a.tq = mq.map;
   a.tdo = mdo.map;
   a.tk = mk.map;
-  a.tv = mv.map;
   a.tacc = macc.map;
   a.q_rows_inner = mq.rows_inner;
   a.kv_rows_inner = mk.rows_inner;
