@@ -441,18 +441,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         ++n_v;
         return true;
       };
+      // K(j) then V(j): the first P V product, which the next tile's S waits
+      // behind, needs V(0) before K(1)
       PartList<kSparse> t;
       t.init(p, si.len, q0, part);
       int kt, bits;
-      bool have = t.next(kt, bits);
-      if (have && !load_k(kt)) { ok = false; break; }
-      while (have) {
-        int nkt, nbits;
-        const bool nhave = t.next(nkt, nbits);
-        if (nhave && !load_k(nkt)) { ok = false; break; }
-        if (!load_v(kt)) { ok = false; break; }
-        have = nhave;
-        kt = nkt;
+      while (t.next(kt, bits)) {
+        if (!load_k(kt) || !load_v(kt)) { ok = false; break; }
       }
       if (!ok) break;
     }
