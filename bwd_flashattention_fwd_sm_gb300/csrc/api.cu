@@ -6,6 +6,7 @@
 // boundary indices are checked, never trusted, because an out-of-range index
 // shows up as a rare hang).  Device-side failures (a bounded wait that ran out)
 // go to a per-device status word, read back by attn_get_status().
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -200,6 +201,8 @@ struct Layout {
   // forward with a split key range: parts per unit and the parts' partial results
   int n_split;
   size_t part_o, part_ml;
+  // forward on the tensor cores in units of one 128-row query tile
+  bool fwd_half;
 };
 
 // Parts to cut each forward unit's key range into.  With fewer units than a
@@ -219,6 +222,14 @@ int forward_split(const attn_params_t* p, const Problem& pr, long long n_units) 
   if (ns > key_tiles / kSplitMinTiles) ns = key_tiles / kSplitMinTiles;
   return ns > 1 ? (int)ns : 1;
 }
+
+// Forward units of one 128-row query tile instead of two when the two-tile
+// units would be fewer than a GB300's 152 SMs (a fixed count, so that the
+// workspace size needs no device query).  The CTA's two softmax warpgroups then
+// split the tile's key range and merge at the end.  Measured on B1 H8 S2048
+// (64 two-tile units): forward 399 -> 472 TFLOP/s; on B2 H16 S2048 causal (256
+// units, more than one per SM) it lost 25%, hence the threshold.
+constexpr long long kHalfUnitsBelow = 152;
 
 KParams base_kparams(const attn_params_t* p, const Problem& pr) {
   KParams k;
@@ -254,7 +265,9 @@ KParams base_kparams(const attn_params_t* p, const Problem& pr) {
   return k;
 }
 
-Layout layout_for(const attn_params_t* p, const Problem& pr, bool backward) {
+// allow_half: the bf16 forward may take 128-row units (kHalfUnitsBelow); the
+// FP8 forward and block masks keep 256-row units.
+Layout layout_for(const attn_params_t* p, const Problem& pr, bool backward, bool allow_half = false) {
   Layout L;
   std::memset(&L, 0, sizeof(L));
   // tensor cores: forward units are 256 query rows (two 128-row tiles sharing
@@ -264,6 +277,12 @@ Layout layout_for(const attn_params_t* p, const Problem& pr, bool backward) {
   KParams k = base_kparams(p, pr);
   L.n_units = count_units(k, p->cu_seqlens_host, backward, L.tile_rows);
   L.n_split = backward ? 1 : forward_split(p, pr, L.n_units);
+  if (allow_half && !backward && L.n_split == 1 && L.tile_rows == 256 && p->mask != ATTN_MASK_BLOCK &&
+      L.n_units < kHalfUnitsBelow) {
+    L.fwd_half = true;
+    L.tile_rows = 128;
+    L.n_units = count_units(k, p->cu_seqlens_host, backward, L.tile_rows);
+  }
   L.n_units *= L.n_split;
   size_t off = 0;
   L.counter = off;
@@ -309,6 +328,7 @@ Layout layout_for(const attn_params_t* p, const Problem& pr, bool backward) {
 // The forward's split key range (parts and partial buffers) from the layout.
 void set_split(KParams& kp, const Layout& L, char* ws) {
   kp.n_split = L.n_split;
+  kp.fwd_half = L.fwd_half ? 1 : 0;
   if (L.n_split > 1) {
     kp.part_o = reinterpret_cast<float*>(ws + L.part_o);
     kp.part_ml = reinterpret_cast<float*>(ws + L.part_ml);
@@ -375,7 +395,8 @@ size_t attn_fwd_workspace_size(const attn_params_t* p) {
   Problem pr;
   if (validate_params(p, &pr) != ATTN_OK) return SIZE_MAX;
   if (pr.empty) return 0;
-  return layout_for(p, pr, false).total;
+  // enough for the bf16 forward and for the FP8 forward, which may lay it out differently
+  return std::max(layout_for(p, pr, false, true).total, layout_for(p, pr, false, false).total);
 }
 
 size_t attn_bwd_workspace_size(const attn_params_t* p) {
@@ -394,7 +415,7 @@ attn_status_t attn_fwd(const attn_params_t* p, const void* q, const void* k, con
   if ((s = check_ptr(q, "q")) || (s = check_ptr(k, "k")) || (s = check_ptr(v, "v")) ||
       (s = check_ptr(o, "o")) || (s = check_ptr(lse, "lse")))
     return s;
-  const Layout L = layout_for(p, pr, false);
+  const Layout L = layout_for(p, pr, false, true);
   if ((s = check_workspace(workspace, workspace_bytes, L.total))) return s;
 
   int* status = nullptr;

@@ -71,6 +71,10 @@ struct KParams {
   int n_split;
   float* part_o;
   float* part_ml;
+  // Forward on the tensor cores with few units: units of one 128-row query
+  // tile instead of two (Unit::tile counts 128-row tiles); the kernel leaves
+  // the pair's other tile idle.
+  int fwd_half;
 
   int* status;               // device status word
   unsigned long long wait_limit_ns;  // bounded-wait limit for pipeline barriers

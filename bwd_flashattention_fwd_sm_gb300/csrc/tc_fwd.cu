@@ -102,6 +102,11 @@ struct Smem {
   int unit_slot[2][4];  // seq, head, 256-row tile, valid
   uint32_t tmem_base;
   ptx::Abort abort;
+  // 128-row units: the second softmax warpgroup's row max and sum for the
+  // first, which merges the two halves of the key range
+  uint64_t pair_full, pair_free;
+  float pair_m[kTile], pair_l[kTile];
+  int pair_have;
 };
 
 static_assert(sizeof(Smem<FwdCfg<false>>) + 1024 <= 232448, "shared memory per CTA is at most 227 KiB");
@@ -142,11 +147,16 @@ __device__ __forceinline__ bool read_unit(const SM& sm, int slot, Unit& un) {
 // [lo, hi) of the unit's tile list, cut into p.n_split near-equal runs (dense
 // and causal lists, of n_dense entries; no split: the whole list).  Every role
 // walks the same entries, so the pipeline's rings stay in step.
-template <bool kSparse>
+//
+// kPair (128-row units): the unit owns one of the two query tiles (keep: its
+// bits, 0x0F for tile 0 or 0xF0 for tile 1).  Key tiles without its bits are
+// skipped, and the kept ones alternate between the two slots (bits 0-3, then
+// 4-7, ...), so that the CTA's two halves split the tile's key range.
+template <bool kSparse, bool kPair = false>
 struct PartList {
   KvTileList2<kSparse> t;
   int e, lo, hi;
-  __device__ void init(const KParams& p, int len, int q0, int part) {
+  __device__ void init(const KParams& p, int len, int q0, int part, int = 0xFF) {
     t.init(p, len, q0);
     e = 0;
     lo = 0;
@@ -164,6 +174,43 @@ struct PartList {
     return false;
   }
 };
+template <bool kSparse>
+struct PartList<kSparse, true> {
+  KvTileList2<kSparse> t;
+  int keep, kept;
+  __device__ void init(const KParams& p, int len, int q0, int, int keep_) {
+    t.init(p, len, q0);
+    keep = keep_;
+    kept = 0;
+  }
+  __device__ bool next(int& kt, int& bits) {
+    while (t.next(kt, bits)) {
+      const int nib = (bits & keep) >> (keep == 0xF0 ? 4 : 0);
+      if (nib == 0) continue;
+      bits = nib << (4 * (kept++ & 1));
+      return true;
+    }
+    return false;
+  }
+};
+
+// The rows of a forward unit: the first row of its 256-row pair of query tiles
+// and the bits of the tiles it owns (both; with 128-row units one, whose key
+// tiles the two halves of the CTA then share, see PartList).
+struct UnitRows {
+  int q0, keep;
+};
+template <bool kPair>
+__device__ __forceinline__ UnitRows unit_rows(const Unit& un) {
+  if constexpr (kPair) return UnitRows{(un.tile >> 1) * 2 * kTile, (un.tile & 1) ? 0xF0 : 0x0F};
+  return UnitRows{un.tile * 2 * kTile, 0xFF};
+}
+// First row of the query rows of slot q (with 128-row units both slots hold
+// the unit's one tile).
+template <bool kPair>
+__device__ __forceinline__ int slot_row(const Unit& un, int q) {
+  return kPair ? un.tile * kTile : un.tile * 2 * kTile + q * kTile;
+}
 
 // Stores P = 0 over eight tensor-memory columns (a 64-key half that no row of
 // the warp sees: nothing of it is read or exponentiated).
@@ -295,7 +342,7 @@ __device__ __forceinline__ float write_p8(const uint32_t (&sr)[128], float c, fl
 // K = 32 per instruction; P rounded to e4m3 into tensor memory; per-tile scales
 // folded into the softmax constant (Q and K) and into P (V, relative to the
 // head's largest V scale, which multiplies O in the epilogue).
-template <bool kSparse, int D, bool kFp8>
+template <bool kSparse, int D, bool kFp8, bool kPair = false>
 __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ FwdArgs a) {
   using SM = Smem<FwdCfg<kFp8>>;
   constexpr int kKStages = SM::kKStages, kVStages = SM::kVStages;
@@ -305,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Waiter<SM> W{sm, p};
   static_assert(!kFp8 || D == 128, "the FP8 forward has head dim 128");
+  static_assert(!kPair || (!kSparse && !kFp8), "128-row units: dense and causal bf16 only");
   constexpr uint32_t kLoadBytes = kFp8 ? (uint32_t)kTile * 128 : tile_bytes<D>();
 
   if (threadIdx.x == 0) {
@@ -330,6 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     ptx::mbar_init(&sm.turn[1], 1);
     ptx::mbar_init(&sm.drain[0], 1);
     ptx::mbar_init(&sm.drain[1], 1);
+    if constexpr (kPair) {
+      ptx::mbar_init(&sm.pair_full, 4);  // the second warpgroup's warps
+      ptx::mbar_init(&sm.pair_free, 4);  // the first warpgroup's warps
+    }
     sm.abort.flag = 0;
     ptx::fence_mbar_init();
   }
@@ -360,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       Unit un{0, 0, 0, 0};
       if (valid) {
         un = p.units[idx];
-        valid = check_unit(p, un, false, 2 * kTile);
+        valid = check_unit(p, un, false, kPair ? kTile : 2 * kTile);
       }
       if (lane == 0) {
         volatile int* s = sm.unit_slot[slot];
@@ -374,13 +426,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       if (!valid) break;
 
       const SeqInfo si = seq_info(p, un.seq);
-      const int h = un.head, g = h / p.group, q0 = un.tile * 2 * kTile;
+      const UnitRows ur = unit_rows<kPair>(un);
+      const int h = un.head, g = h / p.group, q0 = ur.q0;
       // which query tiles have work, for the Q loads
       bool act[2] = {false, false};
       const int part = p.n_split > 1 ? un.cost : 0;
       {
-        PartList<kSparse> t;
-        t.init(p, si.len, q0, part);
+        PartList<kSparse, kPair> t;
+        t.init(p, si.len, q0, part, ur.keep);
         int kt, bits;
         while (t.next(kt, bits)) {
           act[0] |= (bits & 0xF) != 0;
@@ -392,13 +445,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         const uint32_t c = n_q_loads[q];
         if (!W.warp(&sm.q_empty[q], ((c & 1) ^ 1))) { ok = false; break; }
         if (lane == 0) {
-          check_q_row(p, si, h, q0 + q * kTile);
+          const int qr0 = slot_row<kPair>(un, q);
+          check_q_row(p, si, h, qr0);
           ptx::mbar_arrive_expect_tx(&sm.q_full[q], kLoadBytes);
           if constexpr (kFp8)
-            ptx::tma_load_4d(sm.q[q], &a.tq, &sm.q_full[q], 0, q0 + q * kTile, h, si.b);
+            ptx::tma_load_4d(sm.q[q], &a.tq, &sm.q_full[q], 0, qr0, h, si.b);
           else
-            tma_tile(sm.q[q], &a.tq, a.q_rows_inner, &sm.q_full[q], map_row(si, q0 + q * kTile), h, si.b,
-                     kHalfTileBytes, D / 64);
+            tma_tile(sm.q[q], &a.tq, a.q_rows_inner, &sm.q_full[q], map_row(si, qr0), h, si.b, kHalfTileBytes,
+                     D / 64);
         }
         last_q_phase[q] = c & 1;
         ++n_q_loads[q];
@@ -443,8 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       };
       // K(j) then V(j): the first P V product, which the next tile's S waits
       // behind, needs V(0) before K(1)
-      PartList<kSparse> t;
-      t.init(p, si.len, q0, part);
+      PartList<kSparse, kPair> t;
+      t.init(p, si.len, q0, part, ur.keep);
       int kt, bits;
       while (t.next(kt, bits)) {
         if (!load_k(kt) || !load_v(kt)) { ok = false; break; }
@@ -495,11 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       if (!valid) break;
 
       const SeqInfo si = seq_info(p, un.seq);
-      PartList<kSparse> tl;
-      tl.init(p, si.len, un.tile * 2 * kTile, un.cost);
+      const UnitRows ur = unit_rows<kPair>(un);
+      PartList<kSparse, kPair> tl;
+      tl.init(p, si.len, ur.q0, un.cost, ur.keep);
       int n_act = 0;
       {
-        PartList<kSparse> t = tl;
+        PartList<kSparse, kPair> t = tl;
         int kt, bits;
         while (t.next(kt, bits)) n_act += ((bits >> (4 * q)) & 0xF) != 0;
       }
@@ -534,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         return true;
       };
 
-      PartList<kSparse> t = tl;
+      PartList<kSparse, kPair> t = tl;
       int kt, bits;
       bool have = t.next(kt, bits);
       uint32_t cur_stage = 0;
@@ -637,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     const bool elem_causal = p.mask == kMaskCausal || (p.mask == kMaskBlock && p.causal_in_block);
     const float c = p.scale_log2;
     const int row_half = r >= 64 ? 2 : 0;
-    uint32_t n_units_seen = 0, n_s = 0, n_o = 0;
+    uint32_t n_units_seen = 0, n_s = 0, n_o = 0, n_pair = 0;
     bool ok = true;
     for (;;) {
       const int slot = n_units_seen & 1;
@@ -651,7 +706,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
 
       const SeqInfo si = seq_info(p, un.seq);
       const int h = un.head;
-      const int q0 = un.tile * 2 * kTile + q * kTile;  // this tile's first row
+      const UnitRows ur = unit_rows<kPair>(un);
+      const int q0 = slot_row<kPair>(un, q);  // this tile's first row
       const int qi = q0 + r;
       float m_used = -INFINITY, l = 0.f;
       // FP8: this Q tile's scale and the KV head's largest V tile scale
@@ -669,8 +725,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         sv_ref = mx;
       }
       int n_done = 0;
-      PartList<kSparse> t;
-      t.init(p, si.len, un.tile * 2 * kTile, un.cost);
+      PartList<kSparse, kPair> t;
+      t.init(p, si.len, ur.q0, un.cost, ur.keep);
       int kt, bits8;
       while (t.next(kt, bits8)) {
         const int bits = (bits8 >> (4 * q)) & 0xF;
@@ -781,6 +837,71 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       if (n_done > 0) {
         if (!W.warp(&sm.o_final[q], n_o & 1)) { ok = false; break; }
         ptx::tc_fence_after();
+      }
+      if constexpr (kPair) {
+        // 128-row unit: both warpgroups hold partial results of the same rows
+        // over alternate key tiles.  The second hands its row max and sum to the
+        // first, which merges the two halves (each scaled to the larger max)
+        // and writes the rows; the first also frees the second's O columns.
+        if (q == 1) {
+          if (!W.warp(&sm.pair_free, (n_pair & 1) ^ 1)) { ok = false; break; }
+          sm.pair_m[r] = m_used;
+          sm.pair_l[r] = l;
+          if (r == 0) sm.pair_have = n_done > 0 ? 1 : 0;
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&sm.pair_full);
+          if (n_done > 0) ++n_o;
+          ++n_pair;
+          continue;
+        }
+        if (!W.warp(&sm.pair_full, n_pair & 1)) { ok = false; break; }
+        ptx::tc_fence_after();
+        const float m1 = sm.pair_m[r], l1 = sm.pair_l[r];
+        const bool have1 = sm.pair_have != 0;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sm.pair_free);
+        ++n_pair;
+        const bool in0 = l > 0.f, in1 = have1 && l1 > 0.f;
+        const float mm = in0 ? (in1 ? fmaxf(m_used, m1) : m_used) : (in1 ? m1 : 0.f);
+        const float a0 = in0 ? fast_exp2(m_used - mm) : 0.f, a1 = in1 ? fast_exp2(m1 - mm) : 0.f;
+        const float lt = l * a0 + (in1 ? l1 * a1 : 0.f);
+        const float inv = lt > 0.f ? (kFp8 ? sv_ref / lt : 1.f / lt) : 0.f;
+        const float w0 = a0 * inv, w1 = a1 * inv;
+        __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o);
+        const bool row_ok = qi < si.len && check_q_row(p, si, h, qi);
+        __nv_bfloat16* orow = O + (row_ok ? q_off(p, si, h, qi) : 0);
+        const float v0 = n_done > 0 ? w0 : 0.f, v1 = have1 ? w1 : 0.f;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 16; ++cc) {
+          uint32_t o0[16], o1[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o0[i] = o1[i] = 0u;
+          if (n_done > 0) ptx::tmem_ld16(tmem + lane_base + 256 + cc * 16, o0);
+          if (have1) ptx::tmem_ld16(tmem + lane_base + 256 + D + cc * 16, o1);
+          ptx::tmem_ld_wait();
+          if (row_ok) {
+#pragma unroll
+            for (int w4 = 0; w4 < 2; ++w4) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int i = w4 * 8 + 2 * j;
+                pk[j] = ptx::pack_bf16x2(__uint_as_float(o0[i]) * v0 + __uint_as_float(o1[i]) * v1,
+                                         __uint_as_float(o0[i + 1]) * v0 + __uint_as_float(o1[i + 1]) * v1);
+              }
+              *reinterpret_cast<uint4*>(orow + cc * 16 + w4 * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (n_done > 0) ptx::mbar_arrive(&sm.o_free[0]);
+          if (have1) ptx::mbar_arrive(&sm.o_free[1]);
+        }
+        if (n_done > 0) ++n_o;
+        if (row_ok) p.lse[row_index(p, si, h, qi)] = lt > 0.f ? (mm + fast_log2(lt)) * 0.69314718055994530942f : -INFINITY;
+        continue;
       }
       if (p.n_split > 1) {
         // one part of a split key range: the unnormalised O (times the V
@@ -1336,7 +1457,9 @@ cudaError_t launch_tc_fwd(const KParams& p, int sms, cudaStream_t st) {
   a.p = p;
   const size_t smem = sizeof(Smem<FwdCfg<false>>) + 1024;
   const int grid = p.n_units < sms ? p.n_units : sms;
-  auto kernel = p.head_dim == 64
+  auto kernel = p.fwd_half
+                    ? (p.head_dim == 64 ? k_tc_fwd<false, 64, false, true> : k_tc_fwd<false, 128, false, true>)
+                : p.head_dim == 64
                     ? (p.mask == kMaskBlock ? k_tc_fwd<true, 64, false> : k_tc_fwd<false, 64, false>)
                     : (p.mask == kMaskBlock ? k_tc_fwd<true, 128, false> : k_tc_fwd<false, 128, false>);
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
