@@ -134,6 +134,10 @@ typedef struct {
  * (per key block) tile lists.  The forward workspace holds the work list and,
  * when there are few work units for long sequences (each unit's key range is
  * then split into parts run on separate SMs), the parts' float32 partial results.
+ * With fewer units than a GB300 has SMs the bf16 forward lists one 128-row query
+ * tile per unit instead of two, which doubles its work list; the size returned
+ * covers both that list and the FP8 forward's, so one query serves attn_fwd and
+ * attn_fwd_fp8.
  */
 size_t attn_fwd_workspace_size(const attn_params_t* p);
 size_t attn_bwd_workspace_size(const attn_params_t* p);
