@@ -16,6 +16,12 @@
 // into P0, the tensor core runs P1 V and the next Q1 K^T, and the other way
 // round, so matrix work overlaps the exponentials.
 //
+// Few units (fewer than the SMs): units of one 128-row query tile (kPair).
+// Both slots then hold that tile; the key tiles it sees go to the two slots in
+// turn, so each warpgroup keeps a partial (row max, row sum, O) over half of
+// them, and at the end the second hands its max and sum to the first through
+// shared memory, which merges the two halves and writes the rows.
+//
 // Work distribution.  CTAs are persistent (one per SM); the TMA warp takes the
 // next unit from an atomic counter over the cost-ordered work list and hands
 // it to the other roles through a two-slot ring in shared memory, so long
