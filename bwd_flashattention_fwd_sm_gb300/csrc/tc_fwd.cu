@@ -281,25 +281,26 @@ __device__ __forceinline__ float write_p(const uint32_t (&sr)[128], float c, flo
       for (int cc = 4; cc < 8; ++cc) zero_p8(taddr + cc * 8);
     }
     return (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
-  }
+  } else {
 #pragma unroll
-  for (int cc = 0; cc < 8; ++cc) {
-    uint32_t pk[8];
+    for (int cc = 0; cc < 8; ++cc) {
+      uint32_t pk[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int k = cc * 16 + 2 * i;
-      const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2, nmu2);
-      float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-      if constexpr (kMask) {
-        if (!(k < thr)) pp.x = 0.f;
-        if (!(k + 1 < thr)) pp.y = 0.f;
+      for (int i = 0; i < 8; ++i) {
+        const int k = cc * 16 + 2 * i;
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), c2, nmu2);
+        float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+        if constexpr (kMask) {
+          if (!(k < thr)) pp.x = 0.f;
+          if (!(k + 1 < thr)) pp.y = 0.f;
+        }
+        rs2[i & 1] = __fadd2_rn(rs2[i & 1], pp);
+        pk[i] = ptx::pack_bf16x2(pp.x, pp.y);
       }
-      rs2[i & 1] = __fadd2_rn(rs2[i & 1], pp);
-      pk[i] = ptx::pack_bf16x2(pp.x, pp.y);
+      ptx::tmem_st8(taddr + cc * 8, pk);
     }
-    ptx::tmem_st8(taddr + cc * 8, pk);
+    return (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
   }
-  return (rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y);
 }
 
 // The FP8 form of write_p: P-hat = exp2(s * c - mu) rounded to e4m3 (mu also
