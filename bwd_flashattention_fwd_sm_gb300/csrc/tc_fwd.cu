@@ -785,11 +785,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         if (!need_mask) {
           if (lo_ok) {
 #pragma unroll
-            for (int k = 0; k < 64; ++k) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+            for (int k = 0; k < 64; k += 2)
+              e8[(k >> 1) & 7] = fmax3f(e8[(k >> 1) & 7], __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
           }
           if (hi_ok) {
 #pragma unroll
-            for (int k = 64; k < 128; ++k) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+            for (int k = 64; k < 128; k += 2)
+              e8[(k >> 1) & 7] = fmax3f(e8[(k >> 1) & 7], __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
           }
         } else {
 #pragma unroll
@@ -1320,11 +1322,13 @@ __global__ void __launch_bounds__(kThreads256, 1) k_tc_fwd256(const __grid_const
         if (!need_mask) {
           if (lo_ok) {
 #pragma unroll
-            for (int k = 0; k < 64; ++k) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+            for (int k = 0; k < 64; k += 2)
+              e8[(k >> 1) & 7] = fmax3f(e8[(k >> 1) & 7], __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
           }
           if (hi_ok) {
 #pragma unroll
-            for (int k = 64; k < 128; ++k) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+            for (int k = 64; k < 128; k += 2)
+              e8[(k >> 1) & 7] = fmax3f(e8[(k >> 1) & 7], __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
           }
         } else {
 #pragma unroll
