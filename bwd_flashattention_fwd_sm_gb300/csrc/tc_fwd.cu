@@ -783,15 +783,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
 #pragma unroll
         for (int u = 0; u < 8; ++u) e8[u] = -INFINITY;
         if (!need_mask) {
-          if (lo_ok) {
+          // two scores per max instruction at head dim 128; at 64 the
+          // two-input form measured 3% faster (register allocation)
+          if constexpr (D == 128) {
+            if (lo_ok) {
 #pragma unroll
-            for (int k = 0; k < 64; k += 2)
-              e8[(k >> 1) & 7] = fmax3f(e8[(k >> 1) & 7], __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
-          }
-          if (hi_ok) {
+              for (int k = 0; k < 64; k += 2)
+                e8[(k >> 1) & 7] = fmax3f(e8[(k >> 1) & 7], __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
+            }
+            if (hi_ok) {
 #pragma unroll
-            for (int k = 64; k < 128; k += 2)
-              e8[(k >> 1) & 7] = fmax3f(e8[(k >> 1) & 7], __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
+              for (int k = 64; k < 128; k += 2)
+                e8[(k >> 1) & 7] = fmax3f(e8[(k >> 1) & 7], __uint_as_float(sr[k]), __uint_as_float(sr[k + 1]));
+            }
+          } else {
+            if (lo_ok) {
+#pragma unroll
+              for (int k = 0; k < 64; ++k) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+            }
+            if (hi_ok) {
+#pragma unroll
+              for (int k = 64; k < 128; ++k) e8[k & 7] = fmaxf(e8[k & 7], __uint_as_float(sr[k]));
+            }
           }
         } else {
 #pragma unroll
