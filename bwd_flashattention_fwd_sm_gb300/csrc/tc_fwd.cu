@@ -14,7 +14,10 @@
 // memory, so P never leaves the SM: zwxr.cn article, section 5.4).  The
 // tensor core alternates between the two tiles: while warpgroup 0 turns S0
 // into P0, the tensor core runs P1 V and the next Q1 K^T, and the other way
-// round, so matrix work overlaps the exponentials.
+// round, so matrix work overlaps the exponentials.  At head dim 64 the O
+// accumulators take half the columns and P_q gets its own (O0 [256,320) O1
+// [320,384) P0 [384,448) P1 [448,512)): the next S_q is then issued as soon as
+// the softmax has read S_q, and each softmax warpgroup runs tile after tile.
 //
 // Few units (fewer than the SMs): units of one 128-row query tile (kPair).
 // Both slots then hold that tile; the key tiles it sees go to the two slots in
@@ -113,6 +116,9 @@ struct Smem {
   uint64_t pair_full, pair_free;
   float pair_m[kTile], pair_l[kTile];
   int pair_have;
+  // head dim 64 (P in its own columns): s_free[q], the softmax has read S_q;
+  // pv_done[q], the P_q V product has finished
+  uint64_t s_free[2], pv_done[2];
 };
 
 static_assert(sizeof(Smem<FwdCfg<false>>) + 1024 <= 232448, "shared memory per CTA is at most 227 KiB");
@@ -360,6 +366,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
   Waiter<SM> W{sm, p};
   static_assert(!kFp8 || D == 128, "the FP8 forward has head dim 128");
   static_assert(!kPair || (!kSparse && !kFp8), "128-row units: dense and causal bf16 only");
+  // At head dim 64 the O accumulators take 128 columns, so P_q gets columns of
+  // its own ([384, 448) and [448, 512)) instead of S_q's: the next S_q can then
+  // be issued as soon as the softmax holds this S_q in registers, and each
+  // softmax warpgroup runs tile after tile without waiting for its own P V and
+  // S products.
+  constexpr bool kSepP = D == 64 && !kFp8;
   constexpr uint32_t kLoadBytes = kFp8 ? (uint32_t)kTile * 128 : tile_bytes<D>();
 
   if (threadIdx.x == 0) {
@@ -388,6 +400,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     if constexpr (kPair) {
       ptx::mbar_init(&sm.pair_full, 4);  // the second warpgroup's warps
       ptx::mbar_init(&sm.pair_free, 4);  // the first warpgroup's warps
+    }
+    if constexpr (kSepP) {
+      for (int i = 0; i < 2; ++i) {
+        ptx::mbar_init(&sm.s_free[i], 4);  // the softmax warpgroup's warps
+        ptx::mbar_init(&sm.pv_done[i], 1);
+      }
     }
     sm.abort.flag = 0;
     ptx::fence_mbar_init();
@@ -542,7 +560,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     constexpr uint32_t idesc_pv = kFp8 ? ptx::idesc_e4m3(128, D) : ptx::idesc_bf16(128, D, false, true);
     const uint32_t q_addr = ptx::smem_u32(sm.q[q]);
     const uint32_t t_s = tmem + q * 128, t_o = tmem + 256 + q * D;
+    const uint32_t t_p = kSepP ? tmem + 384 + q * 64 : t_s;  // P_q, the A operand of P_q V
     uint32_t n_units_seen = 0, n_q = 0, n_p = 0, n_o = 0, n_k = 0, n_v = 0;
+    uint32_t n_si = 0;  // S_q products issued (all units)
     uint32_t n_turn = 0;  // key tiles walked so far (all units)
     bool ok = true;
     for (;;) {
@@ -568,6 +588,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
       int s_issued = 0, pv_issued = 0;
       // S_q = Q_q K^T into S_q; after the unit's last one, Q_q may be refilled.
       auto issue_s = [&](uint32_t k_addr) -> bool {
+        if constexpr (kSepP) {  // the softmax has read the previous S_q
+          if (n_si > 0 && !W.warp(&sm.s_free[q], (n_si - 1) & 1)) return false;
+          ++n_si;
+        }
         if (s_issued == 0) {
           if (!W.warp(&sm.q_full[q], n_q & 1)) return false;
           ++n_q;
@@ -596,6 +620,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         return true;
       };
 
+      // O_q += P_q V (V from stage vst_); the unit's last one frees O_q for the epilogue.
+      auto issue_pv = [&](uint32_t vst_) {
+        ptx::tc_fence_after();
+        const uint32_t v_addr = ptx::smem_u32(sm.v[vst_]);
+        const uint32_t acc0 = pv_issued > 0 ? 1u : 0u;
+        const bool last = ++pv_issued == n_act;
+        if (ptx::elect_one()) {
+          if constexpr (kFp8) {
+            // B = V^T as (N = head dim, K = keys), keys contiguous: K-major;
+            // A = P, 32 keys per 8 tensor-memory columns
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::mma_ts_f8(t_o, t_p + kk * 8, ptx::sdesc_sw128(v_addr + kk * 32, 16, 1024), idesc_pv,
+                             kk > 0 ? 1u : acc0);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              // B = V as (N = head dim, K = keys), head dim contiguous: MN-major.
+              const uint64_t bdesc = ptx::sdesc_sw128(v_addr + kk * 2048, kHalfTileBytes, 1024);
+              ptx::mma_ts(t_o, t_p + kk * 8, bdesc, idesc_pv, kk > 0 ? 1u : acc0);
+            }
+          }
+          if constexpr (kSepP) ptx::mma_commit(&sm.pv_done[q]);
+          if (last) ptx::mma_commit(&sm.o_final[q]);
+        }
+        __syncwarp();
+        if (last) ++n_o;
+      };
+
       PartList<kSparse, kPair> t = tl;
       int kt, bits;
       bool have = t.next(kt, bits);
@@ -616,6 +669,36 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         int nkt, nbits = 0;
         const bool nhave = t.next(nkt, nbits);
         const uint32_t nst = n_k % kKStages, vst = n_v % kVStages;
+        if constexpr (kSepP) {
+          // S_q of the next tile first: issue_s waits only until the softmax has
+          // read this tile's S_q; then this tile's P_q V once P_q is written.
+          // The issuers do not take turns: each softmax warpgroup runs on as
+          // soon as its next S_q is there.
+          if (nhave) {
+            if (!W.warp(&sm.k_full[nst], (n_k / kKStages) & 1)) { ok = false; break; }
+            ++n_k;
+            if ((nbits >> (4 * q)) & 0xF) {
+              ptx::tc_fence_after();
+              if (!issue_s(ptx::smem_u32(sm.k[nst]))) { ok = false; break; }
+            }
+            if (ptx::elect_one()) ptx::mma_commit(&sm.k_empty[nst]);  // this warp's S product issued
+            __syncwarp();
+          }
+          if (!W.warp(&sm.v_full[vst], (n_v / kVStages) & 1)) { ok = false; break; }
+          ++n_v;
+          if ((cur_bits >> (4 * q)) & 0xF) {
+            if (!W.warp(&sm.p_full[q], n_p & 1)) { ok = false; break; }
+            ++n_p;
+            if (pv_issued == 0 && !W.warp(&sm.o_free[q], (n_o & 1) ^ 1)) { ok = false; break; }
+            issue_pv(vst);
+          }
+          if (ptx::elect_one()) ptx::mma_commit(&sm.v_empty[vst]);  // this warp's P V product issued
+          __syncwarp();
+          have = nhave;
+          cur_bits = nbits;
+          cur_stage = nst;
+          continue;
+        }
         if (!W.warp(&sm.v_full[vst], (n_v / kVStages) & 1)) { ok = false; break; }
         ++n_v;
         // K of the next tile is waited for before P_q: it is normally there long
@@ -637,32 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
           ok = false;
           break;
         }
-        if ((cur_bits >> (4 * q)) & 0xF) {
-          ptx::tc_fence_after();
-          const uint32_t v_addr = ptx::smem_u32(sm.v[vst]);
-          const uint32_t acc0 = pv_issued > 0 ? 1u : 0u;
-          const bool last = ++pv_issued == n_act;
-          if (ptx::elect_one()) {
-            if constexpr (kFp8) {
-              // B = V^T as (N = head dim, K = keys), keys contiguous: K-major;
-              // A = P, 32 keys per 8 tensor-memory columns
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                ptx::mma_ts_f8(t_o, t_s + kk * 8, ptx::sdesc_sw128(v_addr + kk * 32, 16, 1024), idesc_pv,
-                               kk > 0 ? 1u : acc0);
-            } else {
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                // B = V as (N = head dim, K = keys), head dim contiguous: MN-major.
-                const uint64_t bdesc = ptx::sdesc_sw128(v_addr + kk * 2048, kHalfTileBytes, 1024);
-                ptx::mma_ts(t_o, t_s + kk * 8, bdesc, idesc_pv, kk > 0 ? 1u : acc0);
-              }
-            }
-            if (last) ptx::mma_commit(&sm.o_final[q]);
-          }
-          __syncwarp();
-          if (last) ++n_o;
-        }
+        if ((cur_bits >> (4 * q)) & 0xF) issue_pv(vst);
         // S_q of the next tile: the S_q buffer held P_q, consumed by the product above
         if (nhave && ((nbits >> (4 * q)) & 0xF)) {
           ptx::tc_fence_after();
@@ -696,10 +754,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
     const int r = wq * 32 + lane;     // row in the query tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const uint32_t col_s = q * 128, col_o = 256 + q * D;
+    const uint32_t col_p = kSepP ? 384 + q * 64 : col_s;  // where P_q is written
     const bool elem_causal = p.mask == kMaskCausal || (p.mask == kMaskBlock && p.causal_in_block);
     const float c = p.scale_log2;
     const int row_half = r >= 64 ? 2 : 0;
     uint32_t n_units_seen = 0, n_s = 0, n_o = 0, n_pair = 0;
+    uint32_t n_pw = 0;  // P_q tiles written (all units)
     bool ok = true;
     for (;;) {
       const int slot = n_units_seen & 1;
@@ -761,6 +821,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         for (int cc = 0; cc < 4; ++cc)
           ptx::tmem_ld32(tmem + lane_base + col_s + cc * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[cc * 32]));
         ptx::tmem_ld_wait();
+        if constexpr (kSepP) {  // S_q is in registers: the next S_q may overwrite it
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&sm.s_free[q]);
+        }
         // x = s * scale * log2(e) = s' * |c| with s' = s or -s by the sign of the
         // scale, so the row max of x is |c| times the max of s' (8 partials keep the
         // dependency chains short).  Masked keys are left out.
@@ -823,18 +888,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
           m_used = m_new;
         }
         const float mu = m_used == -INFINITY ? 0.f : m_used;
-        // P = exp2(s' |c| - m) as bf16 pairs, written over S_q 8 columns at a time
+        if constexpr (kSepP) {
+          // P_q's columns are free, and O_q stable, once the previous P_q V
+          // product has finished
+          if (n_pw > 0 && !W.warp(&sm.pv_done[q], (n_pw - 1) & 1)) { ok = false; break; }
+          ptx::tc_fence_after();
+        }
+        // P = exp2(s' |c| - m) as bf16 pairs, written 8 columns at a time over
+        // S_q (at head dim 64 into P_q's own columns)
         float rs;
         if constexpr (kFp8)
           rs = (need_mask ? write_p8<true, kSparse>(sr, ca, mu - lr, thr, lo_ok, hi_ok, tmem + lane_base + col_s)
                           : write_p8<false, kSparse>(sr, ca, mu - lr, thr, lo_ok, hi_ok, tmem + lane_base + col_s)) *
                inv_r;
         else
-          rs = need_mask ? write_p<true, kSparse>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s)
-                         : write_p<false, kSparse>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_s);
-        // S_q of this tile was issued after the previous P_q V product and its
-        // completion covers that product, so O_q is stable here; the next product
-        // waits for p_full, so rescaling O_q now (after P is written) is in time.
+          rs = need_mask ? write_p<true, kSparse>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_p)
+                         : write_p<false, kSparse>(sr, ca, mu, thr, lo_ok, hi_ok, tmem + lane_base + col_p);
+        // O_q is stable here: S_q of this tile was issued after the previous P_q V
+        // product, whose completion its completion covers (at head dim 64 the
+        // wait above covers it); the next product waits for p_full, so rescaling
+        // O_q now (after P is written) is in time.
         if (n_done > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
@@ -852,6 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_fwd(const __grid_constant__ 
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&sm.p_full[q]);
         ++n_done;
+        ++n_pw;
       }
       if (!ok) break;
       if (q0 >= si.len) continue;  // this query tile lies past the sequence end
