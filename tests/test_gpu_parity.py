@@ -164,9 +164,10 @@ def test_c5_varlen_sampled_sequences():
     check_all(wl, sub, ref)
 
 
-@pytest.mark.parametrize("name", ["h0_dense_s8192", "h0_causal_s8192", "h2_causal_s8192_d64"])
+@pytest.mark.parametrize("name", ["h0_dense_s8192", "h0_causal_s8192", "h2_dense_s8192_d64", "h2_causal_s8192_d64"])
 def test_h0_s8192_sampled_head(name):
-    """The S=8192, D=128 headline shape (B=2, H=16): full run, one seeded head checked."""
+    """The S=8192 shapes (B=2, H=16; head dim 128, and 64 with P in tensor-memory
+    columns of its own): full run, one seeded head checked."""
     wl = W.WORKLOADS[name]
     inp = W.make_inputs(wl)
     got = gpu_run(wl, inp)
