@@ -177,9 +177,11 @@ def run_ours(args, wl, rank, world, dist):
     ws_f = torch.empty(max(1, lib.attn_fwd_workspace_size(ctypes.byref(p))), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(max(1, lib.attn_bwd_workspace_size(ctypes.byref(p))), dtype=torch.uint8, device=dev)
 
+    det = bool(getattr(args, "deterministic", False))  # attn_bwd_deterministic
+
     def step():
         o, lse = attn_fwd(q, k, v, workspace=ws_f, **kw)
-        dq, dk, dv = attn_bwd(q, k, v, o, do, lse, workspace=ws_b, **kw)
+        dq, dk, dv = attn_bwd(q, k, v, o, do, lse, workspace=ws_b, deterministic=det, **kw)
         return o, lse, dq, dk, dv
 
     for _ in range(args.warmup):
@@ -262,7 +264,8 @@ def run_ours(args, wl, rank, world, dist):
             stream.wait_event(ready)
             d = dev_in[slot]
             o_, lse_ = attn_fwd(d["q"], d["k"], d["v"], workspace=ws_f, **kw)
-            dq_, dk_, dv_ = attn_bwd(d["q"], d["k"], d["v"], o_, d["do"], lse_, workspace=ws_b, **kw)
+            dq_, dk_, dv_ = attn_bwd(d["q"], d["k"], d["v"], o_, d["do"], lse_, workspace=ws_b, deterministic=det,
+                                     **kw)
             outs = (o_, lse_, dq_, dk_, dv_)
             done = torch.cuda.Event()
             done.record(stream)
@@ -308,18 +311,24 @@ def run_ours(args, wl, rank, world, dist):
         try:
             with open(prof) as f:
                 t = json.load(f)
-            if t.get("workload") == wl.name and t.get("kernel_build") == kernel_build_id():
+            if not det and t.get("workload") == wl.name and t.get("kernel_build") == kernel_build_id():
                 traffic = t.get("bwd_main_bytes")
         except Exception:
             traffic = None
-    launches_per_step = 2 + 4 + (1 if wl.mask == "block" else 0)
+    # forward: work list, main kernel; backward: work list, preprocess, main
+    # kernel, dQ conversion (deterministic: a second work list and the dQ pass
+    # instead of the conversion); block-sparse: the mask transpose
+    launches_per_step = 2 + (5 if det else 4) + (1 if wl.mask == "block" else 0)
     # the backward's two HBM-bound kernels, against the HBM copy bandwidth
     hbm = peak_value(peaks, "hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"]
     rows = (int(inp["cu_seqlens"][-1]) if wl.varlen else wl.batch * wl.seqlen) * wl.heads_q
     esz = 2 if wl.dtype == "bf16" else 4
     aux = {}
-    for name, times, per_row in (("bwd_preprocess", pre_ms, 2 * wl.head_dim * esz + 4 + 4 * wl.head_dim),
-                                 ("dq_convert", cvt_ms, 4 * wl.head_dim + wl.head_dim * esz)):
+    # (the deterministic backward has no float32 accumulator: no zero fill, no conversion)
+    legs = [("bwd_preprocess", pre_ms, 2 * wl.head_dim * esz + 4 + (0 if det else 4 * wl.head_dim))]
+    if not det:
+        legs.append(("dq_convert", cvt_ms, 4 * wl.head_dim + wl.head_dim * esz))
+    for name, times, per_row in legs:
         t = sum(times) / len(times)
         gbs = rows * per_row / (t * 1e-3) / 1e9
         aux[name] = {"ms": round(t, 4), "bytes": rows * per_row, "gbs": round(gbs, 1),
@@ -339,7 +348,7 @@ def run_ours(args, wl, rank, world, dist):
         "dtype": "bf16" if wl.dtype == "bf16" else "f32",
         "data": "synthetic: Q,K,V,dO iid N(0,1) from a fixed seed, rounded to bf16",
         "config": {
-            "workload": wl.name,
+            "workload": wl.name + ("_deterministic" if det else ""),
             "batch": wl.batch, "heads_q": wl.heads_q, "heads_kv": wl.heads_kv, "seq_len": wl.seqlen,
             "head_dim": wl.head_dim, "mask": wl.mask, "varlen": wl.varlen,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -350,7 +359,8 @@ def run_ours(args, wl, rank, world, dist):
         "fwd_tflops": round(fwd_ach, 2), "bwd_tflops": round(achieved, 2),
         "fwd_frac_of_peak": round(fwd_ach / peak, 4), "bwd_frac_of_peak": round(achieved / peak, 4),
         "roofline": {
-            "kernel": "backward main (dK/dV-stationary, dQ accumulation)",
+            "kernel": ("backward main without dQ + query-stationary dQ pass (attn_bwd_deterministic)" if det else
+                       "backward main (dK/dV-stationary, dQ accumulation)"),
             "bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
             "peak_source": f"{peak_src} bf16 dense" + (" (MEASURED_PEAKS.json)" if peak_src == "measured" else
@@ -790,6 +800,8 @@ def main():
                     help="measure the FP8 (e4m3) forward (quantisation + forward) on --workload")
     ap.add_argument("--d256", action="store_true",
                     help="measure head dim 256: forward and backward at B=2, H=16, S=8192")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="run the backward as attn_bwd_deterministic (fixed dQ summation order)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
