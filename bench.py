@@ -145,6 +145,71 @@ def gpu_identity(torch):
         return os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or None
 
 
+# Steps in each timed window of an end-to-end leg.  The first step's upload and
+# the last step's download overlap no computation; over 30 steps they are a
+# small share, as in a stream of steps.
+E2E_STEPS = 30
+
+
+def pipelined_e2e(torch, dev, host_in, compute, n_steps, warmup, dist=None):
+    """End to end through the public API with host buffers: every step copies its
+    inputs (the pinned tensors of `host_in`) to the device, runs `compute` on
+    them, which returns the step's output tensors, and copies every output back
+    to pinned host memory.  The copies run on their own streams,
+    double-buffered: step i's inputs travel while step i-1 computes and step
+    i-1's results while step i computes.  Every copy of every step is inside
+    the timed region.  Three timed windows of n_steps, after `warmup` (at most
+    2) untimed steps; returns (median seconds, the windows' seconds, bytes
+    copied back per step).  Each window is the slowest rank's."""
+    names = list(host_in)
+    stream = torch.cuda.current_stream()
+    dev_in = [{n: torch.empty_like(host_in[n], device=dev) for n in names} for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    host_out = [None, None]
+    keep = []  # device outputs stay referenced until their copies are done
+
+    def run(k):
+        comp_done = [None, None]
+        for i in range(k):
+            slot = i & 1
+            with torch.cuda.stream(s_in):
+                if comp_done[slot] is not None:
+                    s_in.wait_event(comp_done[slot])  # step i-2 no longer reads this slot
+                for n in names:
+                    dev_in[slot][n].copy_(host_in[n], non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(s_in)
+            stream.wait_event(ready)
+            outs = compute(dev_in[slot])
+            done = torch.cuda.Event()
+            done.record(stream)
+            comp_done[slot] = done
+            if host_out[slot] is None:
+                host_out[slot] = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done)
+                for h, t in zip(host_out[slot], outs):
+                    h.copy_(t, non_blocking=True)
+            keep.append(outs)
+
+    run(max(1, min(warmup, 2)))
+    torch.cuda.synchronize()
+    keep.clear()
+    # three windows, the median reported: the host copies share the node's host
+    # memory and links with other jobs, and one window can catch a transient
+    windows = []
+    for _ in range(3):
+        if dist is not None:
+            dist.barrier()
+        t0 = time.perf_counter()
+        run(n_steps)
+        torch.cuda.synchronize()
+        windows.append(max_over_ranks(time.perf_counter() - t0, dist, dev))
+        keep.clear()
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    return statistics.median(windows), windows, d2h
+
+
 def run_ours(args, wl, rank, world, dist):
     import ctypes
 
@@ -245,58 +310,15 @@ def run_ours(args, wl, rank, world, dist):
     names_in = ("q", "k", "v", "do")
     host_in = {n: inp[n].pin_memory() for n in names_in}
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    dev_in = [{n: torch.empty_like(inp[n], device=dev) for n in names_in} for _ in range(2)]
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    host_out = [None, None]
-    keep = []  # device outputs stay referenced until their copies are done
 
-    def e2e_run(n_steps):
-        comp_done = [None, None]
-        for i in range(n_steps):
-            slot = i & 1
-            with torch.cuda.stream(s_in):
-                if comp_done[slot] is not None:
-                    s_in.wait_event(comp_done[slot])  # step i-2 no longer reads this slot
-                for n in names_in:
-                    dev_in[slot][n].copy_(host_in[n], non_blocking=True)
-                ready = torch.cuda.Event()
-                ready.record(s_in)
-            stream.wait_event(ready)
-            d = dev_in[slot]
-            o_, lse_ = attn_fwd(d["q"], d["k"], d["v"], workspace=ws_f, **kw)
-            dq_, dk_, dv_ = attn_bwd(d["q"], d["k"], d["v"], o_, d["do"], lse_, workspace=ws_b, deterministic=det,
-                                     **kw)
-            outs = (o_, lse_, dq_, dk_, dv_)
-            done = torch.cuda.Event()
-            done.record(stream)
-            comp_done[slot] = done
-            if host_out[slot] is None:
-                host_out[slot] = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(done)
-                for h, t in zip(host_out[slot], outs):
-                    h.copy_(t, non_blocking=True)
-            keep.append(outs)
+    def compute(d):
+        o_, lse_ = attn_fwd(d["q"], d["k"], d["v"], workspace=ws_f, **kw)
+        dq_, dk_, dv_ = attn_bwd(d["q"], d["k"], d["v"], o_, d["do"], lse_, workspace=ws_b, deterministic=det, **kw)
+        return o_, lse_, dq_, dk_, dv_
 
-    e2e_run(max(1, min(args.warmup, 2)))
-    torch.cuda.synchronize()
-    keep.clear()
-    e2e_steps = max(1, min(args.steps, 10))
-    # three timed windows, the median reported: the host copies share the
-    # node's host memory and links with other jobs, and one window can catch
-    # a transient
-    windows = []
-    for _ in range(3):
-        if dist is not None:
-            dist.barrier()
-        t0 = time.perf_counter()
-        e2e_run(e2e_steps)
-        torch.cuda.synchronize()
-        windows.append(max_over_ranks(time.perf_counter() - t0, dist, dev))
-        keep.clear()
-    e2e_s = statistics.median(windows)
+    e2e_steps = E2E_STEPS
+    e2e_s, windows, d2h = pipelined_e2e(torch, dev, host_in, compute, e2e_steps, args.warmup, dist)
     keep_gpu_samples(wl, step())
-    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
     e2e_value = whole_job_rate(step_flops, world, e2e_steps, e2e_s) / 1e12
 
     peaks, peak_src = load_peaks()
@@ -594,18 +616,11 @@ def run_ln(args):
     bytes_per_call = 8.0 * LN_ROWS * LN_COLS
     gbs = bytes_per_call * args.steps / (sum(ms) * 1e-3) / 1e9
     # end to end: host tensors in pinned memory, copied in and out every call
-    xh, rh = x.cpu().pin_memory(), r.cpu().pin_memory()
-    yh, hh = torch.empty_like(xh).pin_memory(), torch.empty_like(xh).pin_memory()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(1, min(args.steps, 10))
-    e0.record()
-    for _ in range(e2e_steps):
-        y, h = layernorm_residual(xh.to(dev, non_blocking=True), rh.to(dev, non_blocking=True), gm, bt)
-        yh.copy_(y, non_blocking=True)
-        hh.copy_(h, non_blocking=True)
-    e1.record()
-    torch.cuda.synchronize()
-    e2e = bytes_per_call * e2e_steps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    host_in = {"x": x.cpu().pin_memory(), "r": r.cpu().pin_memory()}
+    e2e_steps = E2E_STEPS
+    e2e_s, _, _ = pipelined_e2e(torch, dev, host_in, lambda d: layernorm_residual(d["x"], d["r"], gm, bt), e2e_steps,
+                                args.warmup)
+    e2e = bytes_per_call * e2e_steps / e2e_s / 1e9
     peaks, src = load_peaks()
     peak = peak_value(peaks, "hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"]
     line = {
@@ -710,23 +725,16 @@ def run_fp8(args, wl):
     quant_bytes = 3 * elems  # 2 bytes read and 1 written per element
 
     # end to end: bf16 inputs from pinned host memory, O and LSE back, every step
-    host_in = [t.cpu().pin_memory() for t in (q, k, v)]
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    ho, hl = torch.empty(o.shape, dtype=o.dtype, pin_memory=True), torch.empty(lse.shape, dtype=lse.dtype,
-                                                                                pin_memory=True)
-    e2e_steps = max(1, min(args.steps, 10))
-    e0, e1 = ev(), ev()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        dq_, dk_, dv_ = (h.to(dev, non_blocking=True) for h in host_in)
-        quantize_fp8(dq_, dk_, dv_, out=f)
-        o2, l2 = attn_fwd_fp8(f, workspace=ws, **kw)
-        ho.copy_(o2, non_blocking=True)
-        hl.copy_(l2, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e = fwd_flops * e2e_steps / (e0.elapsed_time(e1) * 1e-3) / 1e12
-    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    host_in = {"q": q.cpu().pin_memory(), "k": k.cpu().pin_memory(), "v": v.cpu().pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+
+    def compute(d):  # the quantised operands f are rewritten in stream order each step
+        quantize_fp8(d["q"], d["k"], d["v"], out=f)
+        return attn_fwd_fp8(f, workspace=ws, **kw)
+
+    e2e_steps = E2E_STEPS
+    e2e_s, _, d2h = pipelined_e2e(torch, dev, host_in, compute, e2e_steps, args.warmup)
+    e2e = fwd_flops * e2e_steps / e2e_s / 1e12
 
     peaks, src = load_peaks()
     bf16_peak = peak_value(peaks, "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
