@@ -2,9 +2,10 @@
 // one pass over HBM per row, statistics merged in registers.
 //
 // A CTA of 256 threads normalises one row at a time (grid-stride over rows).
-// Rows that are whole 16-byte vectors at aligned addresses stream through a
-// ring of shared-memory stages filled by bulk copies, several rows ahead;
-// other rows are loaded straight into registers.  Each thread holds its
+// Long rows (more than two 16-byte vectors per thread) that are whole vectors
+// at aligned addresses stream through a ring of shared-memory stages filled by
+// bulk copies, several rows ahead; other rows are loaded straight into
+// registers, every load of the row issued before any is used.  Each thread holds its
 // 16-byte vectors of the row in registers (8 bf16 or 4 float32 elements each),
 // adds the residual, and summarises every vector
 // as (count, mean, M2) computed from its registers.  Summaries are merged with
@@ -14,9 +15,11 @@
 // through shared memory (the reduction scheme of the tutorial's section 5.2).
 // The row is then normalised from the registers it is already in, so x and
 // the residual are read once and y (and h) written once: the bytes moved set
-// the time (section 5.1 on arithmetic intensity below 1).  rstd uses the IEEE
-// square root and division, not the approximate reciprocal square root the
-// tutorial warns against for LayerNorm (section 4).
+// the time (section 5.1 on arithmetic intensity below 1).  When every thread
+// holds the same number of whole vectors, all merges join equal counts and run
+// without the division.  rstd uses the IEEE square root and division, once per
+// row, not the approximate reciprocal square root the tutorial warns against
+// for LayerNorm (section 4).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -55,13 +58,77 @@ __device__ __forceinline__ Stats merge(Stats a, Stats b) {
   return r;
 }
 
+// merge() for two summaries of equal counts, where n_b / n is exactly 1/2: the
+// same update without the division.  Rows that every thread covers with the
+// same number of whole vectors merge only equal counts (in a tree within the
+// thread, then across lanes and warps), and the divisions' latency was a
+// fifth of the row's time on [16384, 4096] bf16.
+__device__ __forceinline__ Stats merge_eq(Stats a, Stats b) {
+  const float d = b.mean - a.mean;
+  Stats r;
+  r.n = a.n + b.n;
+  r.mean = a.mean + d * 0.5f;
+  r.m2 = a.m2 + b.m2 + d * d * a.n * 0.5f;
+  return r;
+}
+
+// The (count, mean, M2) summary of one whole vector of E values.
+template <int E>
+__device__ __forceinline__ Stats vec_stats(const float (&v)[E]) {
+  float sum = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) sum += v[e];
+  const float m = sum * (1.f / E);
+  float q = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) q += (v[e] - m) * (v[e] - m);
+  return Stats{(float)E, m, q};
+}
+
+// Summaries of all threads merged into warp_stats (lane 0 of each warp), then
+// by warp 0 into row_stats and the row's rstd; `eq`: every summary has the
+// same count.  Leaves row_stats / row_rstd valid after its second barrier.
+__device__ __forceinline__ void block_stats(Stats st, bool eq, int lane, int warp, float cols, float eps,
+                                            Stats* warp_stats, Stats& row_stats, float& row_rstd, float* mean_out,
+                                            float* rstd_out) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    Stats o;
+    o.n = __shfl_xor_sync(0xffffffffu, st.n, off);
+    o.mean = __shfl_xor_sync(0xffffffffu, st.mean, off);
+    o.m2 = __shfl_xor_sync(0xffffffffu, st.m2, off);
+    st = eq ? merge_eq(st, o) : merge(st, o);
+  }
+  if (lane == 0) warp_stats[warp] = st;
+  __syncthreads();
+  if (warp == 0) {
+    // lanes 8.. hold empty summaries; the xor offsets below 8 keep them apart
+    Stats w = lane < kThreadsLn / 32 ? warp_stats[lane] : Stats{0.f, 0.f, 0.f};
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) {
+      Stats o;
+      o.n = __shfl_xor_sync(0xffffffffu, w.n, off);
+      o.mean = __shfl_xor_sync(0xffffffffu, w.mean, off);
+      o.m2 = __shfl_xor_sync(0xffffffffu, w.m2, off);
+      w = eq ? merge_eq(w, o) : merge(w, o);
+    }
+    if (lane == 0) {
+      row_stats = w;
+      row_rstd = 1.f / sqrtf(w.m2 / cols + eps);
+      if (mean_out) *mean_out = w.mean;
+      if (rstd_out) *rstd_out = row_rstd;
+    }
+  }
+  __syncthreads();
+}
+
 template <class T>
 struct Vec;  // one 16-byte vector of T
 template <>
 struct Vec<__nv_bfloat16> {
   static constexpr int E = 8;
-  __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
+  __device__ static void load(const __nv_bfloat16* p, float (&v)[8]) { unpack(*reinterpret_cast<const uint4*>(p), v); }
+  __device__ static void unpack(const uint4& u, float (&v)[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -84,9 +151,9 @@ struct Vec<__nv_bfloat16> {
 template <>
 struct Vec<float> {
   static constexpr int E = 4;
-  __device__ static void load(const float* p, float (&v)[4]) {
-    const float4 f = *reinterpret_cast<const float4*>(p);
-    v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+  __device__ static void load(const float* p, float (&v)[4]) { unpack(*reinterpret_cast<const uint4*>(p), v); }
+  __device__ static void unpack(const uint4& u, float (&v)[4]) {
+    v[0] = __uint_as_float(u.x); v[1] = __uint_as_float(u.y); v[2] = __uint_as_float(u.z); v[3] = __uint_as_float(u.w);
   }
   __device__ static void store(float* p, const float (&v)[4]) {
     *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
@@ -138,10 +205,13 @@ __global__ void __launch_bounds__(kThreadsLn, kVpt >= 8 ? 1 : (kVpt >= 4 ? 2 : 4
   constexpr int E = Vec<T>::E;
   __shared__ Stats warp_stats[kThreadsLn / 32];
   __shared__ Stats row_stats;
+  __shared__ float row_rstd;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t cols = a.p.cols;
   const int64_t nvec = (cols + E - 1) / E;
   const bool ragged = cols % E != 0 || !a.vec;  // element loads where vectors do not fit
+  // every thread holds kVpt whole vectors: summaries of equal counts throughout
+  const bool uniform = !ragged && nvec == (int64_t)kThreadsLn * kVpt;
   const T* X = static_cast<const T*>(a.x);
   const T* R = static_cast<const T*>(a.r);
   T* Y = static_cast<T*>(a.y);
@@ -151,21 +221,40 @@ __global__ void __launch_bounds__(kThreadsLn, kVpt >= 8 ? 1 : (kVpt >= 4 ? 2 : 4
     const T* rr = R ? R + row * a.p.r_stride : nullptr;
     float v[kVpt][E];
     Stats st{0.f, 0.f, 0.f};
+    Stats sv[kVpt];
+    // whole vectors: every load of the row issued first, as raw 16-byte words
+    // (widened only afterwards, so they are all in flight at once)
+    uint4 ux[kVpt], ur[kVpt];
+#pragma unroll
+    for (int j = 0; j < kVpt; ++j) {
+      const int64_t vi = tid + (int64_t)j * kThreadsLn;
+      const int64_t c0 = vi * E;
+      ux[j] = ur[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (vi < nvec && (!ragged || (a.vec && c0 + E <= cols))) {
+        ux[j] = *reinterpret_cast<const uint4*>(xr + c0);
+        if (rr) ur[j] = *reinterpret_cast<const uint4*>(rr + c0);
+      }
+    }
 #pragma unroll
     for (int j = 0; j < kVpt; ++j) {
       const int64_t vi = tid + (int64_t)j * kThreadsLn;
       const int64_t c0 = vi * E;
       int cnt = 0;
+      sv[j] = Stats{0.f, 0.f, 0.f};
       if (vi < nvec) {
         if (!ragged || (a.vec && c0 + E <= cols)) {
-          Vec<T>::load(xr + c0, v[j]);
+          Vec<T>::unpack(ux[j], v[j]);
           if (rr) {
             float t[E];
-            Vec<T>::load(rr + c0, t);
+            Vec<T>::unpack(ur[j], t);
 #pragma unroll
             for (int e = 0; e < E; ++e) v[j][e] += t[e];
           }
           cnt = E;
+          if (uniform) {
+            sv[j] = vec_stats<E>(v[j]);
+            continue;
+          }
         } else {  // the row's last, partial vector
 #pragma unroll
           for (int e = 0; e < E; ++e) {
@@ -191,38 +280,18 @@ __global__ void __launch_bounds__(kThreadsLn, kVpt >= 8 ? 1 : (kVpt >= 4 ? 2 : 4
         st = merge(st, Stats{(float)cnt, m, q});
       }
     }
+    if (uniform) {  // the thread's vectors in a tree of equal counts
+#pragma unroll
+      for (int w = 1; w < kVpt; w <<= 1)
+#pragma unroll
+        for (int j = 0; j + w < kVpt; j += 2 * w) sv[j] = merge_eq(sv[j], sv[j + w]);
+      st = sv[0];
+    }
     // warp, then block
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      Stats o;
-      o.n = __shfl_xor_sync(0xffffffffu, st.n, off);
-      o.mean = __shfl_xor_sync(0xffffffffu, st.mean, off);
-      o.m2 = __shfl_xor_sync(0xffffffffu, st.m2, off);
-      st = merge(st, o);
-    }
-    if (lane == 0) warp_stats[warp] = st;
-    __syncthreads();
-    if (warp == 0) {
-      Stats w = lane < kThreadsLn / 32 ? warp_stats[lane] : Stats{0.f, 0.f, 0.f};
-#pragma unroll
-      for (int off = 4; off > 0; off >>= 1) {
-        Stats o;
-        o.n = __shfl_xor_sync(0xffffffffu, w.n, off);
-        o.mean = __shfl_xor_sync(0xffffffffu, w.mean, off);
-        o.m2 = __shfl_xor_sync(0xffffffffu, w.m2, off);
-        w = merge(w, o);
-      }
-      if (lane == 0) {
-        row_stats = w;
-        const float var = w.m2 / (float)cols;
-        const float rs = 1.f / sqrtf(var + a.p.eps);
-        if (a.mean) a.mean[row] = w.mean;
-        if (a.rstd) a.rstd[row] = rs;
-      }
-    }
-    __syncthreads();
+    block_stats(st, uniform, lane, warp, (float)cols, a.p.eps, warp_stats, row_stats, row_rstd,
+                a.mean ? a.mean + row : nullptr, a.rstd ? a.rstd + row : nullptr);
     const float mu = row_stats.mean;
-    const float rs = 1.f / sqrtf(row_stats.m2 / (float)cols + a.p.eps);
+    const float rs = row_rstd;
     T* yr = Y + row * a.p.y_stride;
     T* hr = H ? H + row * a.p.h_stride : nullptr;
 #pragma unroll
@@ -284,9 +353,11 @@ __global__ void __launch_bounds__(kThreadsLn, ring_ctas<kVpt>()) k_ln_ring(const
   __shared__ uint64_t full[kMaxStages];
   __shared__ Stats warp_stats[kThreadsLn / 32];
   __shared__ Stats row_stats;
+  __shared__ float row_rstd;
   __shared__ ptx::Abort abort;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t cols = a.p.cols, nvec = cols / E;
+  const bool uniform = nvec == (int64_t)kThreadsLn * kVpt;  // equal summary counts throughout
   const bool has_r = a.r != nullptr;
   const uint32_t stage_bytes = row_bytes * (has_r ? 2 : 1);
   const char* X = static_cast<const char*>(a.x);
@@ -322,9 +393,11 @@ __global__ void __launch_bounds__(kThreadsLn, ring_ctas<kVpt>()) k_ln_ring(const
     const uint8_t* xsm = ring + (size_t)s * stage_bytes;
     float v[kVpt][E];
     Stats st{0.f, 0.f, 0.f};
+    Stats sv[kVpt];
 #pragma unroll
     for (int j = 0; j < kVpt; ++j) {
       const int64_t vi = tid + (int64_t)j * kThreadsLn;
+      sv[j] = Stats{0.f, 0.f, 0.f};
       if (vi < nvec) {
         Vec<T>::load(reinterpret_cast<const T*>(xsm) + vi * E, v[j]);
         if (has_r) {
@@ -333,15 +406,16 @@ __global__ void __launch_bounds__(kThreadsLn, ring_ctas<kVpt>()) k_ln_ring(const
 #pragma unroll
           for (int e = 0; e < E; ++e) v[j][e] += t[e];
         }
-        float sum = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) sum += v[j][e];
-        const float m = sum * (1.f / E);
-        float q = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) q += (v[j][e] - m) * (v[j][e] - m);
-        st = merge(st, Stats{(float)E, m, q});
+        sv[j] = vec_stats<E>(v[j]);
+        if (!uniform) st = merge(st, sv[j]);
       }
+    }
+    if (uniform) {  // the thread's vectors in a tree of equal counts
+#pragma unroll
+      for (int w = 1; w < kVpt; w <<= 1)
+#pragma unroll
+        for (int j = 0; j + w < kVpt; j += 2 * w) sv[j] = merge_eq(sv[j], sv[j + w]);
+      st = sv[0];
     }
     // every thread has read stage s (and agrees on the wait): refill the stage
     // with the row `stages` iterations ahead at once (refilling after the
@@ -351,36 +425,10 @@ __global__ void __launch_bounds__(kThreadsLn, ring_ctas<kVpt>()) k_ln_ring(const
       const int64_t next = row + (int64_t)stages * gridDim.x;
       if (next < a.p.rows) issue(s, next);
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      Stats o;
-      o.n = __shfl_xor_sync(0xffffffffu, st.n, off);
-      o.mean = __shfl_xor_sync(0xffffffffu, st.mean, off);
-      o.m2 = __shfl_xor_sync(0xffffffffu, st.m2, off);
-      st = merge(st, o);
-    }
-    if (lane == 0) warp_stats[warp] = st;
-    __syncthreads();
-    if (warp == 0) {
-      Stats w = lane < kThreadsLn / 32 ? warp_stats[lane] : Stats{0.f, 0.f, 0.f};
-#pragma unroll
-      for (int off = 4; off > 0; off >>= 1) {
-        Stats o;
-        o.n = __shfl_xor_sync(0xffffffffu, w.n, off);
-        o.mean = __shfl_xor_sync(0xffffffffu, w.mean, off);
-        o.m2 = __shfl_xor_sync(0xffffffffu, w.m2, off);
-        w = merge(w, o);
-      }
-      if (lane == 0) {
-        row_stats = w;
-        const float r_s = 1.f / sqrtf(w.m2 / (float)cols + a.p.eps);
-        if (a.mean) a.mean[row] = w.mean;
-        if (a.rstd) a.rstd[row] = r_s;
-      }
-    }
-    __syncthreads();
+    block_stats(st, uniform, lane, warp, (float)cols, a.p.eps, warp_stats, row_stats, row_rstd,
+                a.mean ? a.mean + row : nullptr, a.rstd ? a.rstd + row : nullptr);
     const float mu = row_stats.mean;
-    const float r_s = 1.f / sqrtf(row_stats.m2 / (float)cols + a.p.eps);
+    const float r_s = row_rstd;
     T* yr = Y + row * a.p.y_stride;
     T* hr = H ? H + row * a.p.h_stride : nullptr;
 #pragma unroll
@@ -420,7 +468,11 @@ cudaError_t launch_ln(const LnArgs& a, int sms, int* status, unsigned long long 
   // CTAs the kernel is built for
   const int ctas = per <= 2 ? ring_ctas<2>() : (per <= 4 ? ring_ctas<4>() : ring_ctas<8>());
   const int stages = (int)std::min<int64_t>(kMaxStages, (192 * 1024 / ctas) / stage_bytes);
-  if (a.vec && a.p.cols % E == 0 && stages >= 2 && per <= 8) {
+  // the ring for rows of more than two vectors per thread; shorter rows (4096
+  // bf16 or 2048 float32 columns and below) go through registers: on [16384,
+  // 4096] bf16 the register path with its loads issued first and division-free
+  // statistics measured 5.03-5.08 TB/s against 4.66-4.75 for the ring
+  if (a.vec && a.p.cols % E == 0 && stages >= 2 && per > 2 && per <= 8) {
     auto launch = [&](auto kernel) -> cudaError_t {
       const size_t smem = (size_t)stages * stage_bytes;
       cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
