@@ -22,10 +22,15 @@
 // first) and persistent CTAs that take units from an atomic counter; a unit's
 // two 128-row tiles are done one after the other.
 //
-// Warp roles (192 threads):
-//   warps 0-3  compute: thread r owns query row r (TMEM lane r)
-//   warp 4     TMA producer and unit fetcher
-//   warp 5     tensor-core issuer (whole warp; one elected lane issues)
+// Warp roles (320 threads):
+//   warps 0-7  compute: warps w and w + 4 share TMEM lane quarter w mod 4
+//              (query rows 32 (w mod 4) ..), warp w the keys [0, 64) of each
+//              tile and warp w + 4 the keys [64, 128): P and dS need no row-wide
+//              reduction (the forward's LSE fixes P), so the two halves of a
+//              row are independent and a tile's elementwise work is split
+//              over eight warps
+//   warp 8     TMA producer and unit fetcher
+//   warp 9     tensor-core issuer (whole warp; one elected lane issues)
 // Every wait is bounded; a CTA that gives up records ATTN_ERR_DEVICE_TIMEOUT,
 // drains its copies and tensor-core work, frees tensor memory and returns.
 #include <cuda.h>
@@ -39,7 +44,8 @@ namespace gbattn {
 namespace {
 
 constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kComputeWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 // S [0,128)  dP [128,256)  dS (bf16 pairs) [256,320)  dQ [384,512)
 constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDQ = 384;
@@ -113,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&sm.unit_full[i], 1);
-      ptx::mbar_init(&sm.unit_empty[i], 5);  // MMA warp + 4 compute warps
+      ptx::mbar_init(&sm.unit_empty[i], 1 + kComputeWarps);  // MMA warp + compute warps
     }
     ptx::mbar_init(&sm.qd_full, 1);
     ptx::mbar_init(&sm.qd_empty, 1);
@@ -124,16 +130,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
       ptx::mbar_init(&sm.v_empty[s], 1);
     }
     ptx::mbar_init(&sm.sdp_full, 1);
-    ptx::mbar_init(&sm.sdp_free, 4);
-    ptx::mbar_init(&sm.ds_full, 4);
+    ptx::mbar_init(&sm.sdp_free, kComputeWarps);
+    ptx::mbar_init(&sm.ds_full, kComputeWarps);
     ptx::mbar_init(&sm.ds_free, 1);
     ptx::mbar_init(&sm.dq_final, 1);
-    ptx::mbar_init(&sm.dq_free, 4);
+    ptx::mbar_init(&sm.dq_free, kComputeWarps);
     ptx::mbar_init(&sm.drain, 1);
     sm.abort.flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     ptx::tmem_alloc(&sm.tmem_base, kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -142,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
   ptx::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ================================================================ producer
     uint32_t n_units = 0, n_qd = 0, n_kv = 0;
     int last_qd_phase = -1, last_kv_phase[kStages] = {-1, -1};
@@ -215,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
           W.drain(&sm.v_full[s], (uint32_t)last_kv_phase[s]);
         }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ================================================================ MMA issuer
     // The whole warp runs the control flow; elect.sync on the full, converged
     // warp picks the same lane every time, so each commit covers every product
@@ -319,10 +325,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
     __syncwarp();
     if (lane == 0) W.drain(&sm.drain, 0);
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < kComputeWarps) {
     // ================================================================ compute
-    const int r = warp * 32 + lane;  // query row in the tile = TMEM lane
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int wq = warp & 3, hf = warp >> 2;  // TMEM lane quarter; key half of each tile
+    const int r = wq * 32 + lane;             // query row in the tile = TMEM lane
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     const bool elem_causal = p.mask == kMaskCausal || (p.mask == kMaskBlock && p.causal_in_block);
     const float c = p.scale_log2;
     const int row_half = r >= 64 ? 2 : 0;
@@ -346,10 +353,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
         const bool row_ok = qi < si.len && check_q_row(p, si, h, qi);
         const int n_act = count_active<kSparse>(p, si.len, q0u, q);
         __nv_bfloat16* drow = static_cast<__nv_bfloat16*>(p.dq) + (row_ok ? q_off(p, si, h, qi) : 0);
-        if (n_act == 0) {  // no visible key: dQ rows are zero
+        if (n_act == 0) {  // no visible key: dQ rows are zero (each warp its half of the columns)
           if (row_ok) {
 #pragma unroll
-            for (int w = 0; w < D / 8; ++w) *reinterpret_cast<uint4*>(drow + w * 8) = make_uint4(0u, 0u, 0u, 0u);
+            for (int w = 0; w < D / 16; ++w)
+              *reinterpret_cast<uint4*>(drow + hf * (D / 2) + w * 8) = make_uint4(0u, 0u, 0u, 0u);
           }
           continue;
         }
@@ -376,10 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
           int thr = si.len - k0;
           if (elem_causal) thr = min(thr, qi - k0 + 1);
           const bool lo_ok = (bits >> row_half) & 1, hi_ok = (bits >> (row_half + 1)) & 1;
-          // dS = P o (dP - D) as bf16 pairs, 64 keys (half a row) at a time
-          uint32_t pk[64];
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
+          // dS = P o (dP - D) as bf16 pairs over this warp's 64 keys of the row
+          const bool half_ok = hf == 0 ? lo_ok : hi_ok;
+          uint32_t pk[32];
+          {
             uint32_t sr[64], dr[64];
             ptx::tmem_ld32(tmem + lane_base + kColS + hf * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
             ptx::tmem_ld32(tmem + lane_base + kColS + hf * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
@@ -392,12 +400,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
               const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), c2, nl22);
               float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
               if (need_mask) {
-                if (!(k < thr && (k < 64 ? lo_ok : hi_ok))) pp.x = 0.f;
-                if (!(k + 1 < thr && (k + 1 < 64 ? lo_ok : hi_ok))) pp.y = 0.f;
+                if (!(k < thr && half_ok)) pp.x = 0.f;
+                if (!(k + 1 < thr && half_ok)) pp.y = 0.f;
               }
               const float2 t2 = __fadd2_rn(make_float2(__uint_as_float(dr[i]), __uint_as_float(dr[i + 1])), nd2);
               const float2 d2 = __fmul2_rn(pp, t2);
-              pk[hf * 32 + i / 2] = ptx::pack_bf16x2(d2.x, d2.y);
+              pk[i / 2] = ptx::pack_bf16x2(d2.x, d2.y);
             }
           }
           // S and dP of this tile are in registers: the next tile's may overwrite them
@@ -408,20 +416,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
           if (!W.warp(&sm.ds_free, (n_ds & 1) ^ 1)) { ok = false; break; }
           ++n_ds;
           ptx::tc_fence_after();
-          ptx::tmem_st32(tmem + lane_base + kColDS, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-          ptx::tmem_st32(tmem + lane_base + kColDS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+          ptx::tmem_st32(tmem + lane_base + kColDS + hf * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
           ptx::tmem_st_wait();
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(&sm.ds_full);
         }
         if (!ok) break;
-        // epilogue: dQ * scale straight from tensor memory to global memory
+        // epilogue: dQ * scale straight from tensor memory to global memory,
+        // each of the row's two warps half of its columns
         if (!W.warp(&sm.dq_final, n_tiles & 1)) { ok = false; break; }
         ++n_tiles;
         ptx::tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = hf * (D / 64); cc < (hf + 1) * (D / 64); ++cc) {
           uint32_t v[32];
           ptx::tmem_ld32(tmem + lane_base + kColDQ + cc * 32, v);
           ptx::tmem_ld_wait();
@@ -448,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }
