@@ -43,7 +43,10 @@ namespace gbattn {
 
 namespace {
 
-constexpr int kStages = 2;
+// K is held until the tile's dQ product has read it, V only until dP has: K's
+// ring is one stage deeper, so its next load starts a tile earlier (with two K
+// stages the issuer waited about 1250 clocks per tile for K to arrive).
+constexpr int kKStages = 3, kVStages = 2;
 constexpr int kThreads = 320;
 constexpr int kComputeWarps = 8;
 constexpr uint32_t kTmemCols = 512;
@@ -59,11 +62,11 @@ struct DqArgs {
 struct Smem {
   uint8_t q[kTileBytes];
   uint8_t dO[kTileBytes];
-  uint8_t k[kStages][kTileBytes];
-  uint8_t v[kStages][kTileBytes];
+  uint8_t k[kKStages][kTileBytes];
+  uint8_t v[kVStages][kTileBytes];
   uint64_t unit_full[2], unit_empty[2];
   uint64_t qd_full, qd_empty;
-  uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
+  uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
   uint64_t sdp_full, sdp_free, ds_full, ds_free, dq_final, dq_free, drain;
   int unit_slot[2][4];  // seq, head, 256-row tile, valid
   uint32_t tmem_base;
@@ -123,9 +126,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
     }
     ptx::mbar_init(&sm.qd_full, 1);
     ptx::mbar_init(&sm.qd_empty, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       ptx::mbar_init(&sm.k_full[s], 1);
       ptx::mbar_init(&sm.k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       ptx::mbar_init(&sm.v_full[s], 1);
       ptx::mbar_init(&sm.v_empty[s], 1);
     }
@@ -151,7 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
   if (warp == 8) {
     // ================================================================ producer
     uint32_t n_units = 0, n_qd = 0, n_kv = 0;
-    int last_qd_phase = -1, last_kv_phase[kStages] = {-1, -1};
+    int last_qd_phase = -1, last_k_phase[kKStages], last_v_phase[kVStages];
+    for (int s = 0; s < kKStages; ++s) last_k_phase[s] = -1;
+    for (int s = 0; s < kVStages; ++s) last_v_phase[s] = -1;
     bool ok = true;
     for (;;) {
       const int slot = n_units & 1;
@@ -194,19 +201,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
         int kt, bits;
         while (t.next(kt, bits)) {
           if (!((bits >> (4 * q)) & 0xF)) continue;
-          const int st = n_kv % kStages;
-          const uint32_t ph = (n_kv / kStages) & 1;
-          if (!W.warp(&sm.k_empty[st], ph ^ 1) || !W.warp(&sm.v_empty[st], ph ^ 1)) { ok = false; break; }
+          const int kst = n_kv % kKStages, vst = n_kv % kVStages;
+          const uint32_t kph = (n_kv / kKStages) & 1, vph = (n_kv / kVStages) & 1;
+          if (!W.warp(&sm.k_empty[kst], kph ^ 1) || !W.warp(&sm.v_empty[vst], vph ^ 1)) { ok = false; break; }
           if (lane == 0) {
             check_kv_row(p, si, g, kt * kTile);
-            ptx::mbar_arrive_expect_tx(&sm.k_full[st], tile_bytes<D>());
-            tma_tile(sm.k[st], &a.tk, a.kv_rows_inner, &sm.k_full[st], map_row(si, kt * kTile), g, si.b,
+            ptx::mbar_arrive_expect_tx(&sm.k_full[kst], tile_bytes<D>());
+            tma_tile(sm.k[kst], &a.tk, a.kv_rows_inner, &sm.k_full[kst], map_row(si, kt * kTile), g, si.b,
                      kHalfTileBytes, D / 64);
-            ptx::mbar_arrive_expect_tx(&sm.v_full[st], tile_bytes<D>());
-            tma_tile(sm.v[st], &a.tv, a.kv_rows_inner, &sm.v_full[st], map_row(si, kt * kTile), g, si.b,
+            ptx::mbar_arrive_expect_tx(&sm.v_full[vst], tile_bytes<D>());
+            tma_tile(sm.v[vst], &a.tv, a.kv_rows_inner, &sm.v_full[vst], map_row(si, kt * kTile), g, si.b,
                      kHalfTileBytes, D / 64);
           }
-          last_kv_phase[st] = (int)ph;
+          last_k_phase[kst] = (int)kph;
+          last_v_phase[vst] = (int)vph;
           ++n_kv;
         }
       }
@@ -215,11 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
     // wait for this warp's own copies before the CTA may exit
     if (lane == 0) {
       if (last_qd_phase >= 0) W.drain(&sm.qd_full, (uint32_t)last_qd_phase);
-      for (int s = 0; s < kStages; ++s)
-        if (last_kv_phase[s] >= 0) {
-          W.drain(&sm.k_full[s], (uint32_t)last_kv_phase[s]);
-          W.drain(&sm.v_full[s], (uint32_t)last_kv_phase[s]);
-        }
+      for (int s = 0; s < kKStages; ++s)
+        if (last_k_phase[s] >= 0) W.drain(&sm.k_full[s], (uint32_t)last_k_phase[s]);
+      for (int s = 0; s < kVStages; ++s)
+        if (last_v_phase[s] >= 0) W.drain(&sm.v_full[s], (uint32_t)last_v_phase[s]);
     }
   } else if (warp == 9) {
     // ================================================================ MMA issuer
@@ -275,9 +282,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
         int kt, bits, act = 0, prev_st = 0;
         while (t.next(kt, bits)) {
           if (!((bits >> (4 * q)) & 0xF)) continue;
-          const int st = n_kv % kStages;
-          const uint32_t ph = (n_kv / kStages) & 1;
-          if (!W.warp(&sm.k_full[st], ph) || !W.warp(&sm.v_full[st], ph)) { ok = false; break; }
+          const int st = n_kv % kKStages, vst = n_kv % kVStages;
+          if (!W.warp(&sm.k_full[st], (n_kv / kKStages) & 1) || !W.warp(&sm.v_full[vst], (n_kv / kVStages) & 1)) {
+            ok = false;
+            break;
+          }
           ++n_kv;
           if (act == 0) {  // Q and dO of this query tile
             if (!W.warp(&sm.qd_full, n_qd & 1)) { ok = false; break; }
@@ -286,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
           // S and dP of the previous tile have been read by the compute warps
           if (n_sdp > 0 && !W.warp(&sm.sdp_free, (n_sdp - 1) & 1)) { ok = false; break; }
           ptx::tc_fence_after();
-          const uint32_t k_addr = ptx::smem_u32(sm.k[st]), v_addr = ptx::smem_u32(sm.v[st]);
+          const uint32_t k_addr = ptx::smem_u32(sm.k[st]), v_addr = ptx::smem_u32(sm.v[vst]);
           if (ptx::elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -301,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_tc_dq(const __grid_constant__ D
                           ptx::sdesc_sw128(v_addr + off, 16, 1024), idesc_ss, kk > 0 ? 1u : 0u);
             }
             ptx::mma_commit(&sm.sdp_full);
-            ptx::mma_commit(&sm.v_empty[st]);
+            ptx::mma_commit(&sm.v_empty[vst]);
             if (act == n_act - 1) ptx::mma_commit(&sm.qd_empty);
           }
           __syncwarp();
