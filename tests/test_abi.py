@@ -273,3 +273,34 @@ def test_head_dim_256_accepted(lib):
     assert det == _lib.ATTN_ERR_UNSUPPORTED
     p = params(D=512)
     assert fwd(lib, p) == _lib.ATTN_ERR_UNSUPPORTED and b"256" in lib.attn_last_error()
+
+
+def test_workspace_sizes_cover_the_float32_buffers(lib):
+    """The workspace queries are host arithmetic and need no GPU.  The backward's
+    workspace holds at least the float32 dQ accumulator (one float per element
+    of Q) and D (one float per query row).  With few forward units the forward
+    splits each unit's key range; every part then keeps float32 O and its row
+    max and sum per query row, so the forward's workspace holds at least two
+    parts of them."""
+    def sizes(**kw):
+        p = params(**kw)
+        return lib.attn_fwd_workspace_size(ctypes.byref(p)), lib.attn_bwd_workspace_size(ctypes.byref(p))
+
+    for mask in (_lib.ATTN_MASK_NONE, _lib.ATTN_MASK_CAUSAL):
+        rows = 2 * 16 * 8192
+        nf, nb = sizes(B=2, Hq=16, Hkv=16, S=8192, D=128, mask=mask)
+        assert nb >= rows * 128 * 4 + rows * 4
+        assert 0 < nf < nb  # 1024 units: no split, only the work list
+    # 64 two-tile units over 64 key tiles: the key range is split in two
+    rows = 2 * 8192
+    nf, nb = sizes(B=1, Hq=2, Hkv=2, S=8192, D=128, mask=_lib.ATTN_MASK_NONE)
+    assert nf >= 2 * rows * (128 + 2) * 4
+    assert nb >= rows * 128 * 4 + rows * 4
+    # float32 I/O at head dim 64 keeps the same accumulator
+    rows = 1 * 4 * 1000
+    nf, nb = sizes(B=1, Hq=4, Hkv=4, S=1000, D=64, dtype=_lib.ATTN_F32, mask=_lib.ATTN_MASK_NONE)
+    assert nb >= rows * 64 * 4 + rows * 4
+    # more positions never need less
+    small = sizes(B=1, Hq=4, Hkv=2, S=2048, D=128)
+    large = sizes(B=1, Hq=4, Hkv=2, S=4096, D=128)
+    assert large[1] > small[1]
